@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark of the BitLinear W1.58A8 hot path on GB300.
+
+Headline workload (BitNet-3B decode, M = 1 token): one step is the FFN's three
+BitLinear calls of one token, exactly as a decode step runs them:
+    act_quant(x_a [1, 2560])                   (shared by gate and up)
+    forward(gate 2560 -> 10240), forward(up 2560 -> 10240)
+    act_quant(x_b [1, 10240])
+    forward(down 10240 -> 2560)
+i.e. 19,660,800 packed weight bytes per step.  Inputs are seeded synthetic
+tensors (weights ~ N(0, 0.02), activations ~ N(0, 1) with 1% of channels x20).
+Each step uses the next of R copies of the packed weights (R * 19.7 MB > 4x
+L2), so every weight byte comes from HBM.  Steps run as CUDA graphs with
+programmatic dependent launch between kernels.
+
+Metric: packed-weight GB/s (1e9 B/s) over the whole job.  One JSON line on
+rank 0.  `--impl reference` times the CPU oracle on the same workload instead.
+Multi-GPU (torchrun): independent replicas, one per GPU (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W1.58A8 BitLinear: packed-weight GB/s at M=1 (%HBM peak); int8 TOPS at M=2048"
+UNIT = "GB/s"
+WORKLOAD = "bitnet3b_ffn_decode_m1"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="bound of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--no-pdl", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Workload definition (shapes and seeds of the BitNet-3B decode GEMV)
+# ---------------------------------------------------------------------------
+def workload_inputs():
+    from bitlinear_w1_a8_gb300 import synth
+    s = synth.SEEDS["decode"]
+    D, F = synth.DIM_3B, synth.FFN_3B
+    W_up_shape = synth.weight(F, D, s["W_up_shape"])       # gate and up: 2560 -> 10240
+    W_down_shape = synth.weight(D, F, s["W_down_shape"])   # down: 10240 -> 2560
+    x_a = synth.activations(1, D, s["x"], outlier_seed=s["outliers"])
+    x_b = synth.activations(1, F, s["x"], outlier_seed=s["outliers"])
+    return dict(D=D, F=F, W_up_shape=W_up_shape, W_down_shape=W_down_shape, x_a=x_a, x_b=x_b)
+
+
+def step_packed_bytes(D, F):
+    return 3 * (D * F // 4)
+
+
+# ---------------------------------------------------------------------------
+# Reference arm and CPU baseline: the oracle, as it stands, on host cores.
+# ---------------------------------------------------------------------------
+class OracleStep:
+    """One decode step computed by the CPU oracle (single-threaded C)."""
+
+    def __init__(self, inp, row_fraction: float = 1.0):
+        import oracle
+        self.o = oracle
+        D, F = inp["D"], inp["F"]
+        Wq_u, self.sw_u, _ = oracle.weight_quant(inp["W_up_shape"].numpy())
+        Wq_d, self.sw_d, _ = oracle.weight_quant(inp["W_down_shape"].numpy())
+        # a step may process a leading fraction of the output rows (bounded sample)
+        self.nu = max(1, int(F * row_fraction))
+        self.nd = max(1, int(D * row_fraction))
+        self.p_u = oracle.pack(Wq_u[: self.nu])
+        self.p_d = oracle.pack(Wq_d[: self.nd])
+        self.x_a, self.x_b = inp["x_a"].numpy(), inp["x_b"].numpy()
+        self.D, self.F = D, F
+        self.bytes = 2 * self.p_u.size + self.p_d.size
+
+    def run(self):
+        o = self.o
+        xq, sx = o.act_quant(self.x_a)
+        o.forward(xq, sx, self.p_u, self.sw_u, self.nu, self.D)   # gate
+        o.forward(xq, sx, self.p_u, self.sw_u, self.nu, self.D)   # up
+        xq, sx = o.act_quant(self.x_b)
+        o.forward(xq, sx, self.p_d, self.sw_d, self.nd, self.F)   # down
+
+
+def cpu_baseline(inp, seconds: float):
+    step = OracleStep(inp)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        step.run()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 10000:
+            break
+    return {"value": round(step.bytes * n / el / 1e9, 6), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} full decode steps (act_quant x2 + gate/up/down forwards over "
+                      f"{step.bytes} packed bytes each) in {el:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args, rank, world):
+    """The oracle, as it stands, timed on host cores (rank 0 only).  Each step is
+    a bounded sample of the decode step: both act_quant calls and the three
+    forwards over the leading fraction of the output rows, the fraction chosen
+    so that the whole run takes about a minute whatever --steps is."""
+    if rank != 0:
+        return 0
+    inp = workload_inputs()
+    probe = OracleStep(inp, row_fraction=1.0 / 64)
+    t0 = time.perf_counter()
+    probe.run()
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    budget = 60.0 / max(1, args.steps + min(max(args.warmup, 0), 3))
+    frac = min(1.0, max(1.0 / inp["F"], budget / (t_probe * 64)))
+    step = OracleStep(inp, row_fraction=frac)
+    warm = min(max(args.warmup, 0), 3)
+    for _ in range(warm):
+        step.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step.run()
+    el = time.perf_counter() - t0
+    value = step.bytes * args.steps / el / 1e9
+    sample = (f"{args.steps} steps, each act_quant x2 + gate/up/down over the first "
+              f"{frac:.4%} of output rows ({step.bytes} packed bytes), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": warm,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "sample_row_fraction": round(frac, 6)},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_sources, profile_name):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    h = hashlib.sha256()
+    for src in kernel_sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != digest:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+DECODE_SOURCES = ["bitlinear_w1_a8_gb300/csrc/decode.cu", "bitlinear_w1_a8_gb300/csrc/common.cuh"]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import bitlinear_w1_a8_gb300 as bl
+    from bitlinear_w1_a8_gb300 import build as blbuild
+
+    if not os.path.exists(bl.library_path()):
+        blbuild.build()
+    bl.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp = workload_inputs()
+    D, F = inp["D"], inp["F"]
+    bytes_u = bl.bitlinear_packed_bytes(F, D)
+    bytes_d = bl.bitlinear_packed_bytes(D, F)
+    per_step = 2 * bytes_u + bytes_d
+    R = max(8, -(-4 * L2_BYTES // per_step))          # copies so that R * step > 4x L2
+    R = 1 << (R - 1).bit_length()                       # 32 for the 3B shapes
+
+    # Quantise once, then replicate the packed bytes into R slots (distinct memory).
+    pu = torch.empty(bytes_u, dtype=torch.uint8, device=dev)
+    pd = torch.empty(bytes_d, dtype=torch.uint8, device=dev)
+    sw = torch.empty(2, dtype=torch.float32, device=dev)
+    ws = torch.empty(bl.bitlinear_quantize_weights_workspace(F, D), dtype=torch.uint8, device=dev)
+    bl.bitlinear_quantize_weights(inp["W_up_shape"].to(dev), pu, sw[0:1], ws)
+    bl.bitlinear_quantize_weights(inp["W_down_shape"].to(dev), pd, sw[1:2], ws)
+    slots = []
+    for _ in range(R):
+        slots.append((pu.clone(), pu.clone(), pd.clone()))
+    sw_u, sw_d = sw[0:1], sw[1:2]
+    x_a = inp["x_a"].to(dev)
+    x_b = inp["x_b"].to(dev)
+    xq_a = torch.empty(1, D, dtype=torch.int8, device=dev)
+    xq_b = torch.empty(1, F, dtype=torch.int8, device=dev)
+    sx_a = torch.empty(1, dtype=torch.float32, device=dev)
+    sx_b = torch.empty(1, dtype=torch.float32, device=dev)
+    y_g = torch.empty(1, F, dtype=torch.float32, device=dev)
+    y_u = torch.empty(1, F, dtype=torch.float32, device=dev)
+    y_d = torch.empty(1, D, dtype=torch.float32, device=dev)
+    flags = 0 if args.no_pdl else bl.FLAG_PDL
+
+    def step(i, stream):
+        g, u, d = slots[i % R]
+        bl.bitlinear_quant_act(x_a, xq_a, sx_a, stream=stream)
+        bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=stream)
+        bl.bitlinear_forward_ex(xq_a, sx_a, u, sw_u, F, y_u, flags=flags, stream=stream)
+        bl.bitlinear_quant_act(x_b, xq_b, sx_b, stream=stream)
+        bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=stream)
+
+    kernels_per_step = 5
+    stream = torch.cuda.Stream(device=dev)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(0, stream)  # settle any lazy initialisation outside the capture
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fn(i, stream)
+        return g
+
+    # One graph = one full rotation of R steps; K steps = K // R launches + a remainder graph.
+    g_full = capture(step, R)
+    rem = args.steps % R
+    g_rem = capture(step, rem) if rem else None
+
+    def run_steps(k):
+        with torch.cuda.stream(stream):
+            for _ in range(k // R):
+                g_full.replay()
+            if k % R:
+                if k % R == rem and g_rem is not None:
+                    g_rem.replay()
+                else:
+                    for i in range(k % R):
+                        step(i, stream)
+
+    # warm-up
+    run_steps(max(3, args.warmup))
+    torch.cuda.synchronize(dev)
+
+    # timed region
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in visible.split(",") if v.strip()]
+    smi_id = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+    sampler = ClockSampler(smi_id) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    run_steps(args.steps)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    total_bytes = per_step * args.steps * world
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+
+    # Dominant kernel alone: back-to-back forward launches over the rotation.
+    def fwd_only(i, s):
+        g, u, d = slots[i % R]
+        bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=s)
+        bl.bitlinear_forward_ex(xq_a, sx_a, u, sw_u, F, y_u, flags=flags, stream=s)
+        bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=s)
+
+    g_fwd = capture(fwd_only, R)
+    reps = max(3, min(200, args.steps // R))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_fwd.replay()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_fwd.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_launches = reps * 3 * R
+    fwd_ms = e0.elapsed_time(e1) / fwd_launches
+    # algorithmic bytes per forward launch (average over the three launches of a step):
+    # packed weights + int8 activations + one fp32 scale + fp32 outputs
+    alg_bytes = (2 * (bytes_u + D + 4 + 4 * F) + (bytes_d + F + 4 + 4 * D)) / 3.0
+    peak, peak_src = measured_peak_hbm()
+    achieved = alg_bytes / (fwd_ms * 1e-3) / 1e9
+
+    # End to end through the public API: pinned host inputs in, host outputs out.
+    e2e_steps = max(10, min(args.e2e_steps, args.steps))
+    h_xa = inp["x_a"].pin_memory()
+    h_xb = inp["x_b"].pin_memory()
+    h_yg = torch.empty(1, F, dtype=torch.float32).pin_memory()
+    h_yu = torch.empty(1, F, dtype=torch.float32).pin_memory()
+    h_yd = torch.empty(1, D, dtype=torch.float32).pin_memory()
+
+    def e2e_step(i):
+        g, u, d = slots[i % R]
+        x_a.copy_(h_xa, non_blocking=True)
+        x_b.copy_(h_xb, non_blocking=True)
+        bl.bitlinear_quant_act(x_a, xq_a, sx_a)
+        bl.bitlinear_forward(xq_a, sx_a, g, sw_u, F, y_g)
+        bl.bitlinear_forward(xq_a, sx_a, u, sw_u, F, y_u)
+        bl.bitlinear_quant_act(x_b, xq_b, sx_b)
+        bl.bitlinear_forward(xq_b, sx_b, d, sw_d, D, y_d)
+        h_yg.copy_(y_g, non_blocking=True)
+        h_yu.copy_(y_u, non_blocking=True)
+        h_yd.copy_(y_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        q1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = q0.elapsed_time(q1)
+    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = per_step * e2e_steps * world / (float(te.item()) * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {
+                "workload": WORKLOAD, "M": 1,
+                "matrices_per_step": {"gate": [F, D], "up": [F, D], "down": [D, F]},
+                "packed_bytes_per_step": per_step, "weight_copies": R,
+                "l2": f"inputs larger than L2: {R} rotating weight copies, "
+                      f"{R * per_step / 1e6:.0f} MB > 4x {L2_BYTES / 1e6:.0f} MB",
+                "cuda_graph": True, "pdl": not args.no_pdl, "parallelism": f"replicas{world}",
+            },
+            "roofline": {
+                "kernel": "decode_kernel<1> (bitlinear_forward, M=1)", "bound": "hbm",
+                "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(DECODE_SOURCES, "decode_m1_bitnet3b_ncu.txt"),
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": round(alg_bytes, 1),
+                "avg_launch_us": round(fwd_ms * 1e3, 4),
+                "timing": f"{fwd_launches} back-to-back launches in CUDA graphs (PDL), CUDA events",
+            },
+            "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
+                    "h2d_bytes_per_step": 4 * (D + F), "d2h_bytes_per_step": 4 * (2 * F + D),
+                    "steps": e2e_steps,
+                    "note": "eager calls through the Python binding of the C ABI; pinned host "
+                            "inputs copied in and outputs copied out every step"},
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clocks,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

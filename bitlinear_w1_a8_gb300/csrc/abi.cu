@@ -1,0 +1,177 @@
+// abi.cu -- the extern "C" entry points: argument checks, device discovery and
+// dispatch to the kernel launchers.  Nothing here allocates device memory.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace bitlinear {
+namespace {
+
+// One status word per device: kernels record a timed-out bounded wait here.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_devs[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+bitlinear_status current_device(DeviceInfo* out) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  if (d < 0 || d >= kMaxDevices) return BITLINEAR_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[d]) {
+    DeviceInfo info = {};
+    info.device = d;
+    int smem = 0;
+    if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess) {
+      return BITLINEAR_ERR_CUDA;
+    }
+    info.smem_optin = (size_t)smem;
+    // The kernels are built for sm_103a only.
+    if (info.cc_major != 10 || info.cc_minor != 3) return BITLINEAR_ERR_UNSUPPORTED;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    info.status = static_cast<int*>(addr);
+    g_devs[d] = info;
+    g_dev_ready[d] = true;
+  }
+  *out = g_devs[d];
+  return BITLINEAR_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bitlinear_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA; }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+bitlinear_status check_nk(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return BITLINEAR_ERR_SHAPE;
+  if (K % 64 != 0) return BITLINEAR_ERR_SHAPE;
+  if (N * K >= ((int64_t)1 << 40)) return BITLINEAR_ERR_SHAPE;
+  return BITLINEAR_OK;
+}
+
+}  // namespace
+}  // namespace bitlinear
+
+using namespace bitlinear;
+
+extern "C" {
+
+int bitlinear_abi_version(void) { return 1; }
+
+const char* bitlinear_status_string(bitlinear_status s) {
+  switch (s) {
+    case BITLINEAR_OK: return "BITLINEAR_OK";
+    case BITLINEAR_ERR_NULL: return "BITLINEAR_ERR_NULL: a required pointer is NULL";
+    case BITLINEAR_ERR_SHAPE: return "BITLINEAR_ERR_SHAPE: invalid M, N or K";
+    case BITLINEAR_ERR_ALIGN: return "BITLINEAR_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case BITLINEAR_ERR_UNSUPPORTED: return "BITLINEAR_ERR_UNSUPPORTED: unsupported device, algorithm or flag";
+    case BITLINEAR_ERR_CUDA: return "BITLINEAR_ERR_CUDA: a CUDA call failed";
+    case BITLINEAR_ERR_TIMEOUT: return "BITLINEAR_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+    case BITLINEAR_ERR_WORKSPACE: return "BITLINEAR_ERR_WORKSPACE: workspace missing or too small";
+    default: return "BITLINEAR_ERR_UNKNOWN";
+  }
+}
+
+size_t bitlinear_packed_bytes(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0) return 0;
+  return (size_t)N * (size_t)((K + 63) / 64) * 16u;
+}
+
+size_t bitlinear_quantize_weights_workspace(int64_t N, int64_t K) {
+  (void)N;
+  (void)K;
+  return 4096;
+}
+
+bitlinear_status bitlinear_quantize_weights(const float* W, int64_t N, int64_t K, uint8_t* packed,
+                                            float* w_scale, void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  if (!W || !packed || !w_scale) return BITLINEAR_ERR_NULL;
+  bitlinear_status st = check_nk(N, K);
+  if (st != BITLINEAR_OK) return st;
+  if (!workspace || workspace_bytes < bitlinear_quantize_weights_workspace(N, K))
+    return BITLINEAR_ERR_WORKSPACE;
+  if (!aligned16(W) || !aligned16(packed) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(w_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  return from_cuda(launch_weight_quant(W, N, K, packed, w_scale,
+                                       static_cast<unsigned long long*>(workspace), dev,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M, int64_t K,
+                                     const float* rms_weight, double rms_eps, int8_t* xq,
+                                     float* x_scale, void* stream) {
+  if (!x || !xq || !x_scale) return BITLINEAR_ERR_NULL;
+  if (M < 0 || M > kMaxDim || K <= 0 || K % 64 != 0 || K > 32768) return BITLINEAR_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(xq) || (mul && !aligned16(mul)) ||
+      (rms_weight && !aligned16(rms_weight)) || (reinterpret_cast<uintptr_t>(x_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  if (rms_weight && !(rms_eps >= 0.0)) return BITLINEAR_ERR_SHAPE;
+  if (M == 0) return BITLINEAR_OK;
+  DeviceInfo dev;
+  bitlinear_status st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  return from_cuda(launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, int64_t M,
+                                      const uint8_t* packed, const float* w_scale, int64_t N,
+                                      int64_t K, float* y, int32_t* acc, int algo, int flags,
+                                      void* stream) {
+  if (!xq || !x_scale || !packed || !w_scale || !y) return BITLINEAR_ERR_NULL;
+  bitlinear_status st = check_nk(N, K);
+  if (st != BITLINEAR_OK) return st;
+  if (M < 0 || M > kMaxDim) return BITLINEAR_ERR_SHAPE;
+  if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) || (acc && !aligned16(acc)) ||
+      (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
+  if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL)
+    return BITLINEAR_ERR_UNSUPPORTED;
+  if (M == 0) return BITLINEAR_OK;
+  if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_SHAPE;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The tensor-core path is not built yet: every algorithm runs the decode kernel.
+  return from_cuda(launch_decode(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+}
+
+bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
+                                   const uint8_t* packed, const float* w_scale, int64_t N,
+                                   int64_t K, float* y, int32_t* acc, void* stream) {
+  return bitlinear_forward_ex(xq, x_scale, M, packed, w_scale, N, K, y, acc,
+                              BITLINEAR_ALGO_AUTO, 0, stream);
+}
+
+bitlinear_status bitlinear_device_status(void* stream, int clear) {
+  DeviceInfo dev;
+  bitlinear_status st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, dev.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BITLINEAR_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return BITLINEAR_ERR_CUDA;
+  }
+  return word != 0 ? BITLINEAR_ERR_TIMEOUT : BITLINEAR_OK;
+}
+
+}  // extern "C"

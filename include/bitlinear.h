@@ -1,0 +1,173 @@
+/*
+ * bitlinear.h -- C ABI of the GB300 (sm_103a) BitLinear W1.58A8 library.
+ *
+ * BitLinear is the layer that replaces every nn.Linear of a BitNet b1.58
+ * transformer (q, k, v, o and the FFN gate, up, down projections; "Add
+ * Support for BitNet Architecture Inference", Candle PR, list of changes made:
+ * "Replace Linear with BitLinear in MLP and Attention", with an RMSNorm before
+ * each BitLinear and the activation_quant / weight_quant pair of the BitNet
+ * paper).  The layer computes
+ *
+ *   weight_quant (absmean, once per matrix, offline):
+ *       sw = 1 / max(mean|W|, 1e-5),   Wq = clamp(round_half_even(W*sw), -1, 1)
+ *   activation_quant (absmax, per token row):
+ *       sx = 127 / max(max_k |x|, 1e-5), xq = clamp(round_half_even(x*sx), -128, 127)
+ *   contraction and rescale:
+ *       acc[m,n] = sum_k xq[m,k] * Wq[n,k]   (exact int32)
+ *       y[m,n]   = acc[m,n] / (sx[m] * sw)   (fp32: one product, one division)
+ *
+ * Shapes: W is [N, K] fp32 row-major (out features x in features), x is
+ * [M, K] fp32 row-major (M tokens), y is [M, N] fp32 row-major.
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers named "device" are CUDA device pointers on the current
+ *    device; the caller allocates and owns every buffer.  No entry point keeps
+ *    a pointer after it returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    only enqueues work: results are ready when the stream reaches them.
+ *  - Argument errors are reported synchronously, before anything is enqueued:
+ *    a NULL required pointer, a non-positive N or K, a negative M, K not a
+ *    multiple of 64, a pointer not aligned to 16 bytes, or a too small
+ *    workspace.  M == 0 is a valid empty batch and enqueues nothing.
+ *  - A failed launch returns BITLINEAR_ERR_CUDA.  Every wait inside a kernel
+ *    is bounded; a wait that runs out records BITLINEAR_ERR_TIMEOUT in a
+ *    per-device status word that bitlinear_device_status() reports.
+ *  - Non-finite inputs (Inf, NaN) give unspecified outputs.
+ *  - Rounding: every quantisation decision is taken in IEEE fp32 with
+ *    round-to-nearest-even and no fused multiply-add; the sums that feed the
+ *    scales (sum|W| and the RMSNorm sum of squares) are exact, then rounded
+ *    once to fp64, so results do not depend on launch shape or timing.
+ *
+ * Packed weight layout (this library's own 2-bit format; 0.25 byte per
+ * weight, the figure of the pages' memory tables):
+ *  - code = Wq + 1 in {0, 1, 2}; code 3 never occurs; weights past K (none
+ *    while K % 64 == 0) would hold code 1.
+ *  - The 16-byte chunk of row n and k-block kb = k / 64 starts at byte
+ *    (kb * N + n) * 16, so one k-block of all rows is contiguous.
+ *  - Inside a chunk, little-endian 32-bit word w = (k % 64) / 16 holds
+ *    i = k % 16 at bit 8*(i%4) + 2*(i/4): (word >> 2j) & 0x03030303 gives the
+ *    codes of k = 16w+4j .. 16w+4j+3 in bytes 0..3.
+ */
+#ifndef BITLINEAR_H
+#define BITLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int bitlinear_status;
+
+enum {
+  BITLINEAR_OK = 0,
+  BITLINEAR_ERR_NULL = -1,        /* a required pointer is NULL */
+  BITLINEAR_ERR_SHAPE = -2,       /* N or K <= 0, M < 0, K % 64 != 0, size overflow */
+  BITLINEAR_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  BITLINEAR_ERR_UNSUPPORTED = -4, /* no sm_103 device, or an unknown algorithm / flag */
+  BITLINEAR_ERR_CUDA = -5,        /* a CUDA runtime call or a launch failed */
+  BITLINEAR_ERR_TIMEOUT = -6,     /* a bounded wait inside a kernel ran out */
+  BITLINEAR_ERR_WORKSPACE = -7    /* workspace NULL or smaller than required */
+};
+
+/* Version of this ABI (increments on any incompatible change). */
+int bitlinear_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* bitlinear_status_string(bitlinear_status status);
+
+/* Bytes of the packed layout for an [N, K] matrix: N * ceil(K/64) * 16
+ * (0 if N or K is not positive). */
+size_t bitlinear_packed_bytes(int64_t N, int64_t K);
+
+/* Workspace bytes bitlinear_quantize_weights needs (a constant 4096 today:
+ * 256 per-exponent bucket sums of 8 bytes, plus room). */
+size_t bitlinear_quantize_weights_workspace(int64_t N, int64_t K);
+
+/*
+ * weight_quant + pack (absmean ternary quantiser; one fp32 scale per matrix).
+ *   W          device, fp32 [N, K] row-major, read only.
+ *   N, K       N > 0, K > 0, K % 64 == 0, N*K < 2^40.
+ *   packed     device, bitlinear_packed_bytes(N, K) bytes, written.
+ *   w_scale    device, 1 fp32, receives sw = 1 / max(mean|W|, 1e-5).
+ *   workspace  device, >= bitlinear_quantize_weights_workspace(N, K) bytes,
+ *              16-byte aligned; its contents on entry do not matter and are
+ *              overwritten (it is cleared on the stream first).
+ * Three kernels: an exact per-exponent sum of |W|, a one-warp finalisation of
+ * mean and sw, and the quantise-and-pack pass.
+ */
+bitlinear_status bitlinear_quantize_weights(const float* W, int64_t N, int64_t K,
+                                            uint8_t* packed, float* w_scale,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/*
+ * activation_quant with optional fused prologues, one kernel, one CTA per row.
+ *   x           device, fp32 [M, K] row-major.
+ *   mul         device fp32 [M, K] or NULL.  When given, the row fed to the
+ *               quantiser is h = (r*r)*mul with r = max(x, 0) (the ReLU^2
+ *               gating of the BitNet FFN, "Transformer Block" page, section
+ *               "Feed-Forward Network"); x is then the gate projection.
+ *   rms_weight  device fp32 [K] (gamma) or NULL.  When given, h is first
+ *               normalised: inv = 1/sqrt(sum_k h_k^2 / K + rms_eps) computed in
+ *               fp64 from the exact sum, rounded to fp32, then
+ *               h_k = (h_k * inv) * gamma_k in fp32 (an RMSNorm before the
+ *               BitLinear; the gating, when present, comes first).
+ *   rms_eps     the RMSNorm epsilon (ignored without rms_weight), >= 0.
+ *   xq          device, int8 [M, K] row-major, written.
+ *   x_scale     device, fp32 [M], receives sx per row.
+ * K % 64 == 0 and K <= 65536 (the exact sum of squares holds 2^16 terms).
+ */
+bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M, int64_t K,
+                                     const float* rms_weight, double rms_eps,
+                                     int8_t* xq, float* x_scale, void* stream);
+
+/*
+ * Contraction + rescale: y = (xq . Wq^T) / (sx * sw).
+ *   xq, x_scale   device, from bitlinear_quant_act (int8 [M, K], fp32 [M]).
+ *   packed, w_scale  device, from bitlinear_quantize_weights for [N, K].
+ *   y             device, fp32 [M, N] row-major, written.
+ *   acc           device int32 [M, N] or NULL; when given it receives the raw
+ *                 integer accumulators (for checking and debugging).
+ * The kernel is chosen from M (BITLINEAR_ALGO_AUTO): the decode kernel
+ * (packed weights streamed through registers, dp4a on the 2-bit codes) for
+ * small M, the tcgen05 tensor-core kernel for large M.
+ */
+bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
+                                   const uint8_t* packed, const float* w_scale,
+                                   int64_t N, int64_t K, float* y, int32_t* acc,
+                                   void* stream);
+
+enum {
+  BITLINEAR_ALGO_AUTO = 0,
+  BITLINEAR_ALGO_DECODE = 1,   /* CUDA-core kernel, any M */
+  BITLINEAR_ALGO_PREFILL = 2   /* tcgen05 kernel, any M */
+};
+
+enum {
+  /* Launch with programmatic dependent launch: the kernel starts streaming
+   * the packed weights while the previous kernel on the stream (normally the
+   * bitlinear_quant_act that produced xq) is still running, and waits for it
+   * before touching xq / x_scale.  Only valid when `packed` and `w_scale` were
+   * NOT written by the kernel immediately before on the stream. */
+  BITLINEAR_FLAG_PDL = 1
+};
+
+/* bitlinear_forward with an explicit algorithm and flags (see above). */
+bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, int64_t M,
+                                      const uint8_t* packed, const float* w_scale,
+                                      int64_t N, int64_t K, float* y, int32_t* acc,
+                                      int algo, int flags, void* stream);
+
+/* Synchronises `stream`, then returns BITLINEAR_ERR_TIMEOUT if any kernel of
+ * this library recorded a timed-out wait on the current device since the last
+ * call with clear != 0, BITLINEAR_ERR_CUDA if the stream reports an error,
+ * else BITLINEAR_OK.  With clear != 0 the status word is reset. */
+bitlinear_status bitlinear_device_status(void* stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H */

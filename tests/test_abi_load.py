@@ -1,0 +1,83 @@
+"""The C-ABI library loads, exports every symbol include/bitlinear.h declares,
+and rejects bad arguments on the host before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bitlinear_w1_a8_gb300 as bl
+from bitlinear_w1_a8_gb300 import build as blbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "bitlinear.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bitlinear_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    blbuild.build()
+    return bl.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 9
+    assert sorted(bl.EXPORTED_SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_host_only_calls(lib):
+    assert bl.bitlinear_abi_version() == 1
+    assert bl.bitlinear_packed_bytes(10240, 2560) == 6553600
+    assert bl.bitlinear_packed_bytes(2560, 10240) == 6553600
+    assert bl.bitlinear_packed_bytes(50000, 2560) == 32000000
+    assert bl.bitlinear_packed_bytes(3, 65) == 96
+    assert bl.bitlinear_packed_bytes(0, 64) == 0
+    assert bl.bitlinear_quantize_weights_workspace(10240, 2560) >= 256 * 8
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert bl.bitlinear_status_string(code).startswith("BITLINEAR_")
+
+
+# Fake, never dereferenced device addresses: every call below must fail (or
+# return OK for an empty batch) during argument checking, before any CUDA call.
+A = 0x10000   # 16-byte aligned
+U = 0x10004   # misaligned
+
+
+def test_forward_argument_errors(lib):
+    f = lib.bitlinear_forward_ex
+    assert f(None, A, 1, A, A, 64, 64, A, None, 0, 0, None) == -1          # NULL xq
+    assert f(A, A, 1, A, A, 64, 100, A, None, 0, 0, None) == -2            # K % 64
+    assert f(A, A, 1, A, A, 0, 64, A, None, 0, 0, None) == -2              # N == 0
+    assert f(A, A, -1, A, A, 64, 64, A, None, 0, 0, None) == -2            # M < 0
+    assert f(U, A, 1, A, A, 64, 64, A, None, 0, 0, None) == -3             # misaligned xq
+    assert f(A, A, 1, A, A, 64, 64, U, None, 0, 0, None) == -3             # misaligned y
+    assert f(A, A, 1, A, A, 64, 64, A, None, 7, 0, None) == -4             # unknown algo
+    assert f(A, A, 1, A, A, 64, 64, A, None, 0, 8, None) == -4             # unknown flag
+    assert f(A, A, 0, A, A, 64, 64, A, None, 0, 0, None) == 0              # empty batch
+
+
+def test_quant_act_argument_errors(lib):
+    f = lib.bitlinear_quant_act
+    assert f(None, None, 1, 64, None, 1e-6, A, A, None) == -1
+    assert f(A, None, 1, 96, None, 1e-6, A, A, None) == -2                 # K % 64
+    assert f(A, None, 1, 65536, None, 1e-6, A, A, None) == -2              # K too large
+    assert f(A, U, 1, 64, None, 1e-6, A, A, None) == -3                    # misaligned mul
+    assert f(A, None, 1, 64, A, -1.0, A, A, None) == -2                    # negative eps
+    assert f(A, None, 0, 64, None, 1e-6, A, A, None) == 0                  # empty batch
+
+
+def test_quantize_weights_argument_errors(lib):
+    f = lib.bitlinear_quantize_weights
+    assert f(A, 4, 64, A, A, None, 4096, None) == -7                       # no workspace
+    assert f(A, 4, 64, A, A, A, 16, None) == -7                            # too small
+    assert f(A, 4, 60, A, A, A, 4096, None) == -2                          # K % 64
+    assert f(A, 1 << 21, 1 << 20, A, A, A, 4096, None) == -2               # N*K >= 2^40
+    assert f(U, 4, 64, A, A, A, 4096, None) == -3
+    assert f(None, 4, 64, A, A, A, 4096, None) == -1

@@ -1,0 +1,220 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Integer and byte results (packed weights, xq, acc) and the scales (sw, sx)
+must be identical; float outputs within 1e-5 relative error of the oracle's
+fp64 value.  Sizes span several CTAs and ragged tails; the full-size cases
+use the workloads' own shapes (BitNet-3B decode and prefill, BitNet-1.3B FFN).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bitlinear_w1_a8_gb300 as bl
+import oracle
+from bitlinear_w1_a8_gb300 import synth
+from harness import (Y_RTOL, full_parity, gpu_act_quant, gpu_forward, gpu_quantize_weights,
+                     max_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    bl.load_library()
+    torch.cuda.init()
+
+
+ALGOS = [bl.ALGO_DECODE, bl.ALGO_PREFILL]
+
+
+def test_small_bitlinear_m4_k256_n256():
+    """The small single-BitLinear workload: M=4, K=N=256, W seed 0, x seed 1."""
+    W = synth.weight(256, 256, synth.SEEDS["small"]["W"])
+    x = synth.activations(4, 256, synth.SEEDS["small"]["x"])
+    full_parity(W, x)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 64), (2, 1, 128), (1, 80, 64), (3, 300, 192), (5, 1000, 640), (8, 153, 128),
+    (17, 2000, 256), (64, 512, 512), (65, 100, 256), (130, 257, 320), (1, 50000, 128),
+])
+def test_shapes(algo, M, N, K):
+    W = synth.weight(N, K, 100 + N + K)
+    x = synth.activations(M, K, 200 + M + K, outlier_seed=300 + K)
+    full_parity(W, x, algo=algo)
+
+
+@pytest.mark.parametrize("M", [1, 4, 64])
+def test_pdl_flag(M):
+    W = synth.weight(2000, 640, 7)
+    x = synth.activations(M, 640, 8)
+    full_parity(W, x, algo=bl.ALGO_AUTO, flags=bl.FLAG_PDL)
+
+
+@pytest.mark.parametrize("M,K", [(1, 2048), (3, 2048), (7, 8192), (2, 64)])
+def test_prologues(M, K):
+    """ReLU^2 gating, RMSNorm, and both (gating first), bit-exact."""
+    g = synth.activations(M, K, 40 + K)
+    u = synth.activations(M, K, 41 + K)
+    gamma = synth.uniform((K,), 0.5, 1.5, 42 + K)
+    for mul, gm in ((u, None), (None, gamma), (u, gamma)):
+        xq_o, sx_o = oracle.act_quant(g.numpy(), mul=None if mul is None else mul.numpy(),
+                                      gamma=None if gm is None else gm.numpy(), eps=1e-6)
+        xq_g, sx_g, _ = gpu_act_quant(g, mul, gm, 1e-6)
+        np.testing.assert_array_equal(sx_g, sx_o)
+        np.testing.assert_array_equal(xq_g, xq_o)
+
+
+def test_edge_values():
+    """Zero rows, tiny rows (eps path), rounding ties, subnormals, huge values."""
+    K, N = 128, 96
+    x = torch.zeros(6, K)
+    x[1, :4] = torch.tensor([1e-6, -2e-6, 0.0, 3e-7])
+    x[2] = torch.linspace(-127, 127, K).round() + 0.5          # many .5 ties at sx = 127/127.5
+    x[3, 0], x[3, 1:9] = 127.0, torch.tensor([-63.5, 0.5, 1.5, 2.5, -0.5, -1.5, 126.5, 62.5])
+    x[4] = torch.tensor([1e-40, -3e-39] * (K // 2))            # subnormals only
+    x[5] = torch.tensor([3e38, -1e-3] * (K // 2))              # near fp32 max
+    W = synth.weight(N, K, 5)
+    W[0] = 0.0
+    W[1, :8] = torch.tensor([1e-41, -1e-42, 0.0, 1e-38, 3.0, -3.0, 0.01, -0.01])
+    full_parity(W, x)
+    full_parity(W, x, gamma=synth.uniform((K,), 0.5, 1.5, 6), eps=1e-6)
+
+
+def test_zero_weight_matrix_and_ties():
+    K = 64
+    W = torch.zeros(10, K)
+    full_parity(W, synth.activations(3, K, 9))
+    # mean|W| = 1 exactly: entries at +-0.5, +-1.5 are rounding ties
+    W = torch.tensor([[0.5, -0.5, 1.5, -1.5, 2.5, -2.5, 0.375, -0.625] * 8,
+                      [0.75] * 64], dtype=torch.float32)
+    r = full_parity(W, synth.activations(2, K, 10))
+    assert np.isfinite(r["y"]).all()
+
+
+def test_empty_batch_is_noop():
+    W = synth.weight(64, 64, 3)
+    _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+    xq = torch.empty(0, 64, dtype=torch.int8, device="cuda")
+    sx = torch.empty(0, dtype=torch.float32, device="cuda")
+    y = torch.empty(0, 64, dtype=torch.float32, device="cuda")
+    bl.bitlinear_forward(xq, sx, packed_d, sw_d, 64, y)
+    bl.bitlinear_quant_act(torch.empty(0, 64, device="cuda"), xq, sx)
+    assert bl.bitlinear_device_status() == 0
+
+
+def test_misaligned_pointer_rejected():
+    W = synth.weight(64, 64, 3)
+    _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+    buf = torch.zeros(64 * 2 + 16, dtype=torch.int8, device="cuda")
+    xq = buf[1:1 + 128].view(2, 64)  # 1-byte offset: not 16-byte aligned
+    sx = torch.ones(2, device="cuda")
+    y = torch.empty(2, 64, device="cuda")
+    with pytest.raises(bl.BitLinearError) as e:
+        bl.bitlinear_forward(xq, sx, packed_d, sw_d, 64, y)
+    assert e.value.status == -3
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads.
+# ---------------------------------------------------------------------------
+DECODE_SHAPES = [("up_shape", synth.FFN_3B, synth.DIM_3B, "W_up_shape"),
+                 ("down_shape", synth.DIM_3B, synth.FFN_3B, "W_down_shape")]
+
+
+@pytest.mark.parametrize("name,N,K,seed_key", DECODE_SHAPES, ids=[s[0] for s in DECODE_SHAPES])
+def test_decode_m1_full_size(name, N, K, seed_key):
+    """BitNet-3B decode GEMV, M=1, 1% outlier channels x20: every output checked."""
+    s = synth.SEEDS["decode"]
+    W = synth.weight(N, K, s[seed_key])
+    x = synth.activations(1, K, s["x"], outlier_seed=s["outliers"])
+    full_parity(W, x, flags=bl.FLAG_PDL)
+
+
+def _sampled_parity(W, x, rows, cols, algo):
+    """Whole GPU path at full size; the oracle computes the sampled outputs only."""
+    N, K = W.shape
+    Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+    packed_g, sw_g, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+    assert sw_g == sw_o
+    np.testing.assert_array_equal(packed_g, oracle.pack(Wq_o))
+    xq_o, sx_o = oracle.act_quant(x.numpy())
+    xq_g, sx_g, (xq_d, sx_d) = gpu_act_quant(x)
+    np.testing.assert_array_equal(xq_g, xq_o)
+    np.testing.assert_array_equal(sx_g, sx_o)
+    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=algo)
+    acc_o, y_o = oracle.forward(xq_o[rows], sx_o[rows], oracle.pack(Wq_o[cols]), sw_o, len(cols), K)
+    np.testing.assert_array_equal(acc_g[np.ix_(rows, cols)], acc_o)
+    assert max_rel_err(y_g[np.ix_(rows, cols)], y_o) <= Y_RTOL
+    return acc_g, y_g
+
+
+@pytest.mark.parametrize("name,N,K,seed", [("up_shape", synth.FFN_3B, synth.DIM_3B, "W_up_shape"),
+                                            ("down_shape", synth.DIM_3B, synth.FFN_3B, "W_down_shape")])
+def test_prefill_m2048_sampled(name, N, K, seed):
+    """BitNet-3B prefill GEMM, M=2048: sampled rows x columns against the oracle,
+    spread over every output tile, plus the last row and column."""
+    s = synth.SEEDS["prefill"]
+    W = synth.weight(N, K, s[seed])
+    x = synth.activations(2048, K, s["x"])
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(2048, 24, replace=False), [0, 127, 128, 2047]]))
+    cols = np.unique(np.concatenate([rng.choice(N, 160, replace=False), [0, 255, 256, N - 1]]))
+    _sampled_parity(W, x, rows, cols, bl.ALGO_AUTO)
+
+
+@pytest.mark.parametrize("M", [1, 512])
+def test_ffn_1b3_chain(M):
+    """BitNet-1.3B FFN sub-block: RMSNorm -> act_quant -> gate, up -> ReLU^2(gate)*up
+    -> sub-norm -> act_quant -> down.  Stage-wise bit-exact (the oracle is fed
+    the GPU's fp32 stage inputs), sampled columns at M = 512."""
+    s = synth.SEEDS["ffn_1b3"]
+    D, F = synth.DIM_1B3, synth.FFN_1B3
+    gamma = synth.uniform((D,), 0.5, 1.5, s["norm"])
+    gamma_sub = synth.uniform((F,), 0.5, 1.5, s["subnorm"])
+    Wg, Wu, Wd = synth.weight(F, D, s["gate"]), synth.weight(F, D, s["up"]), synth.weight(D, F, s["down"])
+    x = synth.activations(M, D, s["x"])
+    rng = np.random.default_rng(1)
+    cols_f = np.unique(rng.choice(F, 96 if M > 1 else F, replace=False))
+    cols_d = np.unique(rng.choice(D, 96 if M > 1 else D, replace=False))
+    rows = np.arange(M) if M <= 4 else np.unique(rng.choice(M, 12, replace=False))
+
+    # stage 1: normed activations shared by gate and up
+    xq_o, sx_o = oracle.act_quant(x.numpy(), gamma=gamma.numpy(), eps=1e-6)
+    xq_g, sx_g, (xq_d, sx_d) = gpu_act_quant(x, None, gamma, 1e-6)
+    np.testing.assert_array_equal(xq_g, xq_o)
+    np.testing.assert_array_equal(sx_g, sx_o)
+    outs = {}
+    for name, W in (("gate", Wg), ("up", Wu)):
+        Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+        packed_g, sw_g, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        assert sw_g == sw_o
+        acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, F)
+        acc_o, y_o = oracle.forward(xq_o[rows], sx_o[rows], oracle.pack(Wq_o[cols_f]), sw_o,
+                                    len(cols_f), D)
+        np.testing.assert_array_equal(acc_g[np.ix_(rows, cols_f)], acc_o)
+        assert max_rel_err(y_g[np.ix_(rows, cols_f)], y_o) <= Y_RTOL
+        outs[name] = torch.from_numpy(y_g)
+    # stage 2: gating + sub-norm + act_quant, fed the GPU's fp32 gate/up outputs
+    h_q_o, h_sx_o = oracle.act_quant(outs["gate"].numpy(), mul=outs["up"].numpy(),
+                                     gamma=gamma_sub.numpy(), eps=1e-6)
+    h_q_g, h_sx_g, (hq_d, hsx_d) = gpu_act_quant(outs["gate"], outs["up"], gamma_sub, 1e-6)
+    np.testing.assert_array_equal(h_q_g, h_q_o)
+    np.testing.assert_array_equal(h_sx_g, h_sx_o)
+    # stage 3: down projection
+    Wq_o, sw_o, _ = oracle.weight_quant(Wd.numpy())
+    _, sw_g, _, (packed_d, sw_d) = gpu_quantize_weights(Wd)
+    acc_g, y_g = gpu_forward(hq_d, hsx_d, packed_d, sw_d, D)
+    acc_o, y_o = oracle.forward(h_q_o[rows], h_sx_o[rows], oracle.pack(Wq_o[cols_d]), sw_o,
+                                len(cols_d), F)
+    np.testing.assert_array_equal(acc_g[np.ix_(rows, cols_d)], acc_o)
+    assert max_rel_err(y_g[np.ix_(rows, cols_d)], y_o) <= Y_RTOL
+
+
+def test_repeat_calls_are_deterministic():
+    W = synth.weight(3000, 1280, 12)
+    x = synth.activations(3, 1280, 13)
+    a = full_parity(W, x)
+    b = full_parity(W, x, flags=bl.FLAG_PDL)
+    np.testing.assert_array_equal(a["y"], b["y"])
