@@ -206,6 +206,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Whole-job aggregation over ranks (replicas): max time, summed work
+# ---------------------------------------------------------------------------
+def reduce_max_ms(ms: float, dist=None, device=None) -> float:
+    """The slowest rank's time (every rank must call it when dist is given)."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Aggregate throughput: every rank's bytes over the slowest rank's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 def measured_peak_hbm():
@@ -348,13 +366,8 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    total_bytes = per_step * args.steps * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
+    ms_max = reduce_max_ms(ev0.elapsed_time(ev1), dist, dev)
+    value = whole_job_gbs(per_step * args.steps, world, ms_max)
 
     # Dominant kernel alone: back-to-back forward launches over the rotation.
     def fwd_only(i, s):
@@ -419,11 +432,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(i)
         q1.record(stream)
         torch.cuda.synchronize(dev)
-    e2e_ms = q0.elapsed_time(q1)
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = per_step * e2e_steps * world / (float(te.item()) * 1e-3) / 1e9
+    e2e_value = whole_job_gbs(per_step * e2e_steps, world, reduce_max_ms(q0.elapsed_time(q1), dist, dev))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -48,6 +48,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bitlinear_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA; }
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
+// Decode kernel: activations of a token group are staged in shared memory.
+constexpr int64_t kDecodeMaxK = 65536;
+// Tensor-core kernel: the fp32 accumulator is exact while 127 * K < 2^24.
+constexpr int64_t kPrefillMaxK = 131072;
+// AUTO picks the decode kernel up to this many tokens.
+constexpr int64_t kDecodeMaxM = 64;
 
 bitlinear_status check_nk(int64_t N, int64_t K) {
   if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return BITLINEAR_ERR_SHAPE;
@@ -112,13 +118,13 @@ bitlinear_status bitlinear_quantize_weights(const float* W, int64_t N, int64_t K
 bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M, int64_t K,
                                      const float* rms_weight, double rms_eps, int8_t* xq,
                                      float* x_scale, void* stream) {
-  if (!x || !xq || !x_scale) return BITLINEAR_ERR_NULL;
   if (M < 0 || M > kMaxDim || K <= 0 || K % 64 != 0 || K > 32768) return BITLINEAR_ERR_SHAPE;
+  if (rms_weight && !(rms_eps >= 0.0)) return BITLINEAR_ERR_SHAPE;
+  if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
+  if (!x || !xq || !x_scale) return BITLINEAR_ERR_NULL;
   if (!aligned16(x) || !aligned16(xq) || (mul && !aligned16(mul)) ||
       (rms_weight && !aligned16(rms_weight)) || (reinterpret_cast<uintptr_t>(x_scale) & 3u))
     return BITLINEAR_ERR_ALIGN;
-  if (rms_weight && !(rms_eps >= 0.0)) return BITLINEAR_ERR_SHAPE;
-  if (M == 0) return BITLINEAR_OK;
   DeviceInfo dev;
   bitlinear_status st = current_device(&dev);
   if (st != BITLINEAR_OK) return st;
@@ -130,25 +136,32 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
                                       const uint8_t* packed, const float* w_scale, int64_t N,
                                       int64_t K, float* y, int32_t* acc, int algo, int flags,
                                       void* stream) {
-  if (!xq || !x_scale || !packed || !w_scale || !y) return BITLINEAR_ERR_NULL;
+  if (!packed || !w_scale) return BITLINEAR_ERR_NULL;
   bitlinear_status st = check_nk(N, K);
   if (st != BITLINEAR_OK) return st;
   if (M < 0 || M > kMaxDim) return BITLINEAR_ERR_SHAPE;
-  if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) || (acc && !aligned16(acc)) ||
-      (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
-    return BITLINEAR_ERR_ALIGN;
   if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
   if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL)
     return BITLINEAR_ERR_UNSUPPORTED;
-  if (M == 0) return BITLINEAR_OK;
-  if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_SHAPE;
+  if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
+  if (!xq || !x_scale || !y) return BITLINEAR_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) || (acc && !aligned16(acc)) ||
+      (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  int use = algo;
+  if (use == BITLINEAR_ALGO_AUTO) use = (M <= kDecodeMaxM && K <= kDecodeMaxK) ? BITLINEAR_ALGO_DECODE
+                                                                               : BITLINEAR_ALGO_PREFILL;
+  if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
+    return BITLINEAR_ERR_UNSUPPORTED;
+  if (use == BITLINEAR_ALGO_PREFILL && K > kPrefillMaxK) return BITLINEAR_ERR_UNSUPPORTED;
   DeviceInfo dev;
   st = current_device(&dev);
   if (st != BITLINEAR_OK) return st;
   const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The tensor-core path is not built yet: every algorithm runs the decode kernel.
-  return from_cuda(launch_decode(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+  if (use == BITLINEAR_ALGO_DECODE)
+    return from_cuda(launch_decode(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+  return from_cuda(launch_prefill(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
 }
 
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,

@@ -17,7 +17,8 @@
 namespace bitlinear {
 namespace {
 
-constexpr int kActThreads = 256;
+constexpr int kActThreadsMany = 256;   // many rows: several CTAs per SM
+constexpr int kActThreadsFew = 1024;   // few rows: one wide CTA per row for latency
 
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
@@ -37,8 +38,22 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
+// h = x, or h = (r*r)*u with r = max(x, 0) when the gating input u is given.
+__device__ __forceinline__ float4 gated(const float4* __restrict__ xr, const float4* __restrict__ ur, int i) {
+  const float4 g = xr[i];
+  if (!ur) return g;
+  const float4 u = ur[i];
+  float4 h;
+  float r;
+  r = fmaxf(g.x, 0.0f); h.x = __fmul_rn(__fmul_rn(r, r), u.x);
+  r = fmaxf(g.y, 0.0f); h.y = __fmul_rn(__fmul_rn(r, r), u.y);
+  r = fmaxf(g.z, 0.0f); h.z = __fmul_rn(__fmul_rn(r, r), u.z);
+  r = fmaxf(g.w, 0.0f); h.w = __fmul_rn(__fmul_rn(r, r), u.w);
+  return h;
+}
+
 // Dynamic shared memory: the K fp32 values of h for this row.
-__global__ void __launch_bounds__(kActThreads)
+__global__ void __launch_bounds__(kActThreadsFew, 1)
 act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int K,
                  const float* __restrict__ gamma, double eps, int8_t* __restrict__ xq,
                  float* __restrict__ sx) {
@@ -63,26 +78,17 @@ act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int
   }
 
   float amax = 0.0f;
-  // Pass 1: h (gated or plain) into shared memory; exact sum of squares or amax.
-  // Warp-uniform trip count so that every lane joins the bucket aggregation.
-  for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
-    const int i = base + (threadIdx.x & 31);
-    float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < K4) {
-      float4 g = xr[i];
-      if (ur) {
-        const float4 u = ur[i];
-        float r;
-        r = fmaxf(g.x, 0.0f); h.x = __fmul_rn(__fmul_rn(r, r), u.x);
-        r = fmaxf(g.y, 0.0f); h.y = __fmul_rn(__fmul_rn(r, r), u.y);
-        r = fmaxf(g.z, 0.0f); h.z = __fmul_rn(__fmul_rn(r, r), u.z);
-        r = fmaxf(g.w, 0.0f); h.w = __fmul_rn(__fmul_rn(r, r), u.w);
-      } else {
-        h = g;
+  // Pass 1: h (gated or plain) into shared memory, then the exact sum of
+  // squares (norm) or the running max |h| (no norm).
+  if (norm) {
+    // Warp-uniform trip count so that every lane joins the bucket aggregation.
+    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
+      const int i = base + (threadIdx.x & 31);
+      float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < K4) {
+        h = gated(xr, ur, i);
+        hs[i] = h;
       }
-      hs[i] = h;
-    }
-    if (norm) {
       const float f[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -91,7 +97,12 @@ act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int
         fp32_bucket(f[c], &b, &m);
         warp_bucket_add(buckets, b, (unsigned long long)m * (unsigned long long)m);
       }
-    } else {
+    }
+  } else {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+      const float4 h = gated(xr, ur, i);
+      hs[i] = h;
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
     }
   }
@@ -156,7 +167,8 @@ cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_
     configured_device = dev.device;
     configured_smem = dev.smem_optin - 4096;
   }
-  act_quant_kernel<<<(unsigned)M, kActThreads, smem, stream>>>(x, mul, (int)K, gamma, eps, xq, sx);
+  const int threads = M < dev.num_sms ? kActThreadsFew : kActThreadsMany;
+  act_quant_kernel<<<(unsigned)M, threads, smem, stream>>>(x, mul, (int)K, gamma, eps, xq, sx);
   return cudaGetLastError();
 }
 

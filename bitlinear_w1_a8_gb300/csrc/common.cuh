@@ -170,6 +170,10 @@ cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_
                              const float* gamma, double eps, int8_t* xq, float* sx,
                              const DeviceInfo& dev, cudaStream_t stream);
 
+cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+
 cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                           bool pdl, const DeviceInfo& dev, cudaStream_t stream);

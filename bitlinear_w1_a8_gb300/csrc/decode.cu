@@ -12,14 +12,18 @@
 //  * thread t of a CTA owning R rows takes row r = t % R and k-blocks
 //    j, j+J, j+2J, ... with j = t / R, J = blockDim / R; consecutive threads
 //    read consecutive 16-byte chunks of one k-block plane (fully coalesced);
+//  * the first batch of weight loads is issued before griddepcontrol.wait (the
+//    packed weights never come from the previous kernel), then the token
+//    group's int8 activations, their row sums and sx*sw are staged in shared
+//    memory in a single pass, so each CTA waits on memory about twice: once
+//    for HBM (weights, overlapping the previous kernel under PDL) and once
+//    for L2 (activations);
 //  * each 16-byte chunk holds 64 two-bit codes c = Wq+1; (word >> 2s) &
 //    0x03030303 lines four codes up with four int8 activations and one dp4a
 //    adds c*x for all four; the sum of c*x minus the row sum of x equals the
 //    sum of Wq*x (the ternary add/sub) exactly;
 //  * partial sums of the J threads of a row meet in shared memory (int32
 //    atomics, exact in any order), then one thread per row rescales.
-// With BITLINEAR_FLAG_PDL the weight loads of the first batch are issued
-// before griddepcontrol.wait, overlapping the producer of xq.
 #include "common.cuh"
 
 namespace bitlinear {
@@ -38,10 +42,19 @@ struct DecodeParams {
 
 constexpr int kUnroll = 4;
 
+// Dynamic shared memory: xs[MT][K] int8 activations of the token group, then
+// red[MT][rows_tile] int32 partial sums.
 template <int MT>
 __global__ void __launch_bounds__(MT <= 2 ? 1024 : 512, 1) decode_kernel(const DecodeParams p) {
-  extern __shared__ int red[];  // [MT][rows_tile] partial sums
+  extern __shared__ int4 dsmem[];
   __shared__ int sumx[MT];
+  __shared__ float den[MT];
+  int8_t* xs = reinterpret_cast<int8_t*>(dsmem);
+  int* red = reinterpret_cast<int*>(xs + (size_t)MT * p.K);
+
+  // Let the next kernel on the stream (normally the next BitLinear call) start
+  // its weight loads on SMs this grid frees; it still waits for our results.
+  pdl_release_dependents();
 
   const int G = gridDim.x;
   const int c = blockIdx.x;
@@ -51,23 +64,59 @@ __global__ void __launch_bounds__(MT <= 2 ? 1024 : 512, 1) decode_kernel(const D
   const int r1 = (int)(((int64_t)(c + 1) * p.N) / G);
   const int T = blockDim.x;
   const int t = threadIdx.x;
-  const int4* xrow[MT];
+  const int warp = t >> 5, lane = t & 31;
+  const int K16 = p.K >> 4;
+
+  // First tile geometry and its first batch of weight loads: issued before the
+  // wait because the packed weights do not come from the previous kernel.
+  int rt0 = r0;
+  int R = min(p.rows_tile, r1 - rt0);
+  int J = T / R;
+  int r = t % R, j = t / R;
+  uint4 w[kUnroll];
 #pragma unroll
-  for (int m = 0; m < MT; ++m)
-    xrow[m] = reinterpret_cast<const int4*>(p.xq + (int64_t)(m0 + (m < mcount ? m : 0)) * p.K);
+  for (int u = 0; u < kUnroll; ++u) {
+    const int kb = j + u * J;
+    w[u] = (j < J && kb < p.KB) ? ld_stream_u4(p.packed + (int64_t)kb * p.N + rt0 + r)
+                                : make_uint4(0, 0, 0, 0);
+  }
 
-  // Let the next kernel on the stream (normally the next BitLinear call) start
-  // its weight loads on SMs this grid frees; it still waits for our results.
-  pdl_release_dependents();
-  if (t < MT) sumx[t] = 0;
-  bool waited = false;
-  bool first_tile = true;
+  pdl_wait_primary();
 
-  for (int rt0 = r0; rt0 < r1; rt0 += p.rows_tile) {
-    const int R = min(p.rows_tile, r1 - rt0);
-    const int J = T / R;
-    const int r = t % R;
-    const int j = t / R;
+  // Stage the token group's activations (one pass over L2) and the scales.
+  if (t < MT) {
+    sumx[t] = 0;
+    den[t] = t < mcount ? __fmul_rn(p.sx[m0 + t], *p.sw) : 1.0f;
+  }
+  {
+    const int4* src = reinterpret_cast<const int4*>(p.xq + (int64_t)m0 * p.K);
+    int4* dst = reinterpret_cast<int4*>(xs);
+    for (int i = t; i < mcount * K16; i += T) dst[i] = src[i];
+  }
+  __syncthreads();
+  // Row sums of the activations (the bias of the biased codes c = Wq + 1).
+  for (int m = warp; m < mcount; m += T / 32) {
+    const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.K);
+    int s = 0;
+    for (int i = lane; i < K16; i += 32) {
+      const int4 v = row[i];
+      s = __dp4a(v.x, 0x01010101, s);
+      s = __dp4a(v.y, 0x01010101, s);
+      s = __dp4a(v.z, 0x01010101, s);
+      s = __dp4a(v.w, 0x01010101, s);
+    }
+    s = __reduce_add_sync(kFullMask, s);
+    if (lane == 0) sumx[m] = s;
+  }
+
+  bool first = true;
+  for (; rt0 < r1; rt0 += p.rows_tile) {
+    if (!first) {
+      R = min(p.rows_tile, r1 - rt0);
+      J = T / R;
+      r = t % R;
+      j = t / R;
+    }
     for (int i = t; i < MT * p.rows_tile; i += T) red[i] = 0;
     __syncthreads();
 
@@ -78,16 +127,14 @@ __global__ void __launch_bounds__(MT <= 2 ? 1024 : 512, 1) decode_kernel(const D
     if (j < J) {
       const uint4* wcol = p.packed + (rt0 + r);
       for (int kb0 = j; kb0 < p.KB; kb0 += kUnroll * J) {
-        uint4 w[kUnroll];
+        if (!first) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int kb = kb0 + u * J;
-          w[u] = kb < p.KB ? ld_stream_u4(wcol + (int64_t)kb * p.N) : make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * J;
+            w[u] = kb < p.KB ? ld_stream_u4(wcol + (int64_t)kb * p.N) : make_uint4(0, 0, 0, 0);
+          }
         }
-        if (!waited) {
-          pdl_wait_primary();
-          waited = true;
-        }
+        first = false;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int kb = kb0 + u * J;
@@ -102,7 +149,7 @@ __global__ void __launch_bounds__(MT <= 2 ? 1024 : 512, 1) decode_kernel(const D
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
                 if (m < mcount) {
-                  const int4 xv = xrow[m][kb * 4 + wi];
+                  const int4 xv = reinterpret_cast<const int4*>(xs + (size_t)m * p.K)[kb * 4 + wi];
                   int a = acc[m];
                   a = __dp4a(c0, xv.x, a);
                   a = __dp4a(c1, xv.y, a);
@@ -115,52 +162,37 @@ __global__ void __launch_bounds__(MT <= 2 ? 1024 : 512, 1) decode_kernel(const D
           }
         }
       }
-    }
-    if (!waited) {
-      pdl_wait_primary();
-      waited = true;
-    }
-    if (j < J) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
         if (m < mcount) atomicAdd(&red[m * p.rows_tile + r], acc[m]);
     }
-    if (first_tile) {
-      // Row sums of the activations (the bias of the biased codes c = Wq + 1).
-      const int K16 = p.K >> 4;
-      for (int m = 0; m < mcount; ++m) {
-        int s = 0;
-        for (int i = t; i < K16; i += T) {
-          const int4 v = xrow[m][i];
-          s = __dp4a(v.x, 0x01010101, s);
-          s = __dp4a(v.y, 0x01010101, s);
-          s = __dp4a(v.z, 0x01010101, s);
-          s = __dp4a(v.w, 0x01010101, s);
-        }
-        s = __reduce_add_sync(kFullMask, s);
-        if ((t & 31) == 0 && s != 0) atomicAdd(&sumx[m], s);
-      }
-      first_tile = false;
-    }
+    first = false;
     __syncthreads();
     if (t < R) {
       const int n = rt0 + t;
-      const float sw = *p.sw;
       for (int m = 0; m < mcount; ++m) {
         const int total = red[m * p.rows_tile + t] - sumx[m];
-        const float den = __fmul_rn(p.sx[m0 + m], sw);
-        p.y[(int64_t)(m0 + m) * p.N + n] = __fdiv_rn(__int2float_rn(total), den);
+        p.y[(int64_t)(m0 + m) * p.N + n] = __fdiv_rn(__int2float_rn(total), den[m]);
         if (p.acc) p.acc[(int64_t)(m0 + m) * p.N + n] = total;
       }
     }
     __syncthreads();
   }
-  if (!waited) pdl_wait_primary();
 }
 
 template <int MT>
-cudaError_t launch_mt(const DecodeParams& p, int grid_x, int threads, bool pdl, cudaStream_t stream) {
-  const size_t smem = (size_t)MT * p.rows_tile * sizeof(int);
+cudaError_t launch_mt(const DecodeParams& p, int grid_x, int threads, bool pdl, const DeviceInfo& dev,
+                      cudaStream_t stream) {
+  const size_t smem = (size_t)MT * p.K + (size_t)MT * p.rows_tile * sizeof(int);
+  if (smem > 48 * 1024) {
+    static thread_local int configured_device = -1;
+    if (configured_device != dev.device) {
+      cudaError_t err = cudaFuncSetAttribute(decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(dev.smem_optin - 2048));
+      if (err != cudaSuccess) return err;
+      configured_device = dev.device;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid_x, (unsigned)((p.M + MT - 1) / MT), 1);
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -190,17 +222,20 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const ui
   p.N = (int)N;
   p.K = (int)K;
   p.KB = (int)(K / 64);
-  const int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+  // Token group size: up to 8 tokens, with the group's activations (MT * K
+  // bytes) held in at most 64 KB of shared memory.
+  int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+  while (mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
   const int tmax = mt <= 2 ? 1024 : 512;
   const int G = (int)(N < dev.num_sms ? N : dev.num_sms);
   const int rmax = (int)((N + G - 1) / G);
   p.rows_tile = rmax < tmax ? rmax : tmax;
   const int threads = p.rows_tile * (tmax / p.rows_tile);
   switch (mt) {
-    case 1: return launch_mt<1>(p, G, threads, pdl, stream);
-    case 2: return launch_mt<2>(p, G, threads, pdl, stream);
-    case 4: return launch_mt<4>(p, G, threads, pdl, stream);
-    default: return launch_mt<8>(p, G, threads, pdl, stream);
+    case 1: return launch_mt<1>(p, G, threads, pdl, dev, stream);
+    case 2: return launch_mt<2>(p, G, threads, pdl, dev, stream);
+    case 4: return launch_mt<4>(p, G, threads, pdl, dev, stream);
+    default: return launch_mt<8>(p, G, threads, pdl, dev, stream);
   }
 }
 

@@ -1,0 +1,507 @@
+// prefill.cu -- BitLinear contraction for many tokens on the 5th-generation
+// tensor cores (tcgen05, sm_103a).
+//
+// y[m, n] = acc[m, n] / (sx[m] * sw),  acc = xq . Wq^T  (BitNet b1.58 BitLinear;
+// a full-sequence forward runs every projection on [batch*seq, dim] tokens,
+// "Hesper.Models.BitNet" page, section "Architecture", and "Transformer Block"
+// page, section "Forward Pass").  At M = 2048 tokens this is a dense
+// contraction, so it runs on the tensor cores.
+//
+// sm_103a has no integer tcgen05 MMA (ptxas rejects kind::i8 for this
+// target), so the operands are widened to fp16 in shared memory: int8
+// activations (|xq| <= 127) and ternary weights are exact in fp16, every
+// product is an exact integer, and the fp32 accumulator holds every partial
+// sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
+// int32 result is therefore bit-exact.
+//
+// CTA roles (one persistent CTA per SM, 13 warps):
+//   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
+//   warps 4-11  converters: load int8 / packed tiles from global into
+//               registers, widen them to fp16 and store them in the
+//               128-byte-swizzled K-major layout the MMA reads
+//   warp 12     allocates TMEM; one lane issues tcgen05.mma
+// Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles;
+// TMEM holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
+// overlaps the MMAs of the next.  Every mbarrier wait is bounded by the
+// global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
+// status word, every role leaves its loop, the MMA warp waits (bounded) for
+// its own MMAs, frees TMEM and the kernel returns.
+#include "common.cuh"
+
+namespace bitlinear {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileM = 128;
+constexpr int kMaxTileN = 256;
+constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
+constexpr int kABytes = kTileM * 128;            // 16 KB
+constexpr int kBBytes = kMaxTileN * 128;         // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 4;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kMmaWarp = kEpiWarps + kConvWarps;  // 12
+constexpr int kThreads = (kMmaWarp + 1) * 32;      // 416
+constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
+
+struct PrefillParams {
+  const int8_t* xq;
+  const float* sx;
+  const uint4* packed;
+  const float* sw;
+  float* y;
+  int32_t* acc;
+  int* status;
+  int M, N, K, KB;
+  int n_tile;      // multiple of 16, <= 256
+  int tiles_m, tiles_n, num_tiles;
+};
+
+struct SharedCtl {
+  unsigned long long full[kStages];
+  unsigned long long empty[kStages];
+  unsigned long long tmem_full[2];
+  unsigned long long tmem_empty[2];
+  unsigned long long mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_timer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.  Returns false
+// if the CTA is aborting (another role timed out) or this wait timed out.
+__device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, SharedCtl* ctl,
+                                       int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+      if (global_timer() - t0 > kTimeoutNs) {
+        atomicExch(&ctl->abort_flag, 1);
+        atomicExch(status, (int)BITLINEAR_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait that ignores the abort flag: used to drain this thread's own
+// in-flight MMAs before TMEM is freed.
+__device__ __noinline__ void mbar_drain(unsigned long long* bar, uint32_t parity, int* status) {
+  const unsigned long long t0 = global_timer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0u && global_timer() - t0 > kTimeoutNs) {
+      atomicExch(status, (int)BITLINEAR_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(unsigned long long* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), tile base 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3fffu);          // start address
+  d |= (uint64_t)1u << 16;                          // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
+  d |= (uint64_t)1u << 46;                          // descriptor version (sm_100 family)
+  d |= (uint64_t)2u << 61;                          // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = fp16, D = fp32, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 4)                       // D format fp32
+         | (0u << 7) | (0u << 10)        // A, B format fp16
+         | ((uint32_t)(n >> 3) << 17)    // N / 8
+         | ((uint32_t)(m >> 4) << 24);   // M / 16
+}
+
+// int8 x4 -> two fp16x2 words (exact): bias the bytes to b+128, place them in the
+// mantissa of fp16 1024 (0x6400), subtract 1152.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = v ^ 0x80808080u;
+  lo = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
+  hi = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+}
+
+// Two 2-bit codes -> one fp16x2 word of (code - 1): the codes' two bits sit at
+// bit offsets s and s+8 of `word`; they become selector nibbles 1 and 3 (plus 4)
+// of a byte permute over {0, 0, 0, 0, 0xBC, 0x00, 0x3C, 0x00} (high bytes of
+// fp16 -1, 0, +1).
+template <int S>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t word) {
+  uint32_t sel;
+  if constexpr (S <= 4) sel = (word << (4 - S)) & 0x3030u;
+  else sel = (word >> (S - 4)) & 0x3030u;
+  return prmt(0u, 0x003C00BCu, sel | 0x4040u);
+}
+
+// One 16-byte packed chunk (64 weights of a row) -> 8 chunks of 8 fp16.
+// Chunk c holds k = 8c..8c+7: word w = c/2, k%16 = 8(c%2) + t, t = 0..7,
+// i.e. codes at bit 8*(t%4) + 2*(2(c%2) + t/4) of word w.
+__device__ __forceinline__ void store_weight_row(uint32_t row_addr, int r, const uint4 v) {
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w = words[c >> 1];
+    const int j0 = 2 * (c & 1);  // i/4 of t = 0..3; j0 + 1 for t = 4..7
+    uint32_t q0, q1, q2, q3;
+    if (j0 == 0) {
+      q0 = codes_to_f16x2<0>(w);    // t = 0, 1 : bits 0, 8
+      q1 = codes_to_f16x2<16>(w);   // t = 2, 3 : bits 16, 24
+      q2 = codes_to_f16x2<2>(w);    // t = 4, 5 : bits 2, 10
+      q3 = codes_to_f16x2<18>(w);   // t = 6, 7 : bits 18, 26
+    } else {
+      q0 = codes_to_f16x2<4>(w);
+      q1 = codes_to_f16x2<20>(w);
+      q2 = codes_to_f16x2<6>(w);
+      q3 = codes_to_f16x2<22>(w);
+    }
+    st_shared_v4(row_addr + ((uint32_t)((c ^ (r & 7)) << 4)), q0, q1, q2, q3);
+  }
+}
+
+__device__ __forceinline__ void tile_coords(const PrefillParams& p, int tile, int& m0, int& n0) {
+  const int tm = tile % p.tiles_m;
+  const int tn = tile / p.tiles_m;
+  m0 = tm * kTileM;
+  n0 = tn * p.n_tile;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ SharedCtl ctl;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // 1024-byte aligned stage buffers (the swizzle pattern follows address bits)
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t stage_base = (raw_addr + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl.full[s], kConvThreads);
+      mbar_init(&ctl.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl.tmem_full[s], 1);
+      mbar_init(&ctl.tmem_empty[s], kEpiWarps * 32);
+    }
+    mbar_init(&ctl.mma_done, 1);
+    ctl.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+
+  // Inputs are produced by the previous kernel on the stream.
+  pdl_wait_primary();
+
+  if (warp >= kEpiWarps && warp < kMmaWarp) {
+    // ------------------------------------------------------------------ converters
+    const int u = threadIdx.x - kEpiWarps * 32;  // 0 .. 255
+    const int a_row = u >> 1, a_half = u & 1;
+    const int b_row = u;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      int m0, n0;
+      tile_coords(p, tile, m0, n0);
+      const int am = m0 + a_row;
+      const bool a_ok = am < p.M;
+      const uint4* a_src = reinterpret_cast<const uint4*>(p.xq + (int64_t)(a_ok ? am : 0) * p.K) + a_half * 2;
+      const int bn = n0 + b_row;
+      const bool b_ok = b_row < p.n_tile && bn < p.N;
+      const bool b_active = b_row < p.n_tile;
+      const uint4* b_src = p.packed + (b_ok ? bn : 0);
+      // software pipeline: loads of k-step ks+1 are in flight while ks is converted
+      uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, bv = a0;
+      if (a_ok) { a0 = __ldg(a_src); a1 = __ldg(a_src + 1); }
+      if (b_ok) bv = __ldg(b_src);
+      for (int ks = 0; ks < p.KB; ++ks) {
+        uint4 na0 = make_uint4(0, 0, 0, 0), na1 = na0, nbv = na0;
+        if (ks + 1 < p.KB) {
+          if (a_ok) { na0 = __ldg(a_src + (ks + 1) * 4); na1 = __ldg(a_src + (ks + 1) * 4 + 1); }
+          if (b_ok) nbv = __ldg(b_src + (int64_t)(ks + 1) * p.N);
+        }
+        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl, p.status)) { ok = false; break; }
+        const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
+        const uint32_t b_tile = a_tile + kABytes;
+        {
+          // A: 32 int8 (half a row) -> 4 chunks of 8 fp16
+          const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const uint32_t row_addr = a_tile + (uint32_t)a_row * 128u;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t l0, h0, l1, h1;
+            i8x4_to_f16x4(wv[2 * q], l0, h0);
+            i8x4_to_f16x4(wv[2 * q + 1], l1, h1);
+            const int c = 4 * a_half + q;
+            st_shared_v4(row_addr + ((uint32_t)((c ^ (a_row & 7)) << 4)), l0, h0, l1, h1);
+          }
+        }
+        if (b_active) {
+          const uint32_t row_addr = b_tile + (uint32_t)b_row * 128u;
+          if (b_ok) {
+            store_weight_row(row_addr, b_row, bv);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (uint32_t)(c << 4), 0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&ctl.full[stage]);
+        a0 = na0; a1 = na1; bv = nbv;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc(kTileM, p.n_tile);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++it) {
+        const int slot = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kMaxTileN);
+        for (int ks = 0; ks < p.KB; ++ks) {
+          if (!mbar_wait(&ctl.full[stage], phase, &ctl, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
+          const uint64_t a_desc = smem_desc_sw128(a_tile);
+          const uint64_t b_desc = smem_desc_sw128(a_tile + kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kKStep / 16; ++kk) {
+            // advance 16 fp16 = 32 bytes along K inside the swizzle atom
+            mma_f16(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
+                    (ks | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl.empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&ctl.tmem_full[slot]);
+      }
+      // All MMAs this thread issued must be complete before TMEM is freed.
+      mma_commit(&ctl.mma_done);
+      mbar_drain(&ctl.mma_done, 0u, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int row = warp * 32 + lane;  // TMEM lane = row of the tile
+    const float sw = *p.sw;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+      int m0, n0;
+      tile_coords(p, tile, m0, n0);
+      const int slot = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl, p.status)) break;
+      tc_fence_after();
+      const int m = m0 + row;
+      const bool row_ok = m < p.M;
+      const float den = row_ok ? __fmul_rn(p.sx[m], sw) : 1.0f;
+      float* yrow = p.y + (int64_t)(row_ok ? m : 0) * p.N;
+      int32_t* arow = p.acc ? p.acc + (int64_t)(row_ok ? m : 0) * p.N : nullptr;
+      const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
+      for (int c = 0; c < p.n_tile; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(t_row + (uint32_t)c, r);
+        const int n = n0 + c;
+        if (!row_ok || n >= p.N) continue;
+        float yv[16];
+        int av[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float a = __uint_as_float(r[j]);  // an exact integer
+          yv[j] = __fdiv_rn(a, den);
+          av[j] = __float2int_rn(a);
+        }
+        if (n + 16 <= p.N && ((((uintptr_t)(yrow + n)) & 15u) == 0)) {
+          float4* dst = reinterpret_cast<float4*>(yrow + n);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_float4(yv[4 * j], yv[4 * j + 1], yv[4 * j + 2], yv[4 * j + 3]);
+          if (arow) {
+            int4* ad = reinterpret_cast<int4*>(arow + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ad[j] = make_int4(av[4 * j], av[4 * j + 1], av[4 * j + 2], av[4 * j + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (n + j < p.N) {
+              yrow[n + j] = yv[j];
+              if (arow) arow[n + j] = av[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl.tmem_empty[slot]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Output-tile width: the multiple of 16 (<= 256) that minimises
+// (number of waves over the SMs) x (tile width), preferring wider tiles.
+int choose_n_tile(int64_t M, int64_t N, int sms) {
+  const int64_t tiles_m = (M + kTileM - 1) / kTileM;
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int nt = 256; nt >= 64; nt -= 16) {
+    const int64_t tiles = tiles_m * ((N + nt - 1) / nt);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t cost = waves * nt;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = nt;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  PrefillParams p;
+  p.xq = xq;
+  p.sx = sx;
+  p.packed = reinterpret_cast<const uint4*>(packed);
+  p.sw = sw;
+  p.y = y;
+  p.acc = acc;
+  p.status = dev.status;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.KB = (int)(K / kKStep);
+  p.n_tile = choose_n_tile(M, N, dev.num_sms);
+  p.tiles_m = (int)((M + kTileM - 1) / kTileM);
+  p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  const size_t smem = (size_t)kStages * kStageBytes + 1024;
+  static thread_local int configured = -1;
+  if (configured != dev.device) {
+    cudaError_t err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    configured = dev.device;
+  }
+  const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
+}
+
+}  // namespace bitlinear
