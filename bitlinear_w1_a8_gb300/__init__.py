@@ -16,7 +16,7 @@ __all__ = [
     "bitlinear_abi_version", "bitlinear_status_string", "bitlinear_packed_bytes",
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
-    "bitlinear_device_status", "EXPORTED_SYMBOLS",
+    "bitlinear_device_status", "bitlinear_quantize_weights_noalloc", "EXPORTED_SYMBOLS",
     "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "FLAG_PDL",
 ]
 
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_abi_version", "bitlinear_status_string", "bitlinear_packed_bytes",
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
-    "bitlinear_device_status",
+    "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
 )
 
 _lib = None
@@ -78,6 +78,8 @@ def load_library(path: str | None = None):
     lib.bitlinear_forward_ex.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, vp, ctypes.c_int,
                                          ctypes.c_int, vp]
     lib.bitlinear_forward_ex.restype = st
+    lib.bitlinear_quantize_weights_noalloc.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.bitlinear_quantize_weights_noalloc.restype = st
     lib.bitlinear_device_status.argtypes = [vp, ctypes.c_int]
     lib.bitlinear_device_status.restype = st
     if path is None:
@@ -145,6 +147,20 @@ def bitlinear_quantize_weights(W, packed, w_scale, workspace, stream=None):
     _check(load_library().bitlinear_quantize_weights(
         _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _ptr(workspace), workspace.numel(),
         _stream(stream)), "bitlinear_quantize_weights")
+
+
+def bitlinear_quantize_weights_noalloc(W, packed, w_scale, stream=None):
+    """weight_quant + pack like bitlinear_quantize_weights, for callers that cannot
+    allocate device memory: the scratch is a fixed array inside the library
+    (calls on one device must not overlap on the GPU; see include/bitlinear.h)."""
+    import torch
+    _need(W, torch.float32, "W")
+    N, K = W.shape
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+    _need(w_scale, torch.float32, "w_scale")
+    _check(load_library().bitlinear_quantize_weights_noalloc(
+        _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _stream(stream)),
+        "bitlinear_quantize_weights_noalloc")
 
 
 def bitlinear_quant_act(x, xq, x_scale, mul=None, rms_weight=None, rms_eps: float = 1e-6,

@@ -171,6 +171,49 @@ bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64
                               BITLINEAR_ALGO_AUTO, 0, stream);
 }
 
+// ---------------------------------------------------------------------------
+// bitlinear_quantize_weights_noalloc: the weight_quant scratch (bucket sums)
+// lives in this file-scope device array instead of a caller workspace.  Host
+// code may not pass the symbol itself to a kernel (on the host it names a
+// shadow, not device memory): its device address is looked up once per device
+// with cudaGetSymbolAddress and that pointer is passed on.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BITLINEAR_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+bitlinear_status noalloc_scratch(int device, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return BITLINEAR_ERR_CUDA;
+    g_noalloc_ptr[device] = ptr;
+  }
+  *out = g_noalloc_ptr[device];
+  return BITLINEAR_OK;
+}
+}  // namespace
+
+bitlinear_status bitlinear_quantize_weights_noalloc(const float* W, int64_t N, int64_t K, uint8_t* packed,
+                                                    float* w_scale, void* stream) {
+  if (!W || !packed || !w_scale) return BITLINEAR_ERR_NULL;
+  bitlinear_status st = check_nk(N, K);
+  if (st != BITLINEAR_OK) return st;
+  if (bitlinear_quantize_weights_workspace(N, K) > sizeof(g_noalloc_scratch)) return BITLINEAR_ERR_WORKSPACE;
+  if (!aligned16(W) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch(dev.device, &scratch);
+  if (st != BITLINEAR_OK) return st;
+  return from_cuda(launch_weight_quant(W, N, K, packed, w_scale, static_cast<unsigned long long*>(scratch),
+                                       dev, static_cast<cudaStream_t>(stream)));
+}
+
 bitlinear_status bitlinear_device_status(void* stream, int clear) {
   DeviceInfo dev;
   bitlinear_status st = current_device(&dev);

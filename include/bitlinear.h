@@ -160,6 +160,39 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
                                       int64_t N, int64_t K, float* y, int32_t* acc,
                                       int algo, int flags, void* stream);
 
+/* Size of the library's own device scratch array used by
+ * bitlinear_quantize_weights_noalloc. */
+#define BITLINEAR_NOALLOC_SCRATCH_BYTES 4096
+
+/*
+ * bitlinear_quantize_weights without a caller-provided workspace.
+ * (No counterpart on the pages: this is an interface convenience of this
+ * library, not part of the BitLinear method.)
+ *
+ * Some callers cannot allocate device memory at the point where they quantise
+ * weights: a runtime that fixes its memory budget at start-up and forbids
+ * later allocations, a plugin whose host gives it kernels and streams but no
+ * allocator, or code that must not touch the allocator at all.  This entry
+ * point takes the same inputs and outputs as bitlinear_quantize_weights and
+ * gives bit-identical results, but its scratch space (the per-exponent
+ * bucket sums) lives in a 4096-byte array inside this library
+ * (BITLINEAR_NOALLOC_SCRATCH_BYTES), held on every GPU that loads the library
+ * until the process exits.  It calls no cudaMalloc/cudaFree and no allocating
+ * library routine.
+ *  - The first call on a device looks up that array's device address (once
+ *    per device, with the device current); make that first call before any
+ *    stream capture begins.
+ *  - Every call on a device shares the one array and clears it on the stream
+ *    before use, so calls whose kernels overlap on the GPU (different streams
+ *    without ordering between them) race and give wrong results; order them.
+ *  - A matrix whose scratch need would exceed the array is rejected with
+ *    BITLINEAR_ERR_WORKSPACE (never the case today: the need is 4096 bytes for
+ *    every N, K that the shape checks accept).
+ * Other arguments, errors and results: as bitlinear_quantize_weights.
+ */
+bitlinear_status bitlinear_quantize_weights_noalloc(const float* W, int64_t N, int64_t K,
+                                                    uint8_t* packed, float* w_scale, void* stream);
+
 /* Synchronises `stream`, then returns BITLINEAR_ERR_TIMEOUT if any kernel of
  * this library recorded a timed-out wait on the current device since the last
  * call with clear != 0, BITLINEAR_ERR_CUDA if the stream reports an error,

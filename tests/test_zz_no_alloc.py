@@ -1,0 +1,49 @@
+"""bitlinear_quantize_weights_noalloc against bitlinear_quantize_weights.
+
+The no-allocation entry point is for callers that cannot allocate device
+memory when they quantise weights (a runtime with a fixed memory budget, a
+plugin without an allocator): it keeps its scratch in a fixed array inside
+the library instead of a caller workspace.  It must give exactly the same
+packed bytes and scale as the regular entry point, on consecutive calls too
+(the shared scratch keeps the previous call's contents and must be cleared).
+This file is collected last so that a failure here does not hide the others.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bitlinear_w1_a8_gb300 as bl
+from bitlinear_w1_a8_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _regular(W):
+    N, K = W.shape
+    packed = torch.empty(bl.bitlinear_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(bl.bitlinear_quantize_weights_workspace(N, K), dtype=torch.uint8, device="cuda")
+    bl.bitlinear_quantize_weights(W, packed, sw, ws)
+    return packed, sw
+
+
+def _noalloc(W):
+    N, K = W.shape
+    packed = torch.full((bl.bitlinear_packed_bytes(N, K),), 0xEE, dtype=torch.uint8, device="cuda")
+    sw = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    bl.bitlinear_quantize_weights_noalloc(W, packed, sw)
+    return packed, sw
+
+
+@pytest.mark.parametrize("N,K,seed", [(10240, 2560, 10), (300, 640, 3)])
+def test_noalloc_matches_regular_on_two_calls(N, K, seed):
+    bl.load_library()
+    W1 = synth.weight(N, K, seed).cuda()
+    W2 = (synth.weight(N, K, seed + 1) * 3.0).cuda()   # a different scale on the second call
+    for W in (W1, W2):                                  # two calls in a row share the scratch
+        p_ref, s_ref = _regular(W)
+        p_na, s_na = _noalloc(W)
+        assert bl.bitlinear_device_status() == 0
+        # integer codes and the scale: identical (the tolerance of every byte-level parity test)
+        assert s_na.item() == s_ref.item()
+        np.testing.assert_array_equal(p_na.cpu().numpy(), p_ref.cpu().numpy())
