@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the M=2048 prefill measurement")
     return ap.parse_args()
 
 
@@ -261,6 +262,87 @@ def ncu_traffic(kernel_sources, profile_name):
 DECODE_SOURCES = ["bitlinear_w1_a8_gb300/csrc/decode.cu", "bitlinear_w1_a8_gb300/csrc/common.cuh"]
 
 
+def measured_peak_tensor():
+    """Dense fp16/bf16 tensor peak (the prefill kernel runs kind::f16 MMAs)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+PREFILL_SOURCES = ["bitlinear_w1_a8_gb300/csrc/prefill.cu", "bitlinear_w1_a8_gb300/csrc/common.cuh"]
+
+
+def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
+    """BitNet-3B prefill GEMM, M = 2048 tokens, both FFN shapes, on the tensor-core
+    kernel: TOPS = 2*M*N*K / launch time, back-to-back launches in a CUDA graph over
+    rotating copies of inputs and outputs (working set > L2)."""
+    import torch
+    from bitlinear_w1_a8_gb300 import synth
+    s = synth.SEEDS["prefill"]
+    D, F = synth.DIM_3B, synth.FFN_3B
+    x = synth.activations(M, F, s["x"])  # K = 10240 for down; the first D columns for up
+    out = {}
+    peak, peak_src = measured_peak_tensor()
+    for name, N, K, seed in (("up_shape", F, D, s["W_up_shape"]), ("down_shape", D, F, s["W_down_shape"])):
+        W = synth.weight(N, K, seed).to(dev)
+        nb = bl.bitlinear_packed_bytes(N, K)
+        per_copy = nb + M * K + 4 * M * N
+        copies = max(2, -(-2 * L2_BYTES // per_copy))
+        packed = [torch.empty(nb, dtype=torch.uint8, device=dev) for _ in range(copies)]
+        sw = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(bl.bitlinear_quantize_weights_workspace(N, K), dtype=torch.uint8, device=dev)
+        bl.bitlinear_quantize_weights(W, packed[0], sw, ws)
+        for p in packed[1:]:
+            p.copy_(packed[0])
+        xd = x[:, :K].contiguous().to(dev)
+        xq = [torch.empty(M, K, dtype=torch.int8, device=dev) for _ in range(copies)]
+        sx = torch.empty(M, dtype=torch.float32, device=dev)
+        for q in xq:
+            bl.bitlinear_quant_act(xd, q, sx)
+        ys = [torch.empty(M, N, dtype=torch.float32, device=dev) for _ in range(copies)]
+        del W, xd
+
+        def body(i, st):
+            j = i % copies
+            bl.bitlinear_forward_ex(xq[j], sx, packed[j], sw, N, ys[j], algo=bl.ALGO_PREFILL, stream=st)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            body(0, stream)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(launches):
+                    body(i, stream)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = reduce_max_ms(e0.elapsed_time(e1), dist, dev) / launches
+        tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"M": M, "N": N, "K": K, "us_per_launch": round(ms * 1e3, 3),
+                     "tops": round(tops, 2), "frac_of_fp16_peak": round(tops / peak, 4),
+                     "rotating_copies": copies}
+        del packed, xq, ys
+        torch.cuda.empty_cache()
+    tot_ops = sum(2.0 * v["M"] * v["N"] * v["K"] for v in out.values())
+    tot_us = sum(v["us_per_launch"] for v in out.values())
+    achieved = tot_ops / (tot_us * 1e-6) / 1e12
+    out["roofline"] = {"kernel": "prefill_kernel (tcgen05 kind::f16, exact int8 x ternary)",
+                       "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                       "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                       "traffic": ncu_traffic(PREFILL_SOURCES, "prefill_m2048_bitnet3b_ncu.txt"),
+                       "note": "int8-equivalent ops (2*M*N*K) per launch / launch time; no int8 "
+                               "tcgen05 MMA exists on sm_103a, so the dense fp16 peak is the roofline"}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import bitlinear_w1_a8_gb300 as bl
@@ -434,6 +516,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     e2e_value = whole_job_gbs(per_step * e2e_steps, world, reduce_max_ms(q0.elapsed_time(q1), dist, dev))
 
+    prefill = None if args.no_prefill else measure_prefill(bl, dev, stream, dist)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, args.cpu_seconds)
@@ -470,6 +554,8 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clocks,
         }
+        if prefill:
+            line["prefill_m2048"] = prefill
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
