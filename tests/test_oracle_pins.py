@@ -96,6 +96,16 @@ def test_exact_sq_sum_is_correctly_rounded(seed):
     assert oracle.exact_sq_sum(v) == ref
 
 
+def test_exact_sums_of_subnormals():
+    # subnormals alone: |v| = frac * 2^-149 exactly (no hidden bit)
+    v = np.array([1e-45, -1e-45, 1e-45, 2.5e-44, -1.1754942e-38, 5e-40], np.float32)
+    ref = math.fsum(abs(float(t)) for t in v)
+    assert ref > 0 and oracle.exact_abs_sum(v) == ref
+    assert oracle.exact_abs_sum(np.array([1e-45] * 3, np.float32)) == 3 * 2.0 ** -149
+    assert oracle.exact_sq_sum(np.array([1e-45, -1e-45], np.float32)) == 2 * 2.0 ** -298
+    assert oracle.exact_sq_sum(v) == math.fsum(float(t) * float(t) for t in v)
+
+
 def test_exact_sum_rounding_ties():
     # 2^53 + 1 (exact) must round to even 2^53; 2^53 + 3 rounds up to 2^53 + 4.
     big = np.float32(2.0 ** 52)
