@@ -11,7 +11,9 @@ i.e. 19,660,800 packed weight bytes per step.  Inputs are seeded synthetic
 tensors (weights ~ N(0, 0.02), activations ~ N(0, 1) with 1% of channels x20).
 Each step uses the next of R copies of the packed weights (R * 19.7 MB > 4x
 L2), so every weight byte comes from HBM.  Steps run as CUDA graphs with
-programmatic dependent launch between kernels.
+programmatic dependent launch between kernels.  By default a step is two
+bitlinear_linear calls (act_quant fused into the decode kernel; gate and up in
+one launch); --separate times the five separate act_quant / forward calls.
 
 Metric: packed-weight GB/s (1e9 B/s) over the whole job.  One JSON line on
 rank 0.  `--impl reference` times the CPU oracle on the same workload instead.
@@ -51,6 +53,10 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the M=2048 prefill measurement")
+    ap.add_argument("--no-weight-set", action="store_true",
+                    help="skip the full BitNet-3B weight-set measurement (M = 1, 8, 32, 64)")
+    ap.add_argument("--separate", action="store_true",
+                    help="time separate act_quant + forward calls instead of bitlinear_linear")
     return ap.parse_args()
 
 
@@ -343,6 +349,86 @@ def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
     return out
 
 
+def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
+    """BitNet-3B full per-token weight set: 32 layers x (q, k, v, o 2560x2560;
+    gate, up 2560->10240; down 10240->2560) plus the LM head 2560->50000, every
+    matrix independently seeded N(0, 0.02) and quantised once (870,860,800
+    packed bytes, > 4x L2).  One step = every BitLinear call of one decode step
+    of M tokens in block order -- [q||k||v], [o], [gate||up], [down] per layer,
+    then the LM head -- each a bitlinear_linear call on seeded synthetic inputs
+    (attention and residuals are not part of this path), replayed as one CUDA
+    graph with PDL."""
+    import torch
+    from bitlinear_w1_a8_gb300 import synth
+    D, F, V, L = synth.DIM_3B, synth.FFN_3B, synth.VOCAB, synth.LAYERS_3B
+    shapes = [(D, D), (D, D), (D, D), (D, D), (F, D), (F, D), (D, F)]  # q k v o gate up down: (N, K)
+    ws = torch.empty(bl.bitlinear_quantize_weights_workspace(F, D), dtype=torch.uint8, device=dev)
+    layers = []
+    total_bytes = 0
+    for layer in range(L):
+        mats = []
+        for proj, (N, K) in enumerate(shapes):
+            W = synth.normal_cuda((N, K), synth.WEIGHT_STD, synth.weight_set_seed(layer, proj), dev)
+            pk = torch.empty(bl.bitlinear_packed_bytes(N, K), dtype=torch.uint8, device=dev)
+            sc = torch.empty(1, dtype=torch.float32, device=dev)
+            bl.bitlinear_quantize_weights(W, pk, sc, ws)
+            mats.append((pk, sc, N))
+            total_bytes += pk.numel()
+        layers.append(mats)
+    W = synth.normal_cuda((V, D), synth.WEIGHT_STD, synth.SEEDS["weight_set"]["lm_head"], dev)
+    head_pk = torch.empty(bl.bitlinear_packed_bytes(V, D), dtype=torch.uint8, device=dev)
+    head_sc = torch.empty(1, dtype=torch.float32, device=dev)
+    bl.bitlinear_quantize_weights(W, head_pk, head_sc, ws)
+    total_bytes += head_pk.numel()
+    del W
+    weights_n = sum(N * K for N, K in shapes) * L + V * D
+    out = {"packed_bytes_per_step": total_bytes, "weights": weights_n, "launch_calls_per_step": 4 * L + 1}
+    for M in Ms:
+        xa = synth.activations(M, D, synth.SEEDS["weight_set"]["x"]).to(dev)
+        xb = synth.activations(M, F, synth.SEEDS["weight_set"]["x"] + 1).to(dev)
+        xq_a = torch.empty(M, D, dtype=torch.int8, device=dev)
+        xq_b = torch.empty(M, F, dtype=torch.int8, device=dev)
+        sx_a = torch.empty(M, dtype=torch.float32, device=dev)
+        sx_b = torch.empty(M, dtype=torch.float32, device=dev)
+        ys = {n: torch.empty(M, n, dtype=torch.float32, device=dev) for n in (D, F, V)}
+        yq, yk, yv = (torch.empty(M, D, dtype=torch.float32, device=dev) for _ in range(3))
+        yu = torch.empty(M, F, dtype=torch.float32, device=dev)
+
+        def step(s):
+            for mats in layers:
+                (q, sq, _), (k, sk, _), (v, sv, _), (o, so, _), (g, sg, _), (u, su, _), (d, sd, _) = mats
+                bl.bitlinear_linear(xa, [(q, sq, yq), (k, sk, yk), (v, sv, yv)], xq_a, sx_a,
+                                    flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear(xa, [(o, so, ys[D])], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear(xa, [(g, sg, ys[F]), (u, su, yu)], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear(xb, [(d, sd, ys[D])], xq_b, sx_b, flags=bl.FLAG_PDL, stream=s)
+            bl.bitlinear_linear(xa, [(head_pk, head_sc, ys[V])], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step(stream)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                step(stream)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = reduce_max_ms(e0.elapsed_time(e1), dist, dev) / reps
+        out[f"M{M}"] = {"us_per_step": round(ms * 1e3, 2),
+                        "packed_GBps": round(total_bytes / (ms * 1e-3) / 1e9, 1),
+                        "tops": round(2.0 * M * weights_n / (ms * 1e-3) / 1e12, 2),
+                        "us_per_token": round(ms * 1e3 / M, 3)}
+        del g
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import bitlinear_w1_a8_gb300 as bl
@@ -388,7 +474,8 @@ def run_ours(args, rank, world, local_rank):
     y_d = torch.empty(1, D, dtype=torch.float32, device=dev)
     flags = 0 if args.no_pdl else bl.FLAG_PDL
 
-    def step(i, stream):
+    def step_separate(i, stream):
+        # act_quant and forward as separate calls (5 launches per step)
         g, u, d = slots[i % R]
         bl.bitlinear_quant_act(x_a, xq_a, sx_a, stream=stream)
         bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=stream)
@@ -396,7 +483,14 @@ def run_ours(args, rank, world, local_rank):
         bl.bitlinear_quant_act(x_b, xq_b, sx_b, stream=stream)
         bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=stream)
 
-    kernels_per_step = 5
+    def step_linear(i, stream):
+        # bitlinear_linear: act_quant fused into the decode kernel, gate || up in one launch
+        g, u, d = slots[i % R]
+        bl.bitlinear_linear(x_a, [(g, sw_u, y_g), (u, sw_u, y_u)], xq_a, sx_a, flags=flags, stream=stream)
+        bl.bitlinear_linear(x_b, [(d, sw_d, y_d)], xq_b, sx_b, flags=flags, stream=stream)
+
+    step = step_separate if args.separate else step_linear
+    kernels_per_step = 5 if args.separate else 2
     stream = torch.cuda.Stream(device=dev)
 
     def capture(fn, n):
@@ -451,12 +545,35 @@ def run_ours(args, rank, world, local_rank):
     ms_max = reduce_max_ms(ev0.elapsed_time(ev1), dist, dev)
     value = whole_job_gbs(per_step * args.steps, world, ms_max)
 
-    # Dominant kernel alone: back-to-back forward launches over the rotation.
+    # The other path, for comparison (same rotation, same timing method).
+    alt = step_linear if args.separate else step_separate
+    g_alt = capture(alt, R)
+    alt_reps = max(3, min(2000, args.steps // R))
+    with torch.cuda.stream(stream):
+        g_alt.replay()
+    torch.cuda.synchronize(dev)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(alt_reps):
+            g_alt.replay()
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    alt_ms = a0.elapsed_time(a1) / (alt_reps * R)
+    alt_line = {"path": "separate act_quant + forward calls (5 launches)" if not args.separate
+                else "bitlinear_linear (2 launches)",
+                "ms_per_step": round(alt_ms, 6), "value": round(per_step / (alt_ms * 1e-3) / 1e9, 3)}
+
+    # Dominant kernel alone: back-to-back launches of the decode kernel over the rotation.
     def fwd_only(i, s):
         g, u, d = slots[i % R]
-        bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=s)
-        bl.bitlinear_forward_ex(xq_a, sx_a, u, sw_u, F, y_u, flags=flags, stream=s)
-        bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=s)
+        if args.separate:
+            bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=s)
+            bl.bitlinear_forward_ex(xq_a, sx_a, u, sw_u, F, y_u, flags=flags, stream=s)
+            bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=s)
+        else:
+            step_linear(i, s)
 
     g_fwd = capture(fwd_only, R)
     reps = max(3, min(200, args.steps // R))
@@ -472,11 +589,15 @@ def run_ours(args, rank, world, local_rank):
             g_fwd.replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    fwd_launches = reps * 3 * R
+    launches_per_rot = 3 if args.separate else 2
+    fwd_launches = reps * launches_per_rot * R
     fwd_ms = e0.elapsed_time(e1) / fwd_launches
-    # algorithmic bytes per forward launch (average over the three launches of a step):
-    # packed weights + int8 activations + one fp32 scale + fp32 outputs
-    alg_bytes = (2 * (bytes_u + D + 4 + 4 * F) + (bytes_d + F + 4 + 4 * D)) / 3.0
+    if args.separate:
+        # per forward launch: packed weights + int8 activations + one fp32 scale + fp32 outputs
+        alg_bytes = (2 * (bytes_u + D + 4 + 4 * F) + (bytes_d + F + 4 + 4 * D)) / 3.0
+    else:
+        # per fused launch: packed weights + fp32 input + int8 codes and scale written + fp32 outputs
+        alg_bytes = ((2 * bytes_u + 4 * D + D + 4 + 2 * 4 * F) + (bytes_d + 4 * F + F + 4 + 4 * D)) / 2.0
     peak, peak_src = measured_peak_hbm()
     achieved = alg_bytes / (fwd_ms * 1e-3) / 1e9
 
@@ -492,11 +613,15 @@ def run_ours(args, rank, world, local_rank):
         g, u, d = slots[i % R]
         x_a.copy_(h_xa, non_blocking=True)
         x_b.copy_(h_xb, non_blocking=True)
-        bl.bitlinear_quant_act(x_a, xq_a, sx_a)
-        bl.bitlinear_forward(xq_a, sx_a, g, sw_u, F, y_g)
-        bl.bitlinear_forward(xq_a, sx_a, u, sw_u, F, y_u)
-        bl.bitlinear_quant_act(x_b, xq_b, sx_b)
-        bl.bitlinear_forward(xq_b, sx_b, d, sw_d, D, y_d)
+        if args.separate:
+            bl.bitlinear_quant_act(x_a, xq_a, sx_a)
+            bl.bitlinear_forward(xq_a, sx_a, g, sw_u, F, y_g)
+            bl.bitlinear_forward(xq_a, sx_a, u, sw_u, F, y_u)
+            bl.bitlinear_quant_act(x_b, xq_b, sx_b)
+            bl.bitlinear_forward(xq_b, sx_b, d, sw_d, D, y_d)
+        else:
+            bl.bitlinear_linear(x_a, [(g, sw_u, y_g), (u, sw_u, y_u)], xq_a, sx_a)
+            bl.bitlinear_linear(x_b, [(d, sw_d, y_d)], xq_b, sx_b)
         h_yg.copy_(y_g, non_blocking=True)
         h_yu.copy_(y_u, non_blocking=True)
         h_yd.copy_(y_d, non_blocking=True)
@@ -517,6 +642,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = whole_job_gbs(per_step * e2e_steps, world, reduce_max_ms(q0.elapsed_time(q1), dist, dev))
 
     prefill = None if args.no_prefill else measure_prefill(bl, dev, stream, dist)
+    weight_set = None if args.no_weight_set else measure_weight_set(bl, dev, stream, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -535,9 +661,13 @@ def run_ours(args, rank, world, local_rank):
                 "l2": f"inputs larger than L2: {R} rotating weight copies, "
                       f"{R * per_step / 1e6:.0f} MB > 4x {L2_BYTES / 1e6:.0f} MB",
                 "cuda_graph": True, "pdl": not args.no_pdl, "parallelism": f"replicas{world}",
+                "path": ("separate bitlinear_quant_act + bitlinear_forward_ex calls" if args.separate else
+                         "bitlinear_linear: gate||up in one launch, down in one launch, act_quant fused"),
             },
+            "other_path": alt_line,
             "roofline": {
-                "kernel": "decode_kernel<1> (bitlinear_forward, M=1)", "bound": "hbm",
+                "kernel": ("decode_kernel<1> (bitlinear_forward, M=1)" if args.separate else
+                           "decode_kernel<1> (bitlinear_linear: act_quant fused, M=1)"), "bound": "hbm",
                 "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": ncu_traffic(DECODE_SOURCES, "decode_m1_bitnet3b_ncu.txt"),
@@ -556,6 +686,8 @@ def run_ours(args, rank, world, local_rank):
         }
         if prefill:
             line["prefill_m2048"] = prefill
+        if weight_set:
+            line["weight_set_3b"] = weight_set
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -16,7 +16,8 @@ __all__ = [
     "bitlinear_abi_version", "bitlinear_status_string", "bitlinear_packed_bytes",
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
-    "bitlinear_device_status", "bitlinear_quantize_weights_noalloc", "EXPORTED_SYMBOLS",
+    "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "BitLinearWeight", "EXPORTED_SYMBOLS",
     "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "FLAG_PDL",
 ]
 
@@ -35,9 +36,16 @@ EXPORTED_SYMBOLS = (
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear",
 )
 
 _lib = None
+
+
+class BitLinearWeight(ctypes.Structure):
+    """ctypes mirror of the C struct bitlinear_weight."""
+    _fields_ = [("packed", ctypes.c_void_p), ("w_scale", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("y", ctypes.c_void_p), ("acc", ctypes.c_void_p)]
 
 
 class BitLinearError(RuntimeError):
@@ -80,6 +88,11 @@ def load_library(path: str | None = None):
     lib.bitlinear_forward_ex.restype = st
     lib.bitlinear_quantize_weights_noalloc.argtypes = [vp, i64, i64, vp, vp, vp]
     lib.bitlinear_quantize_weights_noalloc.restype = st
+    lib.bitlinear_selftest_wait_timeout.argtypes = [i64, vp]
+    lib.bitlinear_selftest_wait_timeout.restype = st
+    lib.bitlinear_linear.argtypes = [vp, vp, i64, i64, vp, ctypes.c_double, ctypes.POINTER(BitLinearWeight),
+                                     ctypes.c_int, vp, vp, ctypes.c_int, vp]
+    lib.bitlinear_linear.restype = st
     lib.bitlinear_device_status.argtypes = [vp, ctypes.c_int]
     lib.bitlinear_device_status.restype = st
     if path is None:
@@ -216,3 +229,42 @@ def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=
 def bitlinear_device_status(stream=None, clear: bool = True) -> int:
     """Synchronise the stream and return the library's device status (0 = OK)."""
     return int(load_library().bitlinear_device_status(_stream(stream), 1 if clear else 0))
+
+
+def bitlinear_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test kernel (a wait nothing satisfies)."""
+    _check(load_library().bitlinear_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "bitlinear_selftest_wait_timeout")
+
+
+def bitlinear_linear(x, weights, xq, x_scale, mul=None, rms_weight=None, rms_eps: float = 1e-6,
+                     flags: int = 0, stream=None):
+    """act_quant + forward for 1..4 matrices sharing the input x [M, K].
+
+    weights: sequence of (packed, w_scale, y) or (packed, w_scale, y, acc) tuples of
+    CUDA tensors (y [M, N] fp32, acc [M, N] int32 or None).
+    """
+    import torch
+    _need(x, torch.float32, "x")
+    M, K = x.shape
+    _need(xq, torch.int8, "xq", (M, K))
+    _need(x_scale, torch.float32, "x_scale", (M,))
+    if mul is not None:
+        _need(mul, torch.float32, "mul", (M, K))
+    if rms_weight is not None:
+        _need(rms_weight, torch.float32, "rms_weight", (K,))
+    arr = (BitLinearWeight * len(weights))()
+    for i, w in enumerate(weights):
+        packed, w_scale, y = w[0], w[1], w[2]
+        acc = w[3] if len(w) > 3 else None
+        N = y.shape[1]
+        _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+        _need(w_scale, torch.float32, "w_scale")
+        _need(y, torch.float32, "y", (M, N))
+        if acc is not None:
+            _need(acc, torch.int32, "acc", (M, N))
+        arr[i] = BitLinearWeight(packed.data_ptr(), w_scale.data_ptr(), N, y.data_ptr(),
+                                 acc.data_ptr() if acc is not None else None)
+    _check(load_library().bitlinear_linear(
+        _ptr(x), _ptr(mul), M, K, _ptr(rms_weight), float(rms_eps), arr, len(weights), _ptr(xq),
+        _ptr(x_scale), int(flags), _stream(stream)), "bitlinear_linear")

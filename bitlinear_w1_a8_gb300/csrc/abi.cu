@@ -54,6 +54,9 @@ constexpr int64_t kDecodeMaxK = 65536;
 constexpr int64_t kPrefillMaxK = 131072;
 // AUTO picks the decode kernel up to this many tokens.
 constexpr int64_t kDecodeMaxM = 64;
+// bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
+// in shared memory next to the weights.
+constexpr int64_t kFusedMaxK = 16384;
 
 bitlinear_status check_nk(int64_t N, int64_t K) {
   if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return BITLINEAR_ERR_SHAPE;
@@ -159,9 +162,62 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
   if (st != BITLINEAR_OK) return st;
   const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (use == BITLINEAR_ALGO_DECODE)
-    return from_cuda(launch_decode(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+  if (use == BITLINEAR_ALGO_DECODE) {
+    const DecodeMatrix mat = {packed, w_scale, N, y, acc};
+    return from_cuda(launch_decode(xq, x_scale, M, &mat, 1, K, pdl, dev, s));
+  }
   return from_cuda(launch_prefill(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+}
+
+bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,
+                                  const float* rms_weight, double rms_eps, const bitlinear_weight* weights,
+                                  int num_weights, int8_t* xq, float* x_scale, int flags, void* stream) {
+  if (!weights) return BITLINEAR_ERR_NULL;
+  if (num_weights < 1 || num_weights > kMaxDecodeMats) return BITLINEAR_ERR_SHAPE;
+  if (M < 0 || M > kMaxDim || K <= 0 || K % 64 != 0 || K > 32768) return BITLINEAR_ERR_SHAPE;
+  if (rms_weight && !(rms_eps >= 0.0)) return BITLINEAR_ERR_SHAPE;
+  if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
+  for (int i = 0; i < num_weights; ++i) {
+    const bitlinear_weight& w = weights[i];
+    if (!w.packed || !w.w_scale) return BITLINEAR_ERR_NULL;
+    const bitlinear_status st = check_nk(w.N, K);
+    if (st != BITLINEAR_OK) return st;
+    if (!aligned16(w.packed) || (reinterpret_cast<uintptr_t>(w.w_scale) & 3u)) return BITLINEAR_ERR_ALIGN;
+  }
+  if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
+  if (!x || !xq || !x_scale) return BITLINEAR_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || (mul && !aligned16(mul)) || (rms_weight && !aligned16(rms_weight)) ||
+      (reinterpret_cast<uintptr_t>(x_scale) & 3u))
+    return BITLINEAR_ERR_ALIGN;
+  for (int i = 0; i < num_weights; ++i) {
+    if (!weights[i].y) return BITLINEAR_ERR_NULL;
+    if (!aligned16(weights[i].y) || (weights[i].acc && !aligned16(weights[i].acc))) return BITLINEAR_ERR_ALIGN;
+  }
+  DeviceInfo dev;
+  bitlinear_status st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
+  DecodeMatrix mats[kMaxDecodeMats];
+  for (int i = 0; i < num_weights; ++i)
+    mats[i] = DecodeMatrix{weights[i].packed, weights[i].w_scale, weights[i].N, weights[i].y, weights[i].acc};
+  if (M == 1 && K <= kFusedMaxK) {
+    // one launch: every CTA quantises the token itself
+    return from_cuda(launch_decode_fused(x, mul, rms_weight, rms_eps, K, mats, num_weights, xq, x_scale, pdl,
+                                         dev, s));
+  }
+  cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s);
+  if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  if (M <= kDecodeMaxM && K <= kDecodeMaxK) {
+    if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
+    return from_cuda(launch_decode(xq, x_scale, M, mats, num_weights, K, pdl, dev, s));
+  }
+  for (int i = 0; i < num_weights; ++i) {
+    err = launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
+                         pdl, dev, s);
+    if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  }
+  return BITLINEAR_OK;
 }
 
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
@@ -212,6 +268,14 @@ bitlinear_status bitlinear_quantize_weights_noalloc(const float* W, int64_t N, i
   if (st != BITLINEAR_OK) return st;
   return from_cuda(launch_weight_quant(W, N, K, packed, w_scale, static_cast<unsigned long long*>(scratch),
                                        dev, static_cast<cudaStream_t>(stream)));
+}
+
+bitlinear_status bitlinear_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 1000000000ll) return BITLINEAR_ERR_SHAPE;
+  DeviceInfo dev;
+  bitlinear_status st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  return from_cuda(launch_wait_selftest(limit_ns, dev, static_cast<cudaStream_t>(stream)));
 }
 
 bitlinear_status bitlinear_device_status(void* stream, int clear) {

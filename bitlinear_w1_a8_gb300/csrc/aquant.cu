@@ -1,18 +1,7 @@
 // aquant.cu -- per-token absmax activation_quant with the optional fused
-// prologues (ReLU^2 gating and RMSNorm).  One CTA per token row.
-//
-// activation_quant (BitNet b1.58, named in the Candle BitNet PR's list of
-// changes): sx = 127 / max(max_k |h|, 1e-5), xq = clamp(rne(h*sx), -128, 127).
-// Prologues, in this order when both are requested:
-//   gating   h = (r*r)*u, r = max(g, 0)   ("Transformer Block" page, section
-//            "Feed-Forward Network": hidden = ReLU^2(gate) x up)
-//   RMSNorm  inv = fp32(1 / sqrt(S/K + eps)) in fp64 with S the exact sum of
-//            h^2, then h = (h*inv)*gamma in fp32 (an RMSNorm before every
-//            BitLinear, Candle BitNet PR, list of changes; the FFN sub-norm
-//            of the "Transformer Block" layer structure).
-// Every product and the division are single IEEE fp32 operations (no FMA), so
-// the int8 codes do not depend on the launch shape.
-#include "common.cuh"
+// prologues (ReLU^2 gating and RMSNorm).  One CTA per token row; the row
+// routine (quant_row.cuh) states the arithmetic and its sources.
+#include "quant_row.cuh"
 
 namespace bitlinear {
 namespace {
@@ -20,134 +9,18 @@ namespace {
 constexpr int kActThreadsMany = 256;   // many rows: several CTAs per SM
 constexpr int kActThreadsFew = 1024;   // few rows: one wide CTA per row for latency
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-    if (lane == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float r = red[0];
-  __syncthreads();
-  return r;
-}
-
-// h = x, or h = (r*r)*u with r = max(x, 0) when the gating input u is given.
-__device__ __forceinline__ float4 gated(const float4* __restrict__ xr, const float4* __restrict__ ur, int i) {
-  const float4 g = xr[i];
-  if (!ur) return g;
-  const float4 u = ur[i];
-  float4 h;
-  float r;
-  r = fmaxf(g.x, 0.0f); h.x = __fmul_rn(__fmul_rn(r, r), u.x);
-  r = fmaxf(g.y, 0.0f); h.y = __fmul_rn(__fmul_rn(r, r), u.y);
-  r = fmaxf(g.z, 0.0f); h.z = __fmul_rn(__fmul_rn(r, r), u.z);
-  r = fmaxf(g.w, 0.0f); h.w = __fmul_rn(__fmul_rn(r, r), u.w);
-  return h;
-}
-
 // Dynamic shared memory: the K fp32 values of h for this row.
 __global__ void __launch_bounds__(kActThreadsFew, 1)
 act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int K,
                  const float* __restrict__ gamma, double eps, int8_t* __restrict__ xq,
                  float* __restrict__ sx) {
   extern __shared__ float4 hs[];
-  __shared__ unsigned long long buckets[kBuckets];
-  __shared__ unsigned long long digits[kSumDigits];
-  __shared__ float red[32];
-  __shared__ float inv_s;
-
+  __shared__ RowQuantScratch sc;
   // Let a dependent forward kernel start streaming its weights now.
   pdl_release_dependents();
-
   const int64_t row = blockIdx.x;
-  const int K4 = K >> 2;
-  const float4* xr = reinterpret_cast<const float4*>(x + row * (int64_t)K);
-  const float4* ur = mul ? reinterpret_cast<const float4*>(mul + row * (int64_t)K) : nullptr;
-  const bool norm = gamma != nullptr;
-
-  if (norm) {
-    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) buckets[i] = 0ull;
-    __syncthreads();
-  }
-
-  float amax = 0.0f;
-  // Pass 1: h (gated or plain) into shared memory, then the exact sum of
-  // squares (norm) or the running max |h| (no norm).
-  if (norm) {
-    // Warp-uniform trip count so that every lane joins the bucket aggregation.
-    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
-      const int i = base + (threadIdx.x & 31);
-      float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < K4) {
-        h = gated(xr, ur, i);
-        hs[i] = h;
-      }
-      const float f[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        int b;
-        uint32_t m;
-        fp32_bucket(f[c], &b, &m);
-        warp_bucket_add(buckets, b, (unsigned long long)m * (unsigned long long)m);
-      }
-    }
-  } else {
-#pragma unroll 4
-    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-      const float4 h = gated(xr, ur, i);
-      hs[i] = h;
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
-    }
-  }
-
-  if (norm) {
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const double S = warp_fold_buckets(buckets, 2, -298, digits);
-      if (threadIdx.x == 0) {
-        const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-        inv_s = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-      }
-    }
-    __syncthreads();
-    const float inv = inv_s;
-    const float4* g4 = reinterpret_cast<const float4*>(gamma);
-    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-      float4 h = hs[i];
-      const float4 gm = g4[i];
-      h.x = __fmul_rn(__fmul_rn(h.x, inv), gm.x);
-      h.y = __fmul_rn(__fmul_rn(h.y, inv), gm.y);
-      h.z = __fmul_rn(__fmul_rn(h.z, inv), gm.z);
-      h.w = __fmul_rn(__fmul_rn(h.w, inv), gm.w);
-      hs[i] = h;
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
-    }
-  }
-
-  amax = block_max(amax, red);
-  const float s = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
-
-  // Pass 2: quantise; thread i writes the 4 codes of float4 i.
-  int* out = reinterpret_cast<int*>(xq + row * (int64_t)K);
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-    const float4 h = hs[i];
-    const float f[4] = {h.x, h.y, h.z, h.w};
-    uint32_t word = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      int q = __float2int_rn(__fmul_rn(f[c], s));
-      q = q < -128 ? -128 : (q > 127 ? 127 : q);
-      word |= ((uint32_t)q & 0xffu) << (8 * c);
-    }
-    out[i] = (int)word;
-  }
+  const float s = quantize_row(x + row * (int64_t)K, mul ? mul + row * (int64_t)K : nullptr, gamma, eps, K,
+                               hs, sc, xq + row * (int64_t)K);
   if (threadIdx.x == 0) sx[row] = s;
 }
 

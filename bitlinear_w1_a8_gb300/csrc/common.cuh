@@ -174,8 +174,25 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
-cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
-                          const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
-                          bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int64_t limit_ns, const DeviceInfo& dev, cudaStream_t stream);
+
+// One weight matrix of a decode launch (several matrices may share one input).
+constexpr int kMaxDecodeMats = 4;
+struct DecodeMatrix {
+  const uint8_t* packed;
+  const float* w_scale;
+  int64_t N;
+  float* y;
+  int32_t* acc;
+};
+
+cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                          int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+
+// M = 1 only: every CTA quantises x (with the optional gating / RMSNorm
+// prologue) itself; CTA 0 writes xq_out / sx_out when they are not NULL.
+cudaError_t launch_decode_fused(const float* x, const float* mul, const float* gamma, double eps, int64_t K,
+                                const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out, bool pdl,
+                                const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace bitlinear

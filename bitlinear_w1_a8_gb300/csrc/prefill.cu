@@ -14,13 +14,18 @@
 // sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
 // int32 result is therefore bit-exact.
 //
-// CTA roles (one persistent CTA per SM, 13 warps):
+// CTA roles (one persistent CTA per SM, 15 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
-//   warps 4-11  converters: load int8 / packed tiles from global into
-//               registers, widen them to fp16 and store them in the
-//               128-byte-swizzled K-major layout the MMA reads
-//   warp 12     allocates TMEM; one lane issues tcgen05.mma
-// Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles;
+//   warps 4-11  converters: widen the raw int8 / packed tiles to fp16 and
+//               store them in the 128-byte-swizzled K-major layout the MMA
+//               reads
+//   warps 12-13 loaders: copy raw tiles from global memory into a 4-deep
+//               shared-memory ring with cp.async; the copies complete on the
+//               ring's mbarriers, so the converters never have loads of their
+//               own in flight when they fence their stores for the MMA
+//   warp 14     allocates TMEM; one lane issues tcgen05.mma
+// Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles
+// and kRawStages raw stages (A 128x64 int8, B n_tile x 16 B packed);
 // TMEM holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
 // overlaps the MMAs of the next.  Every mbarrier wait is bounded by the
 // global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
@@ -31,18 +36,26 @@
 namespace bitlinear {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;                       // fp16 operand stages read by the MMA
+constexpr int kRawStages = 4;                    // raw int8 / packed k-steps in flight per converter
 constexpr int kTileM = 128;
 constexpr int kMaxTileN = 256;
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
 constexpr int kABytes = kTileM * 128;            // 16 KB
 constexpr int kBBytes = kMaxTileN * 128;         // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRawABytes = kTileM * kKStep;      // 8 KB of int8 activations
+constexpr int kRawBBytes = kMaxTileN * 16;       // 4 KB of packed codes
+constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kMmaWarp = kEpiWarps + kConvWarps;  // 12
-constexpr int kThreads = (kMmaWarp + 1) * 32;      // 416
+constexpr int kLoadWarps = 2;
+constexpr int kLoadThreads = kLoadWarps * 32;
+constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 12
+constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 14
+constexpr int kThreads = (kMmaWarp + 1) * 32;       // 480
 constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
 
@@ -62,6 +75,8 @@ struct PrefillParams {
 struct SharedCtl {
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
+  unsigned long long raw_full[kRawStages];
+  unsigned long long raw_empty[kRawStages];
   unsigned long long tmem_full[2];
   unsigned long long tmem_empty[2];
   unsigned long long mma_done;
@@ -182,6 +197,22 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// 16-byte global -> shared asynchronous copy; src_bytes = 0 writes zeros and
+// reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(unsigned long long* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), tile base 1024-byte aligned.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
@@ -268,6 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       mbar_init(&ctl.full[s], kConvThreads);
       mbar_init(&ctl.empty[s], 1);
     }
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&ctl.raw_full[s], kLoadThreads);
+      mbar_init(&ctl.raw_empty[s], kConvThreads);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.tmem_full[s], 1);
       mbar_init(&ctl.tmem_empty[s], kEpiWarps * 32);
@@ -285,64 +320,98 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   // Inputs are produced by the previous kernel on the stream.
   pdl_wait_primary();
 
-  if (warp >= kEpiWarps && warp < kMmaWarp) {
-    // ------------------------------------------------------------------ converters
-    const int u = threadIdx.x - kEpiWarps * 32;  // 0 .. 255
-    const int a_row = u >> 1, a_half = u & 1;
-    const int b_row = u;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+  const uint32_t raw_base = stage_base + (uint32_t)kStages * kStageBytes;
+  const int my_tiles = (int)blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
+
+  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
+    // ------------------------------------------------------------------ loaders
+    // Copy the raw k-step (128 x 64 int8 activations, n_tile x 16 B packed codes)
+    // into the raw ring with cp.async; the ring slot's barrier completes when
+    // every loader's copies have landed.  Rows past M or N are zero-filled.
+    const int v = threadIdx.x - kLoadWarp0 * 32;  // 0 .. 63
+    for (int f = 0; f < total; ++f) {
+      const int slot = f % kRawStages;
+      const uint32_t use = (uint32_t)(f / kRawStages);
+      if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) break;
+      const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
+      const int ks = f % p.KB;
       int m0, n0;
       tile_coords(p, tile, m0, n0);
-      const int am = m0 + a_row;
-      const bool a_ok = am < p.M;
-      const uint4* a_src = reinterpret_cast<const uint4*>(p.xq + (int64_t)(a_ok ? am : 0) * p.K) + a_half * 2;
-      const int bn = n0 + b_row;
-      const bool b_ok = b_row < p.n_tile && bn < p.N;
-      const bool b_active = b_row < p.n_tile;
-      const uint4* b_src = p.packed + (b_ok ? bn : 0);
-      // software pipeline: loads of k-step ks+1 are in flight while ks is converted
-      uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, bv = a0;
-      if (a_ok) { a0 = __ldg(a_src); a1 = __ldg(a_src + 1); }
-      if (b_ok) bv = __ldg(b_src);
-      for (int ks = 0; ks < p.KB; ++ks) {
-        uint4 na0 = make_uint4(0, 0, 0, 0), na1 = na0, nbv = na0;
-        if (ks + 1 < p.KB) {
-          if (a_ok) { na0 = __ldg(a_src + (ks + 1) * 4); na1 = __ldg(a_src + (ks + 1) * 4 + 1); }
-          if (b_ok) nbv = __ldg(b_src + (int64_t)(ks + 1) * p.N);
-        }
-        if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl, p.status)) { ok = false; break; }
-        const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
-        const uint32_t b_tile = a_tile + kABytes;
-        {
-          // A: 32 int8 (half a row) -> 4 chunks of 8 fp16
-          const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          const uint32_t row_addr = a_tile + (uint32_t)a_row * 128u;
+      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+      for (int i = 0; i < (kTileM * kKStep / 16) / kLoadThreads; ++i) {
+        const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
+        const int row = idx >> 2, q = idx & 3;
+        const int am = m0 + row;
+        const bool ok = am < p.M;
+        cp_async16(raw + (uint32_t)(row * kKStep + q * 16),
+                   p.xq + (int64_t)(ok ? am : 0) * p.K + (int64_t)ks * kKStep + q * 16, ok ? 16u : 0u);
+      }
+      for (int row = v; row < p.n_tile; row += kLoadThreads) {
+        const int bn = n0 + row;
+        const bool ok = bn < p.N;
+        cp_async16(raw + kRawABytes + (uint32_t)(row * 16), p.packed + (int64_t)ks * p.N + (ok ? bn : 0),
+                   ok ? 16u : 0u);
+      }
+      cp_async_arrive(&ctl.raw_full[slot]);
+    }
+  } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
+    // ------------------------------------------------------------------ converters
+    // Thread u widens two 16-byte pieces of activation row u/2 (pieces h and
+    // h+2, h = u%2) and the 16-byte packed chunk of weight row u.
+    const int u = threadIdx.x - kEpiWarps * 32;  // 0 .. 255
+    const int a_row = u >> 1, h = u & 1;
+    const int b_row = u;
+    const bool b_active = b_row < p.n_tile;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int f = 0; f < total; ++f) {
+      const int slot = f % kRawStages;
+      const uint32_t use = (uint32_t)(f / kRawStages);
+      const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
+      int m0, n0;
+      tile_coords(p, tile, m0, n0);
+      if (!mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status)) break;
+      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
+      const uint4 pa0 = ld_shared_v4(raw + (uint32_t)(a_row * kKStep + 16 * h));
+      const uint4 pa1 = ld_shared_v4(raw + (uint32_t)(a_row * kKStep + 32 + 16 * h));
+      uint4 pb = make_uint4(0, 0, 0, 0);
+      if (b_active) pb = ld_shared_v4(raw + kRawABytes + (uint32_t)(b_row * 16));
+      mbar_arrive(&ctl.raw_empty[slot]);
+      if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl, p.status)) break;
+      const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
+      const uint32_t b_tile = a_tile + kABytes;
+      {
+        // A: pieces h and h+2 (16 int8 each) -> fp16 chunks 2q, 2q+1
+        const uint32_t row_addr = a_tile + (uint32_t)a_row * 128u;
+        const uint4 pieces[2] = {pa0, pa1};
+#pragma unroll
+        for (int pi = 0; pi < 2; ++pi) {
+          const int q = h + 2 * pi;
+          const uint32_t wv[4] = {pieces[pi].x, pieces[pi].y, pieces[pi].z, pieces[pi].w};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
             uint32_t l0, h0, l1, h1;
-            i8x4_to_f16x4(wv[2 * q], l0, h0);
-            i8x4_to_f16x4(wv[2 * q + 1], l1, h1);
-            const int c = 4 * a_half + q;
+            i8x4_to_f16x4(wv[2 * half], l0, h0);
+            i8x4_to_f16x4(wv[2 * half + 1], l1, h1);
+            const int c = 2 * q + half;
             st_shared_v4(row_addr + ((uint32_t)((c ^ (a_row & 7)) << 4)), l0, h0, l1, h1);
           }
         }
-        if (b_active) {
-          const uint32_t row_addr = b_tile + (uint32_t)b_row * 128u;
-          if (b_ok) {
-            store_weight_row(row_addr, b_row, bv);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (uint32_t)(c << 4), 0u, 0u, 0u, 0u);
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&ctl.full[stage]);
-        a0 = na0; a1 = na1; bv = nbv;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
+      if (b_active) {
+        const uint32_t row_addr = b_tile + (uint32_t)b_row * 128u;
+        if (n0 + b_row < p.N) {
+          store_weight_row(row_addr, b_row, pb);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (uint32_t)(c << 4), 0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ctl.full[stage]);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -483,7 +552,7 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
   p.tiles_m = (int)((M + kTileM - 1) / kTileM);
   p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
   p.num_tiles = p.tiles_m * p.tiles_n;
-  const size_t smem = (size_t)kStages * kStageBytes + 1024;
+  const size_t smem = (size_t)kSmemBytes + 1024;
   static thread_local int configured = -1;
   if (configured != dev.device) {
     cudaError_t err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -31,6 +31,15 @@ def normal(shape, std: float, seed: int) -> torch.Tensor:
     return torch.randn(*shape, generator=_gen(seed), dtype=torch.float32) * std
 
 
+def normal_cuda(shape, std: float, seed: int, device) -> torch.Tensor:
+    """fp32 N(0, std^2) drawn on a CUDA device from a seeded CUDA generator (for
+    workloads too large to draw on the CPU; deterministic for a given device type
+    and torch version)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=device) * std
+
+
 def uniform(shape, lo: float, hi: float, seed: int) -> torch.Tensor:
     """fp32 U(lo, hi) on the CPU."""
     return torch.rand(*shape, generator=_gen(seed), dtype=torch.float32) * (hi - lo) + lo

@@ -117,7 +117,7 @@ bitlinear_status bitlinear_quantize_weights(const float* W, int64_t N, int64_t K
  *   rms_eps     the RMSNorm epsilon (ignored without rms_weight), >= 0.
  *   xq          device, int8 [M, K] row-major, written.
  *   x_scale     device, fp32 [M], receives sx per row.
- * K % 64 == 0 and K <= 65536 (the exact sum of squares holds 2^16 terms).
+ * K % 64 == 0 and K <= 32768 (the row is staged in shared memory as fp32).
  */
 bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M, int64_t K,
                                      const float* rms_weight, double rms_eps,
@@ -131,8 +131,9 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *   acc           device int32 [M, N] or NULL; when given it receives the raw
  *                 integer accumulators (for checking and debugging).
  * The kernel is chosen from M (BITLINEAR_ALGO_AUTO): the decode kernel
- * (packed weights streamed through registers, dp4a on the 2-bit codes) for
- * small M, the tcgen05 tensor-core kernel for large M.
+ * (packed weights streamed into shared memory by bulk asynchronous copies,
+ * dp4a on the 2-bit codes; K <= 65536) for M <= 64, the tcgen05 tensor-core
+ * kernel (K <= 131072) otherwise.
  */
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale,
@@ -159,6 +160,37 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
                                       const uint8_t* packed, const float* w_scale,
                                       int64_t N, int64_t K, float* y, int32_t* acc,
                                       int algo, int flags, void* stream);
+
+/* One weight matrix of a bitlinear_linear call. */
+typedef struct bitlinear_weight {
+  const uint8_t* packed;  /* device, bitlinear_packed_bytes(N, K) bytes */
+  const float* w_scale;   /* device, 1 fp32 (sw) */
+  int64_t N;              /* output features, > 0 */
+  float* y;               /* device fp32 [M, N] row-major, written */
+  int32_t* acc;           /* device int32 [M, N] or NULL (raw accumulators) */
+} bitlinear_weight;
+
+/*
+ * A whole BitLinear call: activation_quant (with the optional gating and
+ * RMSNorm prologues) and the contraction + rescale for 1..4 weight matrices
+ * that share the input (q, k, v; gate, up; or a single projection).  The
+ * results are exactly those of bitlinear_quant_act(x, mul, M, K, rms_weight,
+ * rms_eps, xq, x_scale) followed by bitlinear_forward for each matrix; xq and
+ * x_scale receive the quantised activations.
+ * With M == 1 and K <= 16384 this is one kernel launch: every CTA streams its
+ * share of the packed weights while it quantises the token itself (CTA 0
+ * writes xq, x_scale), which keeps a separate act_quant kernel and its
+ * latency off the decode critical path; the matrices' CTAs share one grid.
+ * Otherwise it runs bitlinear_quant_act, then one decode launch for all
+ * matrices (M <= 64) or one tensor-core launch per matrix.
+ * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
+ * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
+ * scales must not come from the kernel immediately before on the stream).
+ */
+bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,
+                                  const float* rms_weight, double rms_eps,
+                                  const bitlinear_weight* weights, int num_weights,
+                                  int8_t* xq, float* x_scale, int flags, void* stream);
 
 /* Size of the library's own device scratch array used by
  * bitlinear_quantize_weights_noalloc. */
@@ -192,6 +224,14 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
  */
 bitlinear_status bitlinear_quantize_weights_noalloc(const float* W, int64_t N, int64_t K,
                                                     uint8_t* packed, float* w_scale, void* stream);
+
+/* Exercises the failure-detection path without faulting anything: launches a
+ * one-warp kernel that waits on an mbarrier nothing ever arrives on, with the
+ * same bounded wait the kernels use, giving up after limit_ns (0 < limit_ns
+ * <= 1 s).  The expired wait records BITLINEAR_ERR_TIMEOUT in the device
+ * status word (read it with bitlinear_device_status); the CUDA context stays
+ * usable. */
+bitlinear_status bitlinear_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
 /* Synchronises `stream`, then returns BITLINEAR_ERR_TIMEOUT if any kernel of
  * this library recorded a timed-out wait on the current device since the last

@@ -218,3 +218,52 @@ def test_repeat_calls_are_deterministic():
     a = full_parity(W, x)
     b = full_parity(W, x, flags=bl.FLAG_PDL)
     np.testing.assert_array_equal(a["y"], b["y"])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing satisfies gives up after its limit, records
+    BITLINEAR_ERR_TIMEOUT, and the context keeps working."""
+    assert bl.bitlinear_device_status(clear=True) == 0
+    bl.bitlinear_selftest_wait_timeout(20_000_000)  # 20 ms
+    assert bl.bitlinear_device_status(clear=True) == -6
+    assert bl.bitlinear_device_status(clear=True) == 0
+    W = synth.weight(64, 128, 4)
+    x = synth.activations(2, 128, 5)
+    full_parity(W, x)
+
+
+@pytest.mark.parametrize("M,K,Ns,prolog", [
+    (1, 2560, (10240, 10240), None),        # gate || up of a BitNet-3B decode step, one launch
+    (1, 10240, (2560,), "gated"),           # down projection fed ReLU^2(gate)*up
+    (1, 2048, (300, 1000, 64), "norm"),     # three matrices, RMSNorm prologue
+    (1, 8192, (2048,), "gated+norm"),       # the 1.3B FFN sub-norm path
+    (1, 128, (5,), None),                   # tiny
+    (3, 640, (500, 77), None),              # M > 1: act_quant + one decode launch for both
+    (130, 320, (257, 100), "norm"),         # tensor-core path per matrix
+])
+def test_linear_matches_oracle(M, K, Ns, prolog):
+    """bitlinear_linear (act_quant + forward for matrices sharing one input) against the oracle."""
+    x = synth.activations(M, K, 60 + K, outlier_seed=61 + K)
+    mul = synth.activations(M, K, 62 + K) if prolog and "gated" in prolog else None
+    gamma = synth.uniform((K,), 0.5, 1.5, 63 + K) if prolog and "norm" in prolog else None
+    xq_o, sx_o = oracle.act_quant(x.numpy(), mul=None if mul is None else mul.numpy(),
+                                  gamma=None if gamma is None else gamma.numpy(), eps=1e-6)
+    mats, refs = [], []
+    for i, N in enumerate(Ns):
+        W = synth.weight(N, K, 70 + i + K)
+        Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+        refs.append(oracle.forward(xq_o, sx_o, oracle.pack(Wq_o), sw_o, N, K))
+        _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        y = torch.full((M, N), 5.5, device="cuda")
+        acc = torch.full((M, N), -3, dtype=torch.int32, device="cuda")
+        mats.append((packed_d, sw_d, y, acc))
+    xq = torch.zeros(M, K, dtype=torch.int8, device="cuda")
+    sx = torch.zeros(M, dtype=torch.float32, device="cuda")
+    bl.bitlinear_linear(x.cuda(), mats, xq, sx, mul=None if mul is None else mul.cuda(),
+                        rms_weight=None if gamma is None else gamma.cuda(), rms_eps=1e-6, flags=bl.FLAG_PDL)
+    assert bl.bitlinear_device_status() == 0
+    np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
+    np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
+    for (packed_d, sw_d, y, acc), (acc_o, y_o) in zip(mats, refs):
+        np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
+        assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
