@@ -265,7 +265,8 @@ def ncu_traffic(kernel_sources, profile_name):
         return None
 
 
-DECODE_SOURCES = ["bitlinear_w1_a8_gb300/csrc/decode.cu", "bitlinear_w1_a8_gb300/csrc/common.cuh"]
+DECODE_SOURCES = ["bitlinear_w1_a8_gb300/csrc/decode.cu", "bitlinear_w1_a8_gb300/csrc/quant_row.cuh",
+                  "bitlinear_w1_a8_gb300/csrc/common.cuh"]
 
 
 def measured_peak_tensor():
