@@ -14,16 +14,18 @@
 // sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
 // int32 result is therefore bit-exact.
 //
-// CTA roles (one persistent CTA per SM, 15 warps):
+// CTA roles (one persistent CTA per SM, 14 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
 //   warps 4-11  converters: widen the raw int8 / packed tiles to fp16 and
 //               store them in the 128-byte-swizzled K-major layout the MMA
 //               reads
-//   warps 12-13 loaders: copy raw tiles from global memory into a 4-deep
-//               shared-memory ring with cp.async; the copies complete on the
-//               ring's mbarriers, so the converters never have loads of their
-//               own in flight when they fence their stores for the MMA
-//   warp 14     allocates TMEM; one lane issues tcgen05.mma
+//   warp 12     one lane issues the loads of the raw tiles into a 4-deep
+//               shared-memory ring: the int8 activation tile by a 2-D TMA
+//               tensor map, the packed weight chunks of the k-block (contiguous
+//               in the packed layout) by one bulk copy
+//   warp 13     allocates TMEM; one lane issues tcgen05.mma
+// Every hand-off between roles is one mbarrier arrival per warp (or the TMA
+// byte count), never one per thread.
 // Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles
 // and kRawStages raw stages (A 128x64 int8, B n_tile x 16 B packed);
 // TMEM holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
@@ -31,6 +33,11 @@
 // global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace bitlinear {
@@ -50,12 +57,9 @@ constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kConvWarps = 8;
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kLoadWarps = 2;
-constexpr int kLoadThreads = kLoadWarps * 32;
-constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 12
-constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 14
-constexpr int kThreads = (kMmaWarp + 1) * 32;       // 480
+constexpr int kProdWarp = kEpiWarps + kConvWarps;  // 12: TMA producer (one lane)
+constexpr int kMmaWarp = kProdWarp + 1;            // 13
+constexpr int kThreads = (kMmaWarp + 1) * 32;      // 448
 constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
 
@@ -197,15 +201,24 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// 16-byte global -> shared asynchronous copy; src_bytes = 0 writes zeros and
-// reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive(unsigned long long* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+// Tiled TMA loads (the tensor maps are __grid_constant__ kernel parameters);
+// the copies complete on the mbarrier with their byte count.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Contiguous global -> shared bulk copy (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, unsigned long long* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
@@ -285,7 +298,8 @@ __device__ __forceinline__ void tile_coords(const PrefillParams& p, int tile, in
   n0 = tn * p.n_tile;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SharedCtl ctl;
   const int warp = threadIdx.x >> 5;
@@ -296,16 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.full[s], kConvThreads);
+      mbar_init(&ctl.full[s], kConvWarps);
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&ctl.raw_full[s], kLoadThreads);
-      mbar_init(&ctl.raw_empty[s], kConvThreads);
+      mbar_init(&ctl.raw_full[s], 1);
+      mbar_init(&ctl.raw_empty[s], kConvWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.tmem_full[s], 1);
-      mbar_init(&ctl.tmem_empty[s], kEpiWarps * 32);
+      mbar_init(&ctl.tmem_empty[s], kEpiWarps);
     }
     mbar_init(&ctl.mma_done, 1);
     ctl.abort_flag = 0;
@@ -324,39 +338,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
   const int my_tiles = (int)blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
 
-  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
-    // ------------------------------------------------------------------ loaders
-    // Copy the raw k-step (128 x 64 int8 activations, n_tile x 16 B packed codes)
-    // into the raw ring with cp.async; the ring slot's barrier completes when
-    // every loader's copies have landed.  Rows past M or N are zero-filled.
-    const int v = threadIdx.x - kLoadWarp0 * 32;  // 0 .. 63
-    for (int f = 0; f < total; ++f) {
-      const int slot = f % kRawStages;
-      const uint32_t use = (uint32_t)(f / kRawStages);
-      if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) break;
-      const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
-      const int ks = f % p.KB;
-      int m0, n0;
-      tile_coords(p, tile, m0, n0);
-      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
-#pragma unroll
-      for (int i = 0; i < (kTileM * kKStep / 16) / kLoadThreads; ++i) {
-        const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
-        const int row = idx >> 2, q = idx & 3;
-        const int am = m0 + row;
-        const bool ok = am < p.M;
-        cp_async16(raw + (uint32_t)(row * kKStep + q * 16),
-                   p.xq + (int64_t)(ok ? am : 0) * p.K + (int64_t)ks * kKStep + q * 16, ok ? 16u : 0u);
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    // One lane loads each raw k-step: the 128 x 64 int8 activation tile (rows
+    // past M read as zeros) and the packed chunks of the tile's rows below N.
+    if (lane == 0) {
+      for (int f = 0; f < total; ++f) {
+        const int slot = f % kRawStages;
+        const uint32_t use = (uint32_t)(f / kRawStages);
+        if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) break;
+        const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
+        const int ks = f % p.KB;
+        int m0, n0;
+        tile_coords(p, tile, m0, n0);
+        const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
+        // the packed chunks of rows n0 .. n0 + n_tile - 1 of k-block ks are contiguous
+        const int b_rows = min(p.n_tile, p.N - n0);
+        const uint32_t b_bytes = (uint32_t)b_rows * 16u;
+        mbar_expect_tx(&ctl.raw_full[slot], (uint32_t)kRawABytes + b_bytes);
+        tma_load_2d(raw, &map_a, ks * kKStep, m0, &ctl.raw_full[slot]);
+        bulk_load(raw + kRawABytes, p.packed + (int64_t)ks * p.N + n0, b_bytes, &ctl.raw_full[slot]);
       }
-      for (int row = v; row < p.n_tile; row += kLoadThreads) {
-        const int bn = n0 + row;
-        const bool ok = bn < p.N;
-        cp_async16(raw + kRawABytes + (uint32_t)(row * 16), p.packed + (int64_t)ks * p.N + (ok ? bn : 0),
-                   ok ? 16u : 0u);
-      }
-      cp_async_arrive(&ctl.raw_full[slot]);
     }
-  } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
+    __syncwarp();
+  } else if (warp >= kEpiWarps && warp < kProdWarp) {
     // ------------------------------------------------------------------ converters
     // Thread u widens two 16-byte pieces of activation row u/2 (pieces h and
     // h+2, h = u%2) and the 16-byte packed chunk of weight row u.
@@ -378,7 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
       const uint4 pa1 = ld_shared_v4(raw + (uint32_t)(a_row * kKStep + 32 + 16 * h));
       uint4 pb = make_uint4(0, 0, 0, 0);
       if (b_active) pb = ld_shared_v4(raw + kRawABytes + (uint32_t)(b_row * 16));
-      mbar_arrive(&ctl.raw_empty[slot]);
+      // The next TMA write into this slot is an async-proxy write after these
+      // generic-proxy reads: order them before releasing the slot.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.raw_empty[slot]);  // one arrival per warp
       if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl, p.status)) break;
       const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
       const uint32_t b_tile = a_tile + kABytes;
@@ -410,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&ctl.full[stage]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.full[stage]);  // one arrival per warp
       if (++stage == kStages) { stage = 0; phase ^= 1u; }
     }
   } else if (warp == kMmaWarp) {
@@ -501,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         }
       }
       tc_fence_before();
-      mbar_arrive(&ctl.tmem_empty[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.tmem_empty[slot]);  // one arrival per warp
     }
   }
 
@@ -559,6 +570,32 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
     if (err != cudaSuccess) return err;
     configured = dev.device;
   }
+  // Tensor map of A = xq as a 2-D uint8 tensor {K, M}, box {64, 128}; rows past
+  // M read as zeros.  (B needs none: one k-block of n_tile rows is contiguous.)
+  static std::mutex enc_mutex;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(enc_mutex);
+    if (!encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return cudaErrorNotSupported;
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  CUtensorMap map_a;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {(cuuint32_t)kKStep, (cuuint32_t)kTileM};
+    const cuuint32_t es[2] = {1, 1};
+    if (encode(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(xq), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -570,7 +607,7 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, p, map_a);
 }
 
 }  // namespace bitlinear
