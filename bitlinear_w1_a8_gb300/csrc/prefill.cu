@@ -14,37 +14,30 @@
 // sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
 // int32 result is therefore bit-exact.
 //
-// CTA roles (one persistent CTA per SM, 14 warps):
+// CTA roles (one persistent CTA per SM, 21 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
-//   warps 4-11  converters: widen the raw int8 / packed tiles to fp16 and
-//               store them in the 128-byte-swizzled K-major layout the MMA
-//               reads
-//   warp 12     one lane issues the loads of the raw tiles into a 4-deep
-//               shared-memory ring: the int8 activation tile by a 2-D TMA
-//               tensor map, the packed weight chunks of the k-block (contiguous
-//               in the packed layout) by one bulk copy
-//   warp 13     allocates TMEM; one lane issues tcgen05.mma
-// Every hand-off between roles is one mbarrier arrival per warp (or the TMA
-// byte count), never one per thread.
+//   warps 4-15  converters, three groups of four: group g widens the raw
+//               int8 / packed tiles of every third k-step to fp16 in stage g,
+//               in the 128-byte-swizzled K-major layout the MMA reads
+//   warps 16-19 loaders: copy raw tiles from global memory into a 6-deep
+//               shared-memory ring with 16-byte cp.async, 3 k-steps in
+//               flight per warp (many small TMA requests proved slower)
+//   warp 20     allocates TMEM; one lane issues tcgen05.mma
+// Every hand-off between roles is one mbarrier arrival per warp.
 // Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles
-// and kRawStages raw stages (A 128x64 int8, B n_tile x 16 B packed);
-// TMEM holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
+// and kRawStages raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM
+// holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
 // overlaps the MMAs of the next.  Every mbarrier wait is bounded by the
 // global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "common.cuh"
 
 namespace bitlinear {
 namespace {
 
 constexpr int kStages = 3;                       // fp16 operand stages read by the MMA
-constexpr int kRawStages = 4;                    // raw int8 / packed k-steps in flight per converter
+constexpr int kRawStages = 6;                    // raw int8 / packed k-steps in the ring
 constexpr int kTileM = 128;
 constexpr int kMaxTileN = 256;
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
@@ -56,10 +49,23 @@ constexpr int kRawBBytes = kMaxTileN * 16;       // 4 KB of packed codes
 constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
-constexpr int kConvWarps = 8;
-constexpr int kProdWarp = kEpiWarps + kConvWarps;  // 12: TMA producer (one lane)
-constexpr int kMmaWarp = kProdWarp + 1;            // 13
-constexpr int kThreads = (kMmaWarp + 1) * 32;      // 448
+constexpr int kConvGroups = kStages;                // group g converts the k-steps f with f % kStages == g
+constexpr int kGroupWarps = 4;
+constexpr int kGroupThreads = kGroupWarps * 32;     // 128
+constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 12
+constexpr int kLoadWarps = 4;
+constexpr int kLoadThreads = kLoadWarps * 32;       // 128
+constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 16
+constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 20
+constexpr int kThreads = (kMmaWarp + 1) * 32;       // 672
+constexpr int kLoadDepth = 4;                       // k-steps in flight per loader warp
+constexpr int kPiecesPerThread = kTileM * kKStep / 16 / kGroupThreads;  // 4 activation pieces
+constexpr int kHalvesPerThread = 2 * kMaxTileN / kGroupThreads;        // <= 4 weight half-rows
+static_assert(kTileM * kKStep / 16 == kPiecesPerThread * kGroupThreads, "activation pieces split evenly");
+static_assert(2 * kMaxTileN == kHalvesPerThread * kGroupThreads, "weight half-rows split evenly");
+static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
+static_assert(kLoadDepth < kRawStages + 1, "copies in flight fit the raw ring");
+static_assert(kThreads * 96 <= 65536, "registers for one CTA per SM");
 constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
 
@@ -201,24 +207,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+// 16-byte global -> shared asynchronous copy; src_bytes = 0 writes zeros and
+// reads nothing.  Completion: cp.async.wait_group of the issuing thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-// Tiled TMA loads (the tensor maps are __grid_constant__ kernel parameters);
-// the copies complete on the mbarrier with their byte count.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            unsigned long long* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-// Contiguous global -> shared bulk copy (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, unsigned long long* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
@@ -269,24 +266,26 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t word) {
 // One 16-byte packed chunk (64 weights of a row) -> 8 chunks of 8 fp16.
 // Chunk c holds k = 8c..8c+7: word w = c/2, k%16 = 8(c%2) + t, t = 0..7,
 // i.e. codes at bit 8*(t%4) + 2*(2(c%2) + t/4) of word w.
-__device__ __forceinline__ void store_weight_row(uint32_t row_addr, int r, const uint4 v) {
-  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+// Half of a packed chunk (words 2*half, 2*half+1: k = 32*half .. 32*half+31)
+// -> fp16 chunks 4*half .. 4*half+3 of weight row r.
+__device__ __forceinline__ void store_weight_half(uint32_t row_addr, int r, int half, const uint2 v) {
+  const uint32_t words[2] = {v.x, v.y};
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t w = words[c >> 1];
-    const int j0 = 2 * (c & 1);  // i/4 of t = 0..3; j0 + 1 for t = 4..7
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint32_t w = words[cc >> 1];
     uint32_t q0, q1, q2, q3;
-    if (j0 == 0) {
-      q0 = codes_to_f16x2<0>(w);    // t = 0, 1 : bits 0, 8
-      q1 = codes_to_f16x2<16>(w);   // t = 2, 3 : bits 16, 24
-      q2 = codes_to_f16x2<2>(w);    // t = 4, 5 : bits 2, 10
-      q3 = codes_to_f16x2<18>(w);   // t = 6, 7 : bits 18, 26
+    if ((cc & 1) == 0) {
+      q0 = codes_to_f16x2<0>(w);
+      q1 = codes_to_f16x2<16>(w);
+      q2 = codes_to_f16x2<2>(w);
+      q3 = codes_to_f16x2<18>(w);
     } else {
       q0 = codes_to_f16x2<4>(w);
       q1 = codes_to_f16x2<20>(w);
       q2 = codes_to_f16x2<6>(w);
       q3 = codes_to_f16x2<22>(w);
     }
+    const int c = 4 * half + cc;
     st_shared_v4(row_addr + ((uint32_t)((c ^ (r & 7)) << 4)), q0, q1, q2, q3);
   }
 }
@@ -299,7 +298,7 @@ __device__ __forceinline__ void tile_coords(const PrefillParams& p, int tile, in
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap map_a) {
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SharedCtl ctl;
   const int warp = threadIdx.x >> 5;
@@ -310,12 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.full[s], kConvWarps);
+      mbar_init(&ctl.full[s], kGroupWarps);
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&ctl.raw_full[s], 1);
-      mbar_init(&ctl.raw_empty[s], kConvWarps);
+      mbar_init(&ctl.raw_full[s], kLoadWarps);
+      mbar_init(&ctl.raw_empty[s], kGroupWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl.tmem_full[s], 1);
@@ -338,40 +337,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_tiles = (int)blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
 
-  if (warp == kProdWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    // One lane loads each raw k-step: the 128 x 64 int8 activation tile (rows
-    // past M read as zeros) and the packed chunks of the tile's rows below N.
-    if (lane == 0) {
-      for (int f = 0; f < total; ++f) {
+  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
+    // ------------------------------------------------------------------ loaders
+    // Copy each raw k-step (128 x 64 int8 activations, n_tile x 16 B packed
+    // codes) into the raw ring with 16-byte cp.async (coalesced: a warp covers
+    // 8 activation rows or 32 weight rows), kLoadDepth k-steps in flight per
+    // warp; a slot is handed over once every loader warp's copies have landed.
+    const int v = threadIdx.x - kLoadWarp0 * 32;  // 0 .. 127
+    bool ok = true;
+    for (int f = 0; f < total + kLoadDepth - 1 && ok; ++f) {
+      if (f < total) {
         const int slot = f % kRawStages;
         const uint32_t use = (uint32_t)(f / kRawStages);
-        if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) break;
+        if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) { ok = false; break; }
         const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
         const int ks = f % p.KB;
         int m0, n0;
         tile_coords(p, tile, m0, n0);
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
-        // the packed chunks of rows n0 .. n0 + n_tile - 1 of k-block ks are contiguous
-        const int b_rows = min(p.n_tile, p.N - n0);
-        const uint32_t b_bytes = (uint32_t)b_rows * 16u;
-        mbar_expect_tx(&ctl.raw_full[slot], (uint32_t)kRawABytes + b_bytes);
-        tma_load_2d(raw, &map_a, ks * kKStep, m0, &ctl.raw_full[slot]);
-        bulk_load(raw + kRawABytes, p.packed + (int64_t)ks * p.N + n0, b_bytes, &ctl.raw_full[slot]);
+#pragma unroll
+        for (int i = 0; i < (kTileM * kKStep / 16) / kLoadThreads; ++i) {
+          const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
+          const int row = idx >> 2, q = idx & 3;
+          const int am = m0 + row;
+          const bool in = am < p.M;
+          cp_async16(raw + (uint32_t)(row * kKStep + q * 16),
+                     p.xq + (int64_t)(in ? am : 0) * p.K + (int64_t)ks * kKStep + q * 16, in ? 16u : 0u);
+        }
+        for (int row = v; row < p.n_tile; row += kLoadThreads) {
+          const int bn = n0 + row;
+          const bool in = bn < p.N;
+          cp_async16(raw + kRawABytes + (uint32_t)(row * 16), p.packed + (int64_t)ks * p.N + (in ? bn : 0),
+                     in ? 16u : 0u);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      const int g = f - (kLoadDepth - 1);  // the oldest k-step in flight
+      if (g >= 0) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLoadDepth - 1) : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.raw_full[g % kRawStages]);
       }
     }
-    __syncwarp();
-  } else if (warp >= kEpiWarps && warp < kProdWarp) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
     // ------------------------------------------------------------------ converters
-    // Thread u widens two 16-byte pieces of activation row u/2 (pieces h and
-    // h+2, h = u%2) and the 16-byte packed chunk of weight row u.
-    const int u = threadIdx.x - kEpiWarps * 32;  // 0 .. 255
-    const int a_row = u >> 1, h = u & 1;
-    const int b_row = u;
-    const bool b_active = b_row < p.n_tile;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int f = 0; f < total; ++f) {
+    // Group g (4 warps) converts the flat k-steps f = g, g + kStages, ... into
+    // stage g, so the groups work on different k-steps at once.  Thread u of a
+    // group widens activation pieces u + 128j (16 int8: row p/4, k = 16(p%4)
+    // ..) and weight half-rows u + 128j (half h of row r: k = 32h .. 32h+31 of
+    // the row's packed chunk).
+    const int cw = warp - kEpiWarps;
+    const int grp = cw / kGroupWarps;
+    const int u = (cw % kGroupWarps) * 32 + lane;  // 0 .. 127
+    const int nh = 2 * p.n_tile;                   // weight half-rows, <= 512
+    for (int f = grp; f < total; f += kConvGroups) {
       const int slot = f % kRawStages;
       const uint32_t use = (uint32_t)(f / kRawStages);
       const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
@@ -379,49 +399,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(p, tile, m0, n0);
       if (!mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status)) break;
       const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
-      const uint4 pa0 = ld_shared_v4(raw + (uint32_t)(a_row * kKStep + 16 * h));
-      const uint4 pa1 = ld_shared_v4(raw + (uint32_t)(a_row * kKStep + 32 + 16 * h));
-      uint4 pb = make_uint4(0, 0, 0, 0);
-      if (b_active) pb = ld_shared_v4(raw + kRawABytes + (uint32_t)(b_row * 16));
-      // The next TMA write into this slot is an async-proxy write after these
-      // generic-proxy reads: order them before releasing the slot.
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.raw_empty[slot]);  // one arrival per warp
-      if (!mbar_wait(&ctl.empty[stage], phase ^ 1u, &ctl, p.status)) break;
-      const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
+      const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
+      if (!mbar_wait(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl, p.status)) break;
+      const uint32_t a_tile = stage_base + (uint32_t)grp * kStageBytes;
       const uint32_t b_tile = a_tile + kABytes;
-      {
-        // A: pieces h and h+2 (16 int8 each) -> fp16 chunks 2q, 2q+1
-        const uint32_t row_addr = a_tile + (uint32_t)a_row * 128u;
-        const uint4 pieces[2] = {pa0, pa1};
 #pragma unroll
-        for (int pi = 0; pi < 2; ++pi) {
-          const int q = h + 2 * pi;
-          const uint32_t wv[4] = {pieces[pi].x, pieces[pi].y, pieces[pi].z, pieces[pi].w};
+      for (int j = 0; j < kPiecesPerThread; ++j) {
+        const int pc = u + j * kGroupThreads;
+        const int row = pc >> 2, q = pc & 3;
+        const uint32_t row_addr = a_tile + (uint32_t)row * 128u;
+        const uint4 av = ld_shared_v4(raw + (uint32_t)(pc * 16));  // raw piece p sits at 16p
+        const uint32_t wv[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t l0, h0, l1, h1;
-            i8x4_to_f16x4(wv[2 * half], l0, h0);
-            i8x4_to_f16x4(wv[2 * half + 1], l1, h1);
-            const int c = 2 * q + half;
-            st_shared_v4(row_addr + ((uint32_t)((c ^ (a_row & 7)) << 4)), l0, h0, l1, h1);
-          }
+        for (int half = 0; half < 2; ++half) {
+          uint32_t l0, h0, l1, h1;
+          i8x4_to_f16x4(wv[2 * half], l0, h0);
+          i8x4_to_f16x4(wv[2 * half + 1], l1, h1);
+          const int c = 2 * q + half;
+          st_shared_v4(row_addr + ((uint32_t)((c ^ (row & 7)) << 4)), l0, h0, l1, h1);
         }
       }
-      if (b_active) {
-        const uint32_t row_addr = b_tile + (uint32_t)b_row * 128u;
-        if (n0 + b_row < p.N) {
-          store_weight_row(row_addr, b_row, pb);
-        } else {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (uint32_t)(c << 4), 0u, 0u, 0u, 0u);
+      for (int j = 0; j < kHalvesPerThread; ++j) {
+        const int h = u + j * kGroupThreads;
+        if (h >= nh) continue;
+        const int row = h >> 1, half = h & 1;
+        const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
+        if (n0 + row < p.N) {
+          store_weight_half(row_addr, row, half, ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)));
+        } else {  // rows past N are zeros
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) st_shared_v4(row_addr + (uint32_t)((4 * half + cc) << 4), 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.full[stage]);  // one arrival per warp
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (lane == 0) {  // one arrival per warp on each
+        mbar_arrive(&ctl.raw_empty[slot]);
+        mbar_arrive(&ctl.full[grp]);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -524,16 +540,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Output-tile width: the multiple of 16 (<= 256) that minimises
-// (number of waves over the SMs) x (tile width), preferring wider tiles.
+// Output-tile width: the multiple of 16 in 64..256 that minimises
+// (waves of tiles over the SMs) x (tile width + 64), preferring wider tiles.
+// Every k-step of a tile widens the 128 x 64 activation block whatever the
+// width, so the width carries a fixed cost of about 64 weight columns.
 int choose_n_tile(int64_t M, int64_t N, int sms) {
   const int64_t tiles_m = (M + kTileM - 1) / kTileM;
-  int best = 256;
+  int best = kMaxTileN;
   int64_t best_cost = -1;
-  for (int nt = 256; nt >= 64; nt -= 16) {
+  for (int nt = kMaxTileN; nt >= 64; nt -= 16) {
     const int64_t tiles = tiles_m * ((N + nt - 1) / nt);
     const int64_t waves = (tiles + sms - 1) / sms;
-    const int64_t cost = waves * nt;
+    const int64_t cost = waves * (nt + 64);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = nt;
@@ -570,32 +588,6 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
     if (err != cudaSuccess) return err;
     configured = dev.device;
   }
-  // Tensor map of A = xq as a 2-D uint8 tensor {K, M}, box {64, 128}; rows past
-  // M read as zeros.  (B needs none: one k-block of n_tile rows is contiguous.)
-  static std::mutex enc_mutex;
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(enc_mutex);
-    if (!encode) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return cudaErrorNotSupported;
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
-  CUtensorMap map_a;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K};
-    const cuuint32_t box[2] = {(cuuint32_t)kKStep, (cuuint32_t)kTileM};
-    const cuuint32_t es[2] = {1, 1};
-    if (encode(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(xq), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
   const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -607,7 +599,7 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, p, map_a);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
 }
 
 }  // namespace bitlinear
