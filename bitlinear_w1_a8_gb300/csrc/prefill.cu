@@ -20,8 +20,9 @@
 //               int8 / packed tiles of every third k-step to fp16 in stage g,
 //               in the 128-byte-swizzled K-major layout the MMA reads
 //   warps 16-19 loaders: copy raw tiles from global memory into a 6-deep
-//               shared-memory ring with 16-byte cp.async, 3 k-steps in
-//               flight per warp (many small TMA requests proved slower)
+//               shared-memory ring with 16-byte cp.async; each thread's
+//               copies arrive on the slot's barrier as they land, so the
+//               whole ring can be in flight
 //   warp 20     allocates TMEM; one lane issues tcgen05.mma
 // Every hand-off between roles is one mbarrier arrival per warp.
 // Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles
@@ -39,7 +40,7 @@ namespace {
 constexpr int kStages = 3;                       // fp16 operand stages read by the MMA
 constexpr int kRawStages = 6;                    // raw int8 / packed k-steps in the ring
 constexpr int kTileM = 128;
-constexpr int kMaxTileN = 256;
+constexpr int kMaxTileN = 256;                    // multiple of 16, <= 256
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
 constexpr int kABytes = kTileM * 128;            // 16 KB
 constexpr int kBBytes = kMaxTileN * 128;         // 32 KB
@@ -58,13 +59,10 @@ constexpr int kLoadThreads = kLoadWarps * 32;       // 128
 constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 16
 constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 20
 constexpr int kThreads = (kMmaWarp + 1) * 32;       // 672
-constexpr int kLoadDepth = 4;                       // k-steps in flight per loader warp
 constexpr int kPiecesPerThread = kTileM * kKStep / 16 / kGroupThreads;  // 4 activation pieces
-constexpr int kHalvesPerThread = 2 * kMaxTileN / kGroupThreads;        // <= 4 weight half-rows
+constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kTileM * kKStep / 16 == kPiecesPerThread * kGroupThreads, "activation pieces split evenly");
-static_assert(2 * kMaxTileN == kHalvesPerThread * kGroupThreads, "weight half-rows split evenly");
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
-static_assert(kLoadDepth < kRawStages + 1, "copies in flight fit the raw ring");
 static_assert(kThreads * 96 <= 65536, "registers for one CTA per SM");
 constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
@@ -207,8 +205,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Arrive on an mbarrier once every cp.async this thread issued so far has
+// completed (the arrival does not raise the expected count).
+__device__ __forceinline__ void cp_async_arrive(unsigned long long* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // 16-byte global -> shared asynchronous copy; src_bytes = 0 writes zeros and
-// reads nothing.  Completion: cp.async.wait_group of the issuing thread.
+// reads nothing.  Completion: cp_async_arrive (or cp.async.wait_all) of the
+// issuing thread.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -243,50 +247,52 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);   // M / 16
 }
 
-// int8 x4 -> two fp16x2 words (exact): bias the bytes to b+128, place them in the
-// mantissa of fp16 1024 (0x6400), subtract 1152.
+// Order of k inside the fp16 tiles.  Both operands list the k of every group
+// of four in the order (0, 2, 1, 3); a dot product does not depend on the order
+// of its terms (and these partial sums are exact integers), and this order lets
+// the weight codes be widened without shifting each pair into place.
+
+// int8 x4 (k0..k3) -> fp16x2 words (k0, k2) and (k1, k3), exactly: bias the
+// bytes to b + 128, place them in the mantissa of fp16 1024 (0x6400), subtract
+// 1152.
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = v ^ 0x80808080u;
-  lo = hsub2(prmt(u, 0x64646464u, 0x4140u), 0x64806480u);
-  hi = hsub2(prmt(u, 0x64646464u, 0x4342u), 0x64806480u);
+  lo = hsub2(prmt(u, 0x64646464u, 0x4240u), 0x64806480u);
+  hi = hsub2(prmt(u, 0x64646464u, 0x4341u), 0x64806480u);
 }
 
-// Two 2-bit codes -> one fp16x2 word of (code - 1): the codes' two bits sit at
-// bit offsets s and s+8 of `word`; they become selector nibbles 1 and 3 (plus 4)
-// of a byte permute over {0, 0, 0, 0, 0xBC, 0x00, 0x3C, 0x00} (high bytes of
-// fp16 -1, 0, +1).
-template <int S>
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t word) {
-  uint32_t sel;
-  if constexpr (S <= 4) sel = (word << (4 - S)) & 0x3030u;
-  else sel = (word >> (S - 4)) & 0x3030u;
-  return prmt(0u, 0x003C00BCu, sel | 0x4040u);
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
-// One 16-byte packed chunk (64 weights of a row) -> 8 chunks of 8 fp16.
-// Chunk c holds k = 8c..8c+7: word w = c/2, k%16 = 8(c%2) + t, t = 0..7,
-// i.e. codes at bit 8*(t%4) + 2*(2(c%2) + t/4) of word w.
+// 32-bit packed word (16 codes; k = 16w + b + 4t sits in byte b at bit 2t) ->
+// 8 fp16x2 words of code - 1 in the order above.  (word >> 8b') & (3 << 2t) in
+// both 16-bit halves, ORed into fp16 1024 (0x6400), is 1024 + c * 4^t; scaling
+// by 4^-t and subtracting 1024 * 4^-t + 1 gives c - 1 (all steps exact).
+__device__ __forceinline__ void codes_to_f16x8(uint32_t w, uint32_t out[8]) {
+  const uint32_t w8 = w >> 8;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t mask = 0x00030003u << (2 * t);
+    const uint32_t scale = t == 0 ? 0x3C003C00u : t == 1 ? 0x34003400u : t == 2 ? 0x2C002C00u : 0x24002400u;
+    const uint32_t bias = t == 0 ? 0xE401E401u : t == 1 ? 0xDC04DC04u : t == 2 ? 0xD410D410u : 0xCC40CC40u;
+    out[2 * t] = hfma2((w & mask) | 0x64006400u, scale, bias);       // bytes 0, 2: k = 4t, 4t + 2
+    out[2 * t + 1] = hfma2((w8 & mask) | 0x64006400u, scale, bias);  // bytes 1, 3: k = 4t + 1, 4t + 3
+  }
+}
+
 // Half of a packed chunk (words 2*half, 2*half+1: k = 32*half .. 32*half+31)
 // -> fp16 chunks 4*half .. 4*half+3 of weight row r.
 __device__ __forceinline__ void store_weight_half(uint32_t row_addr, int r, int half, const uint2 v) {
-  const uint32_t words[2] = {v.x, v.y};
+  uint32_t q[16];
+  codes_to_f16x8(v.x, q);
+  codes_to_f16x8(v.y, q + 8);
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
-    const uint32_t w = words[cc >> 1];
-    uint32_t q0, q1, q2, q3;
-    if ((cc & 1) == 0) {
-      q0 = codes_to_f16x2<0>(w);
-      q1 = codes_to_f16x2<16>(w);
-      q2 = codes_to_f16x2<2>(w);
-      q3 = codes_to_f16x2<18>(w);
-    } else {
-      q0 = codes_to_f16x2<4>(w);
-      q1 = codes_to_f16x2<20>(w);
-      q2 = codes_to_f16x2<6>(w);
-      q3 = codes_to_f16x2<22>(w);
-    }
     const int c = 4 * half + cc;
-    st_shared_v4(row_addr + ((uint32_t)((c ^ (r & 7)) << 4)), q0, q1, q2, q3);
+    st_shared_v4(row_addr + ((uint32_t)((c ^ (r & 7)) << 4)), q[4 * cc], q[4 * cc + 1], q[4 * cc + 2], q[4 * cc + 3]);
   }
 }
 
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&ctl.raw_full[s], kLoadWarps);
+      mbar_init(&ctl.raw_full[s], kLoadThreads);
       mbar_init(&ctl.raw_empty[s], kGroupWarps);
     }
     for (int s = 0; s < 2; ++s) {
@@ -341,45 +347,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ loaders
     // Copy each raw k-step (128 x 64 int8 activations, n_tile x 16 B packed
     // codes) into the raw ring with 16-byte cp.async (coalesced: a warp covers
-    // 8 activation rows or 32 weight rows), kLoadDepth k-steps in flight per
-    // warp; a slot is handed over once every loader warp's copies have landed.
+    // 8 activation rows or 32 weight rows); a slot is handed over once every
+    // loader thread's copies into it have landed.
+    // Source addresses are set once per tile and advanced per k-step: with
+    // one loader warp per scheduler, index arithmetic would otherwise set the
+    // pace.
     const int v = threadIdx.x - kLoadWarp0 * 32;  // 0 .. 127
-    bool ok = true;
-    for (int f = 0; f < total + kLoadDepth - 1 && ok; ++f) {
-      if (f < total) {
-        const int slot = f % kRawStages;
-        const uint32_t use = (uint32_t)(f / kRawStages);
-        if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) { ok = false; break; }
-        const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
-        const int ks = f % p.KB;
-        int m0, n0;
-        tile_coords(p, tile, m0, n0);
+    constexpr int kAPieces = kTileM * kKStep / 16 / kLoadThreads;  // activation pieces per thread
+    constexpr int kBRows = (kMaxTileN + kLoadThreads - 1) / kLoadThreads;  // weight rows per thread
+    const int8_t* a_src[kAPieces];
+    uint32_t a_bytes[kAPieces];
+    const uint4* b_src[kBRows];
+    uint32_t b_bytes[kBRows];
+    int ks = 0, tile = blockIdx.x;
+    auto start_tile = [&]() {
+      int m0, n0;
+      tile_coords(p, tile, m0, n0);
+#pragma unroll
+      for (int i = 0; i < kAPieces; ++i) {
+        const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
+        const int am = m0 + (idx >> 2);
+        const bool in = am < p.M;
+        a_src[i] = p.xq + (int64_t)(in ? am : 0) * p.K + (idx & 3) * 16;
+        a_bytes[i] = in ? 16u : 0u;  // rows past M read as zeros
+      }
+#pragma unroll
+      for (int j = 0; j < kBRows; ++j) {
+        const int bn = n0 + v + j * kLoadThreads;
+        const bool in = bn < p.N;
+        b_src[j] = p.packed + (in ? bn : 0);
+        b_bytes[j] = in ? 16u : 0u;
+      }
+    };
+    if (total > 0) start_tile();
+    int slot = 0;
+    uint32_t parity = 0;
+    for (int f = 0; f < total; ++f) {
+      {
+        if (!mbar_wait(&ctl.raw_empty[slot], parity ^ 1u, &ctl, p.status)) break;
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
 #pragma unroll
-        for (int i = 0; i < (kTileM * kKStep / 16) / kLoadThreads; ++i) {
-          const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
-          const int row = idx >> 2, q = idx & 3;
-          const int am = m0 + row;
-          const bool in = am < p.M;
-          cp_async16(raw + (uint32_t)(row * kKStep + q * 16),
-                     p.xq + (int64_t)(in ? am : 0) * p.K + (int64_t)ks * kKStep + q * 16, in ? 16u : 0u);
+        for (int i = 0; i < kAPieces; ++i) {
+          cp_async16(raw + (uint32_t)((v + i * kLoadThreads) * 16), a_src[i], a_bytes[i]);  // piece idx at 16 idx
+          a_src[i] += kKStep;
         }
-        for (int row = v; row < p.n_tile; row += kLoadThreads) {
-          const int bn = n0 + row;
-          const bool in = bn < p.N;
-          cp_async16(raw + kRawABytes + (uint32_t)(row * 16), p.packed + (int64_t)ks * p.N + (in ? bn : 0),
-                     in ? 16u : 0u);
+#pragma unroll
+        for (int j = 0; j < kBRows; ++j) {
+          const int row = v + j * kLoadThreads;
+          if (row < p.n_tile) cp_async16(raw + kRawABytes + (uint32_t)(row * 16), b_src[j], b_bytes[j]);
+          b_src[j] += p.N;
         }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      const int g = f - (kLoadDepth - 1);  // the oldest k-step in flight
-      if (g >= 0) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kLoadDepth - 1) : "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.raw_full[g % kRawStages]);
+        // this thread's arrival on raw_full lands once its copies above have
+        cp_async_arrive(&ctl.raw_full[slot]);
+        if (++ks == p.KB) {
+          ks = 0;
+          tile += gridDim.x;
+          if (f + 1 < total) start_tile();
+        }
+        if (++slot == kRawStages) { slot = 0; parity ^= 1u; }
       }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
   } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
     // ------------------------------------------------------------------ converters
     // Group g (4 warps) converts the flat k-steps f = g, g + kStages, ... into
@@ -391,12 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = cw / kGroupWarps;
     const int u = (cw % kGroupWarps) * 32 + lane;  // 0 .. 127
     const int nh = 2 * p.n_tile;                   // weight half-rows, <= 512
+    int cks = grp, ctile = blockIdx.x;             // k-step f as (tile, k-step in tile)
+    while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
+    int n0 = (ctile / p.tiles_m) * p.n_tile;
     for (int f = grp; f < total; f += kConvGroups) {
       const int slot = f % kRawStages;
       const uint32_t use = (uint32_t)(f / kRawStages);
-      const int tile = blockIdx.x + (f / p.KB) * gridDim.x;
-      int m0, n0;
-      tile_coords(p, tile, m0, n0);
       if (!mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status)) break;
       const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
@@ -437,6 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {  // one arrival per warp on each
         mbar_arrive(&ctl.raw_empty[slot]);
         mbar_arrive(&ctl.full[grp]);
+      }
+      cks += kConvGroups;
+      if (cks >= p.KB) {
+        while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
+        n0 = (ctile / p.tiles_m) * p.n_tile;
       }
     }
   } else if (warp == kMmaWarp) {
