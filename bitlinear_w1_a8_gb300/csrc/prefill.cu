@@ -8,7 +8,7 @@
 // contraction, so it runs on the tensor cores.
 //
 // sm_103a has no integer tcgen05 MMA (ptxas rejects kind::i8 for this
-// target), so the operands are widened to fp16 in shared memory: int8
+// target), so the operands are widened to fp16 on chip: int8
 // activations (|xq| <= 127) and ternary weights are exact in fp16, every
 // product is an exact integer, and the fp32 accumulator holds every partial
 // sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
@@ -17,18 +17,22 @@
 // CTA roles (one persistent CTA per SM, 21 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
 //   warps 4-15  converters, three groups of four: group g widens the raw
-//               int8 / packed tiles of every third k-step to fp16 in stage g,
-//               in the 128-byte-swizzled K-major layout the MMA reads
-//   warps 16-19 loaders: copy raw tiles from global memory into a 6-deep
+//               tiles of every third k-step to fp16 in stage g -- the
+//               activations into TMEM (one row per lane), the weights into
+//               shared memory in the 128-byte-swizzled K-major layout
+//   warps 16-19 loaders: copy raw tiles from global memory into an 8-deep
 //               shared-memory ring with 16-byte cp.async; each thread's
 //               copies arrive on the slot's barrier as they land, so the
 //               whole ring can be in flight
 //   warp 20     allocates TMEM; one lane issues tcgen05.mma
 // Every hand-off between roles is one mbarrier arrival per warp.
-// Shared memory holds kStages stages of (A 128x64, B n_tile x 64) fp16 tiles
-// and kRawStages raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM
-// holds two 128 x n_tile fp32 accumulators so the epilogue of one tile
-// overlaps the MMAs of the next.  Every mbarrier wait is bounded by the
+// The MMA takes A (activations) from TMEM and B (weights) from shared memory,
+// so the widened activations never pass through shared memory, whose
+// bandwidth the weight stores, the raw copies and the MMA's reads of B share.
+// Shared memory holds kStages fp16 weight stages (n_tile x 64) and kRawStages
+// raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM holds two
+// 128 x n_tile fp32 accumulators, so the epilogue of one tile overlaps the
+// MMAs of the next, and kStages 128 x 64 fp16 activation stages.  Every mbarrier wait is bounded by the
 // global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
@@ -38,15 +42,14 @@ namespace bitlinear {
 namespace {
 
 constexpr int kStages = 3;                       // fp16 operand stages read by the MMA
-constexpr int kRawStages = 6;                    // raw int8 / packed k-steps in the ring
+constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring
 constexpr int kTileM = 128;
-constexpr int kMaxTileN = 256;                    // multiple of 16, <= 256
+constexpr int kMaxTileN = 208;                   // multiple of 16; TMEM holds 2 x 208 + 3 x 32 columns
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
-constexpr int kABytes = kTileM * 128;            // 16 KB
-constexpr int kBBytes = kMaxTileN * 128;         // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBBytes = kMaxTileN * 128;         // 26 KB of fp16 weights per stage
+constexpr int kStageBytes = kBBytes;             // (the fp16 activations of a stage live in TMEM)
 constexpr int kRawABytes = kTileM * kKStep;      // 8 KB of int8 activations
-constexpr int kRawBBytes = kMaxTileN * 16;       // 4 KB of packed codes
+constexpr int kRawBBytes = kMaxTileN * 16;       // 3.25 KB of packed codes
 constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
@@ -59,12 +62,15 @@ constexpr int kLoadThreads = kLoadWarps * 32;       // 128
 constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 16
 constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 20
 constexpr int kThreads = (kMmaWarp + 1) * 32;       // 672
-constexpr int kPiecesPerThread = kTileM * kKStep / 16 / kGroupThreads;  // 4 activation pieces
 constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
-static_assert(kTileM * kKStep / 16 == kPiecesPerThread * kGroupThreads, "activation pieces split evenly");
+static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
 static_assert(kThreads * 96 <= 65536, "registers for one CTA per SM");
-constexpr uint32_t kTmemCols = 512;                // two accumulators of up to 256 columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
+constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
+static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget");
+static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
 
 struct PrefillParams {
@@ -168,15 +174,26 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D (TMEM) (+)= A (TMEM: lane m holds row m, column c fp16 k = 2c, 2c + 1) x B (smem)
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// This warp's 32 lanes (one row each) <- 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mma_commit(unsigned long long* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -356,7 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kAPieces = kTileM * kKStep / 16 / kLoadThreads;  // activation pieces per thread
     constexpr int kBRows = (kMaxTileN + kLoadThreads - 1) / kLoadThreads;  // weight rows per thread
     const int8_t* a_src[kAPieces];
-    uint32_t a_bytes[kAPieces];
+    uint32_t a_bytes[kAPieces], a_dst[kAPieces];
+    // Raw activation row r keeps its 16-byte piece q at r*64 + 16*(q ^ ((r/2) % 4)),
+    // so a quarter-warp reading one piece of 8 consecutive rows hits 8 bank groups.
+#pragma unroll
+    for (int i = 0; i < kAPieces; ++i) {
+      const int idx = v + i * kLoadThreads, row = idx >> 2, q = idx & 3;
+      a_dst[i] = (uint32_t)(row * kKStep + ((q ^ ((row >> 1) & 3)) << 4));
+    }
     const uint4* b_src[kBRows];
     uint32_t b_bytes[kBRows];
     int ks = 0, tile = blockIdx.x;
@@ -388,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
 #pragma unroll
         for (int i = 0; i < kAPieces; ++i) {
-          cp_async16(raw + (uint32_t)((v + i * kLoadThreads) * 16), a_src[i], a_bytes[i]);  // piece idx at 16 idx
+          cp_async16(raw + a_dst[i], a_src[i], a_bytes[i]);
           a_src[i] += kKStep;
         }
 #pragma unroll
@@ -412,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ converters
     // Group g (4 warps) converts the flat k-steps f = g, g + kStages, ... into
     // stage g, so the groups work on different k-steps at once.  Thread u of a
-    // group widens activation pieces u + 128j (16 int8: row p/4, k = 16(p%4)
+    // group widens activation row u (its warp's TMEM lanes are rows 32(u/32)
     // ..) and weight half-rows u + 128j (half h of row r: k = 32h .. 32h+31 of
     // the row's packed chunk).
     const int cw = warp - kEpiWarps;
@@ -429,22 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
       if (!mbar_wait(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl, p.status)) break;
-      const uint32_t a_tile = stage_base + (uint32_t)grp * kStageBytes;
-      const uint32_t b_tile = a_tile + kABytes;
+      tc_fence_after();  // the MMAs that read this stage are complete
+      const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
+      {
+        // Activations: row u of the tile -> TMEM lane u, columns of stage grp.
+        const uint32_t row_raw = raw + (uint32_t)(u * kKStep);
+        const uint32_t sw = (uint32_t)((u >> 1) & 3);
+        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
+                                (uint32_t)grp * kTmemAStageCols;
 #pragma unroll
-      for (int j = 0; j < kPiecesPerThread; ++j) {
-        const int pc = u + j * kGroupThreads;
-        const int row = pc >> 2, q = pc & 3;
-        const uint32_t row_addr = a_tile + (uint32_t)row * 128u;
-        const uint4 av = ld_shared_v4(raw + (uint32_t)(pc * 16));  // raw piece p sits at 16p
-        const uint32_t wv[4] = {av.x, av.y, av.z, av.w};
+        for (int hpair = 0; hpair < 2; ++hpair) {  // pieces 2h, 2h+1 -> columns 16h .. 16h+15
+          uint32_t cols[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t l0, h0, l1, h1;
-          i8x4_to_f16x4(wv[2 * half], l0, h0);
-          i8x4_to_f16x4(wv[2 * half + 1], l1, h1);
-          const int c = 2 * q + half;
-          st_shared_v4(row_addr + ((uint32_t)((c ^ (row & 7)) << 4)), l0, h0, l1, h1);
+          for (int pi = 0; pi < 2; ++pi) {
+            const uint32_t piece = (uint32_t)(2 * hpair + pi);
+            const uint4 av = ld_shared_v4(row_raw + ((piece ^ sw) << 4));
+            const uint32_t wv[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) i8x4_to_f16x4(wv[j], cols[8 * pi + 2 * j], cols[8 * pi + 2 * j + 1]);
+          }
+          tmem_st16(t_addr + (uint32_t)(16 * hpair), cols);
         }
       }
 #pragma unroll
@@ -460,6 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < 4; ++cc) st_shared_v4(row_addr + (uint32_t)((4 * half + cc) << 4), 0u, 0u, 0u, 0u);
         }
       }
+      tmem_st_wait();
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {  // one arrival per warp on each
@@ -489,14 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < p.KB; ++ks) {
           if (!mbar_wait(&ctl.full[stage], phase, &ctl, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_tile = stage_base + (uint32_t)stage * kStageBytes;
-          const uint64_t a_desc = smem_desc_sw128(a_tile);
-          const uint64_t b_desc = smem_desc_sw128(a_tile + kABytes);
+          const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
+          const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < kKStep / 16; ++kk) {
-            // advance 16 fp16 = 32 bytes along K inside the swizzle atom
-            mma_f16(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 2), idesc,
-                    (ks | kk) != 0 ? 1u : 0u);
+            // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
+            mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
+                       (ks | kk) != 0 ? 1u : 0u);
           }
           mma_commit(&ctl.empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
