@@ -25,7 +25,8 @@
 //               copies arrive on the slot's barrier as they land, so the
 //               whole ring can be in flight
 //   warp 20     allocates TMEM; one lane issues tcgen05.mma
-// Every hand-off between roles is one mbarrier arrival per warp.
+// Every hand-off between roles is one mbarrier arrival per warp, except
+// "stage full" (converters -> MMA warp), which is a named barrier per stage.
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
 // so the widened activations never pass through shared memory, whose
 // bandwidth the weight stores, the raw copies and the MMA's reads of B share.
@@ -66,6 +67,7 @@ constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThr
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
 static_assert(kThreads * 96 <= 65536, "registers for one CTA per SM");
+static_assert(kStages + 1 <= 16, "named barriers 1 .. kStages");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
 constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
@@ -87,8 +89,7 @@ struct PrefillParams {
 };
 
 struct SharedCtl {
-  unsigned long long full[kStages];
-  unsigned long long empty[kStages];
+  unsigned long long empty[kStages];  // stage s consumed (tcgen05.commit); "full" is named barrier 1 + s
   unsigned long long raw_full[kRawStages];
   unsigned long long raw_empty[kRawStages];
   unsigned long long tmem_full[2];
@@ -155,6 +156,14 @@ __device__ __noinline__ void mbar_drain(unsigned long long* bar, uint32_t parity
       return;
     }
   }
+}
+// Named barriers 1 .. kStages: stage s is full once its converter group's
+// warps have arrived and the MMA warp syncs.
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -332,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl.full[s], kGroupWarps);
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
@@ -446,13 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cks = grp, ctile = blockIdx.x;             // k-step f as (tile, k-step in tile)
     while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
     int n0 = (ctile / p.tiles_m) * p.n_tile;
+    // Every k-step this group owns ends with its arrival on the stage's named
+    // barrier -- after an abort too, without the work -- so the MMA warp's
+    // barrier syncs, which cannot time out, always complete.
+    bool live = true;
     for (int f = grp; f < total; f += kConvGroups) {
       const int slot = f % kRawStages;
       const uint32_t use = (uint32_t)(f / kRawStages);
-      if (!mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status)) break;
-      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
-      if (!mbar_wait(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl, p.status)) break;
+      live = live && mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status) &&
+             mbar_wait(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl, p.status);
+      if (!live) {
+        named_bar_arrive(1 + grp, kGroupThreads + 32);
+        continue;
+      }
+      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       tc_fence_after();  // the MMAs that read this stage are complete
       const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
       {
@@ -492,10 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {  // one arrival per warp on each
-        mbar_arrive(&ctl.raw_empty[slot]);
-        mbar_arrive(&ctl.full[grp]);
-      }
+      if (lane == 0) mbar_arrive(&ctl.raw_empty[slot]);  // one arrival per warp
+      named_bar_arrive(1 + grp, kGroupThreads + 32);
       cks += kConvGroups;
       if (cks >= p.KB) {
         while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
@@ -504,35 +518,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp takes each stage's named barrier; lane 0 issues.  (An
+    // mbarrier wait or any shared-memory load by the issuing thread returned
+    // only after its in-flight MMAs had drained, which idled the tensor pipe
+    // between k-steps; a named barrier does not.)
+    {
       const uint32_t idesc = make_idesc(kTileM, p.n_tile);
       int stage = 0;
-      uint32_t phase = 0;
       bool ok = true;
       int it = 0;
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++it) {
         const int slot = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        if (!mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl, p.status)) { ok = false; break; }
-        tc_fence_after();
+        if (lane == 0) ok = mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl, p.status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
         const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kMaxTileN);
         for (int ks = 0; ks < p.KB; ++ks) {
-          if (!mbar_wait(&ctl.full[stage], phase, &ctl, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
-          const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
+          named_bar_sync(1 + stage, kGroupThreads + 32);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
+            const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < kKStep / 16; ++kk) {
-            // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
-            mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
-                       (ks | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kKStep / 16; ++kk) {
+              // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
+              mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
+                         (ks | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit(&ctl.empty[stage]);
           }
-          mma_commit(&ctl.empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          __syncwarp();
+          if (++stage == kStages) stage = 0;
         }
-        if (!ok) break;
-        mma_commit(&ctl.tmem_full[slot]);
+        if (lane == 0) mma_commit(&ctl.tmem_full[slot]);
       }
+    }
+    if (lane == 0) {
       // All MMAs this thread issued must be complete before TMEM is freed.
       mma_commit(&ctl.mma_done);
       mbar_drain(&ctl.mma_done, 0u, p.status);
