@@ -42,10 +42,10 @@
 namespace bitlinear {
 namespace {
 
-constexpr int kStages = 3;                       // fp16 operand stages read by the MMA
+constexpr int kStages = 4;                       // fp16 operand stages read by the MMA
 constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring
 constexpr int kTileM = 128;
-constexpr int kMaxTileN = 208;                   // multiple of 16; TMEM holds 2 x 208 + 3 x 32 columns
+constexpr int kMaxTileN = 192;                   // multiple of 16; TMEM holds 2 x 192 + 4 x 32 columns
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
 constexpr int kBBytes = kMaxTileN * 128;         // 26 KB of fp16 weights per stage
 constexpr int kStageBytes = kBBytes;             // (the fp16 activations of a stage live in TMEM)
@@ -66,7 +66,7 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;       // 672
 constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
-static_assert(kThreads * 96 <= 65536, "registers for one CTA per SM");
+static_assert(kThreads * 80 <= 65536, "80 registers a thread for one CTA per SM");
 static_assert(kStages + 1 <= 16, "named barriers 1 .. kStages");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
