@@ -137,4 +137,113 @@ static __device__ __forceinline__ float quantize_row(const float* __restrict__ x
   return s;
 }
 
+// 16-byte global -> shared copy that bypasses the registers; completes at the
+// issuing thread's cp.async.wait_all.
+__device__ __forceinline__ void cp_async16_row(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
+               "l"(src)
+               : "memory");
+}
+
+// quantize_row in two parts for the fused decode kernel: the row, the gating
+// input and gamma are first staged in shared memory with cp.async -- every
+// thread issues all of its copies before waiting, so the row costs one memory
+// round trip, and the kernel can queue its weight loads behind them -- and the
+// arithmetic then runs from shared memory, element by element the same
+// operations as quantize_row.  hs, us, gs: K floats of shared memory each (us
+// only with mul, gs only with gamma).  *sumx (shared, zero on entry) receives
+// sum_k xq[k].  Returns sx.
+// Part 1: issue this thread's copies of the row (and mul, gamma) into shared
+// memory.  Part 2 (quantize_row_staged) waits for them.
+static __device__ __forceinline__ void stage_row(const float* __restrict__ x, const float* __restrict__ mul,
+                                                 const float* __restrict__ gamma, int K, float4* hs, float4* us,
+                                                 float4* gs) {
+  const int K4 = K >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x);
+  const float4* ur = reinterpret_cast<const float4*>(mul);
+  const float4* gr = reinterpret_cast<const float4*>(gamma);
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    cp_async16_row(hs + i, xr + i);
+    if (ur) cp_async16_row(us + i, ur + i);
+    if (gr) cp_async16_row(gs + i, gr + i);
+  }
+}
+static __device__ __forceinline__ float quantize_row_staged(bool gated, bool norm, double eps, int K, float4* hs,
+                                                  const float4* us, const float4* gs, RowQuantScratch& sc,
+                                                  int8_t* out, int* sumx) {
+  const int K4 = K >> 2;
+  if (norm)
+    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  const float4* hsc = hs;
+  const float4* usc = gated ? us : nullptr;
+  float amax = 0.0f;
+  if (norm) {
+    // Warp-uniform trip count so that every lane joins the bucket aggregation.
+    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
+      const int i = base + (threadIdx.x & 31);
+      float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < K4) {
+        h = gated4(hsc, usc, i);
+        hs[i] = h;
+      }
+      const float f[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        int b;
+        uint32_t m;
+        fp32_bucket(f[c], &b, &m);
+        warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const double S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
+      if (threadIdx.x == 0) {
+        const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
+        sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
+      }
+    }
+    __syncthreads();
+    const float inv = sc.inv;
+    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+      float4 h = hs[i];
+      const float4 gm = gs[i];
+      h.x = __fmul_rn(__fmul_rn(h.x, inv), gm.x);
+      h.y = __fmul_rn(__fmul_rn(h.y, inv), gm.y);
+      h.z = __fmul_rn(__fmul_rn(h.z, inv), gm.z);
+      h.w = __fmul_rn(__fmul_rn(h.w, inv), gm.w);
+      hs[i] = h;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
+    }
+  } else {
+    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+      const float4 h = gated4(hsc, usc, i);
+      if (usc) hs[i] = h;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
+    }
+  }
+  amax = block_max(amax, sc.red);
+  const float s = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
+  int* o = reinterpret_cast<int*>(out);
+  int qsum = 0;
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    const float4 h = hs[i];
+    const float f[4] = {h.x, h.y, h.z, h.w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      int q = __float2int_rn(__fmul_rn(f[c], s));
+      q = q < -128 ? -128 : (q > 127 ? 127 : q);
+      qsum += q;
+      word |= ((uint32_t)q & 0xffu) << (8 * c);
+    }
+    o[i] = (int)word;
+  }
+  qsum = __reduce_add_sync(kFullMask, qsum);
+  if ((threadIdx.x & 31) == 0 && qsum != 0) atomicAdd(sumx, qsum);
+  return s;
+}
+
 }  // namespace bitlinear
