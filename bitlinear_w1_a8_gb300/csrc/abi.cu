@@ -52,8 +52,18 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 constexpr int64_t kDecodeMaxK = 65536;
 // Tensor-core kernel: the fp32 accumulator is exact while 127 * K < 2^24.
 constexpr int64_t kPrefillMaxK = 131072;
-// AUTO picks the decode kernel up to this many tokens.
-constexpr int64_t kDecodeMaxM = 64;
+// AUTO: the decode kernel (dp4a; its work grows with every token) for few
+// tokens, the tensor-core kernel (128-token tiles) beyond.  Measured on GB300
+// over BitNet-3B shapes: decode wins up to M = 16 (M = 4 for very wide
+// outputs such as a 50000-row LM head, where the tensor-core grid is full),
+// and up to M = 32 for narrow outputs (N <= 4096, where 128 x n tiles leave
+// most SMs idle at small M).
+bool auto_decode(int64_t M, int64_t N, int64_t K) {
+  if (K > 65536) return false;
+  if (M <= 4) return true;
+  if (M <= 16) return N < 32768;
+  return M <= 32 && N <= 4096;
+}
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
 // in shared memory next to the weights.
 constexpr int64_t kFusedMaxK = 16384;
@@ -152,8 +162,7 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
       (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
     return BITLINEAR_ERR_ALIGN;
   int use = algo;
-  if (use == BITLINEAR_ALGO_AUTO) use = (M <= kDecodeMaxM && K <= kDecodeMaxK) ? BITLINEAR_ALGO_DECODE
-                                                                               : BITLINEAR_ALGO_PREFILL;
+  if (use == BITLINEAR_ALGO_AUTO) use = auto_decode(M, N, K) ? BITLINEAR_ALGO_DECODE : BITLINEAR_ALGO_PREFILL;
   if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
     return BITLINEAR_ERR_UNSUPPORTED;
   if (use == BITLINEAR_ALGO_PREFILL && K > kPrefillMaxK) return BITLINEAR_ERR_UNSUPPORTED;
@@ -208,11 +217,19 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
   }
   cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s);
   if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
-  if (M <= kDecodeMaxM && K <= kDecodeMaxK) {
+  // The matrices the decode kernel takes share one launch; the rest get one
+  // tensor-core launch each.
+  DecodeMatrix dec[kMaxDecodeMats];
+  int ndec = 0;
+  for (int i = 0; i < num_weights; ++i)
+    if (auto_decode(M, mats[i].N, K)) dec[ndec++] = mats[i];
+  if (ndec > 0) {
     if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
-    return from_cuda(launch_decode(xq, x_scale, M, mats, num_weights, K, pdl, dev, s));
+    err = launch_decode(xq, x_scale, M, dec, ndec, K, pdl, dev, s);
+    if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   for (int i = 0; i < num_weights; ++i) {
+    if (auto_decode(M, mats[i].N, K)) continue;
     err = launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
                          pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;

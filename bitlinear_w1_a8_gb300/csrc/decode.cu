@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
     int a0[MT], a1[MT], a2[MT], a3[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
+#pragma unroll 2
     for (int kb = j; kb < KB; kb += J) {
       const uint4 wv = wsm[(size_t)kb * R + r];
       const uint32_t cw[4] = {wv.x, wv.y, wv.z, wv.w};

@@ -130,10 +130,10 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *   y             device, fp32 [M, N] row-major, written.
  *   acc           device int32 [M, N] or NULL; when given it receives the raw
  *                 integer accumulators (for checking and debugging).
- * The kernel is chosen from M (BITLINEAR_ALGO_AUTO): the decode kernel
- * (packed weights streamed into shared memory by bulk asynchronous copies,
- * dp4a on the 2-bit codes; K <= 65536) for M <= 64, the tcgen05 tensor-core
- * kernel (K <= 131072) otherwise.
+ * The kernel is chosen from M and N (BITLINEAR_ALGO_AUTO): the decode kernel
+ * (packed weights bulk-copied into shared memory, dp4a on the 2-bit codes;
+ * K <= 65536) for M <= 4, for M <= 16 when N < 32768 and for M <= 32 when
+ * N <= 4096; the tcgen05 tensor-core kernel (K <= 131072) otherwise.
  */
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale,
@@ -181,8 +181,9 @@ typedef struct bitlinear_weight {
  * share of the packed weights while it quantises the token itself (CTA 0
  * writes xq, x_scale), which keeps a separate act_quant kernel and its
  * latency off the decode critical path; the matrices' CTAs share one grid.
- * Otherwise it runs bitlinear_quant_act, then one decode launch for all
- * matrices (M <= 64) or one tensor-core launch per matrix.
+ * Otherwise it runs bitlinear_quant_act, then one decode launch for the
+ * matrices that bitlinear_forward's AUTO rule gives to the decode kernel and
+ * one tensor-core launch for each of the others.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream).
