@@ -356,7 +356,8 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
     matrix independently seeded N(0, 0.02) and quantised once (870,860,800
     packed bytes, > 4x L2).  One step = every BitLinear call of one decode step
     of M tokens in block order -- [q||k||v], [o], [gate||up], [down] per layer,
-    then the LM head -- each a bitlinear_linear call on seeded synthetic inputs
+    then the LM head and the greedy token (bitlinear_argmax, 4 bytes a token)
+    -- each a bitlinear_linear call on seeded synthetic inputs
     (attention and residuals are not part of this path), replayed as one CUDA
     graph with PDL."""
     import torch
@@ -383,7 +384,7 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
     total_bytes += head_pk.numel()
     del W
     weights_n = sum(N * K for N, K in shapes) * L + V * D
-    out = {"packed_bytes_per_step": total_bytes, "weights": weights_n, "launch_calls_per_step": 4 * L + 1}
+    out = {"packed_bytes_per_step": total_bytes, "weights": weights_n, "launch_calls_per_step": 4 * L + 2}
     for M in Ms:
         xa = synth.activations(M, D, synth.SEEDS["weight_set"]["x"]).to(dev)
         xb = synth.activations(M, F, synth.SEEDS["weight_set"]["x"] + 1).to(dev)
@@ -394,6 +395,7 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
         ys = {n: torch.empty(M, n, dtype=torch.float32, device=dev) for n in (D, F, V)}
         yq, yk, yv = (torch.empty(M, D, dtype=torch.float32, device=dev) for _ in range(3))
         yu = torch.empty(M, F, dtype=torch.float32, device=dev)
+        token = torch.empty(M, dtype=torch.int32, device=dev)
 
         def step(s):
             for mats in layers:
@@ -404,6 +406,7 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
                 bl.bitlinear_linear(xa, [(g, sg, ys[F]), (u, su, yu)], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
                 bl.bitlinear_linear(xb, [(d, sd, ys[D])], xq_b, sx_b, flags=bl.FLAG_PDL, stream=s)
             bl.bitlinear_linear(xa, [(head_pk, head_sc, ys[V])], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
+            bl.bitlinear_argmax(ys[V], token, stream=s)
 
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):

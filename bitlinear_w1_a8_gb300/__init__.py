@@ -17,7 +17,8 @@ __all__ = [
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
-    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "BitLinearWeight", "EXPORTED_SYMBOLS",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax", "BitLinearWeight",
+    "EXPORTED_SYMBOLS",
     "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "FLAG_PDL",
 ]
 
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
-    "bitlinear_selftest_wait_timeout", "bitlinear_linear",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax",
 )
 
 _lib = None
@@ -93,6 +94,8 @@ def load_library(path: str | None = None):
     lib.bitlinear_linear.argtypes = [vp, vp, i64, i64, vp, ctypes.c_double, ctypes.POINTER(BitLinearWeight),
                                      ctypes.c_int, vp, vp, ctypes.c_int, vp]
     lib.bitlinear_linear.restype = st
+    lib.bitlinear_argmax.argtypes = [vp, i64, i64, vp, vp]
+    lib.bitlinear_argmax.restype = st
     lib.bitlinear_device_status.argtypes = [vp, ctypes.c_int]
     lib.bitlinear_device_status.restype = st
     if path is None:
@@ -229,6 +232,17 @@ def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=
 def bitlinear_device_status(stream=None, clear: bool = True) -> int:
     """Synchronise the stream and return the library's device status (0 = OK)."""
     return int(load_library().bitlinear_device_status(_stream(stream), 1 if clear else 0))
+
+
+def bitlinear_argmax(y, index, stream=None):
+    """index[m] = first n of the largest y[m, n] (y [M, N] fp32, index [M] int32)."""
+    import torch
+    _need(y, torch.float32, "y")
+    if y.dim() != 2:
+        raise ValueError("y must be [M, N]")
+    M, N = y.shape
+    _need(index, torch.int32, "index", (M,))
+    _check(load_library().bitlinear_argmax(_ptr(y), M, N, _ptr(index), _stream(stream)), "bitlinear_argmax")
 
 
 def bitlinear_selftest_wait_timeout(limit_ns: int, stream=None):

@@ -237,6 +237,17 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
   return BITLINEAR_OK;
 }
 
+bitlinear_status bitlinear_argmax(const float* y, int64_t M, int64_t N, int32_t* index, void* stream) {
+  if (M < 0 || M > kMaxDim || N <= 0 || N > 0x7fffffffLL) return BITLINEAR_ERR_SHAPE;
+  if (M == 0) return BITLINEAR_OK;
+  if (!y || !index) return BITLINEAR_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(y) & 3u) || (reinterpret_cast<uintptr_t>(index) & 3u)) return BITLINEAR_ERR_ALIGN;
+  DeviceInfo dev;
+  const bitlinear_status st = current_device(&dev);
+  if (st != BITLINEAR_OK) return st;
+  return from_cuda(launch_argmax(y, M, N, index, static_cast<cudaStream_t>(stream)));
+}
+
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale, int64_t N,
                                    int64_t K, float* y, int32_t* acc, void* stream) {

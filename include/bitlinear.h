@@ -226,6 +226,20 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
 bitlinear_status bitlinear_quantize_weights_noalloc(const float* W, int64_t N, int64_t K,
                                                     uint8_t* packed, float* w_scale, void* stream);
 
+/* Greedy token choice after the LM head (which is a BitLinear too,
+ * "Hesper.Models.BitNet" page, section "Performance (BitNet-3B on A100)"):
+ * index[m] = the smallest n with y[m, n] == max over n of y[m, n], so that
+ * only 4 bytes per token need to reach the host.
+ *   y      device, fp32 [M, N] row-major (e.g. bitlinear_forward's output).
+ *   M      rows (tokens), M >= 0; M == 0 enqueues nothing.
+ *   N      1 <= N < 2^31.
+ *   index  device int32 [M], written.
+ * Ties go to the smaller index; -0.0 and +0.0 are equal.  Rows holding NaN
+ * give an unspecified index (like every non-finite input here).
+ * Errors: BITLINEAR_ERR_NULL, BITLINEAR_ERR_SHAPE, BITLINEAR_ERR_ALIGN (y not
+ * 4-byte aligned), BITLINEAR_ERR_CUDA. */
+bitlinear_status bitlinear_argmax(const float* y, int64_t M, int64_t N, int32_t* index, void* stream);
+
 /* Exercises the failure-detection path without faulting anything: launches a
  * one-warp kernel that waits on an mbarrier nothing ever arrives on, with the
  * same bounded wait the kernels use, giving up after limit_ns (0 < limit_ns

@@ -68,6 +68,8 @@ def _load():
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_forward_unpacked.argtypes = [vp, vp, i64, vp, ctypes.c_float, i64, i64, vp, vp]
         lib.oracle_forward_unpacked.restype = ctypes.c_int
+        lib.oracle_argmax.argtypes = [vp, i64, i64, vp]
+        lib.oracle_argmax.restype = ctypes.c_int
         del f32p, f64p
         _lib = lib
     return _lib
@@ -186,6 +188,15 @@ def forward_unpacked(xq, sx, Wq, sw: float):
     _check(_load().oracle_forward_unpacked(_ptr(xq), _ptr(sx), M, _ptr(Wq), float(sw), N, K,
                                            _ptr(acc), _ptr(y)), "forward_unpacked")
     return acc, y
+
+
+def argmax(y):
+    """First index of each row's largest value: y [M, N] (fp32 or fp64) -> int32 [M]."""
+    y = _c(y, np.float64)
+    M, N = y.shape
+    out = np.empty(M, np.int32)
+    _check(_load().oracle_argmax(_ptr(y), M, N, _ptr(out)), "argmax")
+    return out
 
 
 def bitlinear(x, W, mul=None, gamma=None, eps: float = 1e-6):

@@ -323,3 +323,20 @@ int oracle_forward_unpacked(const int8_t* xq, const float* sx, int64_t M,
   }
   return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Greedy choice after the LM head: out[m] = the first n whose y[m, n] is    */
+/* the row's largest ("Hesper.Models.BitNet" page, "Performance (BitNet-3B   */
+/* on A100)": the LM head is a BitLinear; greedy decoding takes the argmax   */
+/* of its logits).  fp32 inputs are passed widened to fp64 (exact).          */
+/* ------------------------------------------------------------------------ */
+int oracle_argmax(const double* y, int64_t M, int64_t N, int32_t* out) {
+  if (M < 0 || N <= 0) return ORACLE_ERR_SHAPE;
+  for (int64_t m = 0; m < M; ++m) {
+    int64_t best = 0;
+    for (int64_t n = 1; n < N; ++n)
+      if (y[m * N + n] > y[m * N + best]) best = n;
+    out[m] = (int32_t)best;
+  }
+  return ORACLE_OK;
+}

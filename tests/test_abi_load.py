@@ -81,3 +81,15 @@ def test_quantize_weights_argument_errors(lib):
     assert f(A, 1 << 21, 1 << 20, A, A, A, 4096, None) == -2               # N*K >= 2^40
     assert f(U, 4, 64, A, A, A, 4096, None) == -3
     assert f(None, 4, 64, A, A, A, 4096, None) == -1
+
+
+def test_argmax_argument_errors(lib):
+    f = lib.bitlinear_argmax
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(None, 1, 8, A, None) == -1                                     # NULL y
+    assert f(A, 1, 8, None, None) == -1                                     # NULL index
+    assert f(A, 1, 0, A, None) == -2                                        # N == 0
+    assert f(A, -1, 8, A, None) == -2                                       # M < 0
+    assert f(A, 1, 1 << 31, A, None) == -2                                  # N too large
+    assert f(A + 2, 1, 8, A, None) == -3                                    # y not 4-byte aligned
+    assert f(A, 0, 8, A, None) == 0                                         # empty batch

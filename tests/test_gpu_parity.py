@@ -12,8 +12,8 @@ import torch
 import bitlinear_w1_a8_gb300 as bl
 import oracle
 from bitlinear_w1_a8_gb300 import synth
-from harness import (Y_RTOL, full_parity, gpu_act_quant, gpu_forward, gpu_quantize_weights,
-                     max_rel_err)
+from harness import (Y_RTOL, check_canary, full_parity, gpu_act_quant, gpu_forward, gpu_quantize_weights,
+                     guarded, max_rel_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -267,3 +267,64 @@ def test_linear_matches_oracle(M, K, Ns, prolog):
     for (packed_d, sw_d, y, acc), (acc_o, y_o) in zip(mats, refs):
         np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
         assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
+
+
+# --- greedy choice after the LM head -------------------------------------------
+def _gpu_argmax(y):
+    """y: numpy fp32 [M, N] -> int32 [M] through bitlinear_argmax (canary-guarded)."""
+    M, N = y.shape
+    idx, ifull = guarded(M, torch.int32, -5)
+    bl.bitlinear_argmax(torch.from_numpy(np.ascontiguousarray(y)).cuda(), idx)
+    assert bl.bitlinear_device_status() == 0
+    check_canary(ifull, -5)
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (3, 50000), (5, 257), (2, 4), (4, 3001), (65537, 8)])
+def test_argmax_matches_oracle(M, N):
+    g = torch.Generator().manual_seed(40 + N % 97)
+    y = torch.randn(M, N, generator=g).numpy().astype(np.float32)
+    # planted ties: the row maximum again, later in the row
+    for m in range(min(M, 64)):
+        j = int(np.argmax(y[m]))
+        if j + 1 < N:
+            y[m, N - 1] = y[m, j]
+    np.testing.assert_array_equal(_gpu_argmax(y), oracle.argmax(y))
+
+
+def test_argmax_special_rows():
+    y = np.array([[0.0, -0.0, 0.0, -1.0], [-np.inf, -np.inf, -3.0, -np.inf],
+                  [1.0, 1.0, 1.0, 1.0], [-2.0, 5.0, 5.0, 4.0]], np.float32)
+    np.testing.assert_array_equal(_gpu_argmax(y), oracle.argmax(y))
+
+
+def test_argmax_unaligned_rows():
+    """N odd and a base that is only 4-byte aligned: the scalar scan."""
+    M, N = 3, 1001
+    g = torch.Generator().manual_seed(41)
+    buf = torch.randn(M * N + 1, generator=g).cuda()
+    y = buf[1:].view(M, N)
+    idx = torch.empty(M, dtype=torch.int32, device="cuda")
+    bl.bitlinear_argmax(y, idx)
+    assert bl.bitlinear_device_status() == 0
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle.argmax(y.cpu().numpy()))
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_lm_head_greedy_token(M):
+    """LM head 2560 -> 50000 (BitNet-3B vocabulary) then the greedy token: the GPU
+    index is the oracle's argmax of the GPU logits, and a maximum of the oracle's
+    own fp64 logits up to the fp32 rescale's rounding."""
+    N, K = synth.VOCAB, synth.DIM_3B
+    W = synth.weight(N, K, synth.SEEDS["weight_set"]["lm_head"])
+    x = synth.activations(M, K, synth.SEEDS["weight_set"]["x"])
+    _, sw, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+    xq, sx, (xq_d, sx_d) = gpu_act_quant(x)
+    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N)
+    idx = _gpu_argmax(y_g)
+    np.testing.assert_array_equal(idx, oracle.argmax(y_g))
+    Wq, sw_o, _ = oracle.weight_quant(W.numpy())
+    acc_o, y_o = oracle.forward(xq, sx, oracle.pack(Wq), sw_o, N, K)
+    for m in range(M):
+        best = y_o[m].max()
+        assert y_o[m, idx[m]] >= best - Y_RTOL * abs(best)

@@ -35,6 +35,9 @@ MUTATIONS = [
     ("sticky bit dropped", "if (round_bit && (sticky || (m & 1u))) {", "if (round_bit && (m & 1u)) {"),
     ("subnormal exponent", "if (e == 0) { *mant = frac; *e2 = -149; }", "if (e == 0) { *mant = frac; *e2 = -150; }"),
     ("lost carry", "a->d[j + 1] += c;", "a->d[j + 1] += 0 * c;"),
+    ("argmax ties to the last", "if (y[m * N + n] > y[m * N + best]) best = n;",
+     "if (y[m * N + n] >= y[m * N + best]) best = n;"),
+    ("argmax misses the last column", "for (int64_t n = 1; n < N; ++n)", "for (int64_t n = 1; n < N - 1; ++n)"),
     ("fp64 weight decision", "float t = W[i] * sw;\n    Wq[i] = (int8_t)rne_clamp(t, -1, 1);",
      "double t = (double)W[i] * (double)sw;\n    double rr = nearbyint(t);\n    Wq[i] = (int8_t)(rr < -1 ? -1 : (rr > 1 ? 1 : rr));"),
     ("fp64 activation decision", "float t = h[k] * s;\n      xq[m * K + k] = (int8_t)rne_clamp(t, -128, 127);",

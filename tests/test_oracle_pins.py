@@ -396,3 +396,28 @@ def test_zero_weights_give_zero():
     r = oracle.bitlinear(x, W)
     assert r["sw"] == float(np.float32(1) / np.float32(1e-5))
     assert np.all(r["y"] == 0) and np.all(r["acc"] == 0)
+
+
+# --- greedy choice after the LM head ------------------------------------------
+# Hand-worked rows with known answers: the first index of the row maximum.
+@pytest.mark.parametrize("row, want", [
+    ([1.0, 3.0, 3.0, 2.0], 1),            # tie: the earlier index
+    ([-5.0, -1.0, -1.0, -7.0], 1),        # all negative
+    ([0.0, -0.0, 0.0, -1.0], 0),          # -0 and +0 are equal
+    ([7.5], 0),                           # one element
+    ([-np.inf, -3.0], 1),
+    ([2.0, 1.0, 1.0, 2.0, 2.5], 4),       # maximum last
+    ([1e30, 1e30 * 1.0000001, 1e30], 1),  # one ulp apart in fp32
+])
+def test_argmax_hand_rows(row, want):
+    y = np.array([row], np.float32)
+    assert oracle.argmax(y)[0] == want
+
+
+def test_argmax_rows_are_independent_one_hot():
+    M, N = 3, 50000
+    y = np.zeros((M, N), np.float32)
+    hot = [31337, 0, N - 1]
+    for m, h in enumerate(hot):
+        y[m, h] = 1.0
+    assert list(oracle.argmax(y)) == hot
