@@ -176,9 +176,6 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
 
 cudaError_t launch_wait_selftest(int64_t limit_ns, const DeviceInfo& dev, cudaStream_t stream);
 
-// index[m] = first n of the largest y[m, n], M rows of N floats.
-cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, cudaStream_t stream);
-
 // One weight matrix of a decode launch (several matrices may share one input).
 constexpr int kMaxDecodeMats = 4;
 struct DecodeMatrix {
