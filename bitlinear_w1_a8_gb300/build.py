@@ -74,7 +74,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                 sys.stderr.write(err)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".{os.getpid()}.tmp"
-        run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+        run([nvcc, *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
 

@@ -5,6 +5,11 @@
 #include "common.cuh"
 
 namespace bitlinear {
+// argmax.cu: index[m] = first n of the largest y[m, n], M rows of N floats.
+cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, cudaStream_t stream);
+}  // namespace bitlinear
+
+namespace bitlinear {
 namespace {
 
 // One status word per device: kernels record a timed-out bounded wait here.
@@ -236,11 +241,6 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
   }
   return BITLINEAR_OK;
 }
-
-namespace bitlinear {
-// argmax.cu: index[m] = first n of the largest y[m, n], M rows of N floats.
-cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, cudaStream_t stream);
-}  // namespace bitlinear
 
 bitlinear_status bitlinear_argmax(const float* y, int64_t M, int64_t N, int32_t* index, void* stream) {
   if (M < 0 || M > kMaxDim || N <= 0 || N > 0x7fffffffLL) return BITLINEAR_ERR_SHAPE;
