@@ -19,13 +19,13 @@ __all__ = [
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
     "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax", "BitLinearWeight",
     "EXPORTED_SYMBOLS",
-    "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "FLAG_PDL",
+    "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "ALGO_BATCHED", "FLAG_PDL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libbitlinear.so")
 
-ALGO_AUTO, ALGO_DECODE, ALGO_PREFILL = 0, 1, 2
+ALGO_AUTO, ALGO_DECODE, ALGO_PREFILL, ALGO_BATCHED = 0, 1, 2, 3
 FLAG_PDL = 1
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_ALIGN", -4: "ERR_UNSUPPORTED",

@@ -7,6 +7,10 @@
 namespace bitlinear {
 // argmax.cu: index[m] = first n of the largest y[m, n], M rows of N floats.
 cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, cudaStream_t stream);
+// prefill.cu, 1 <= M <= 128: weight rows on the MMA's M side, tokens on its N side.
+cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 }  // namespace bitlinear
 
 namespace bitlinear {
@@ -57,18 +61,23 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 constexpr int64_t kDecodeMaxK = 65536;
 // Tensor-core kernel: the fp32 accumulator is exact while 127 * K < 2^24.
 constexpr int64_t kPrefillMaxK = 131072;
-// AUTO: the decode kernel (dp4a; its work grows with every token) for few
-// tokens, the tensor-core kernel (128-token tiles) beyond.  Measured on GB300
-// over BitNet-3B shapes: decode wins up to M = 16 (M = 4 for very wide
-// outputs such as a 50000-row LM head, where the tensor-core grid is full),
-// and up to M = 32 for narrow outputs (N <= 4096, where 128 x n tiles leave
-// most SMs idle at small M).
-bool auto_decode(int64_t M, int64_t N, int64_t K) {
-  if (K > 65536) return false;
-  if (M <= 4) return true;
-  if (M <= 16) return N < 32768;
-  return M <= 32 && N <= 4096;
+// AUTO, from timings on GB300 over the BitNet-3B shapes (hot L2):
+//  * the decode kernel (dp4a; its work grows with every token) for a few
+//    tokens: M <= 4 always, M <= 16 unless K is long (K >= 8192: M <= 8) or the
+//    output very wide (N >= 32768, e.g. a 50000-row LM head);
+//  * the batched tensor-core kernel (weight rows on the MMA's M side, all
+//    tokens in one tile, K split when tiles are few) up to M = 32, and up to
+//    M = 96 (128 for K >= 8192) for narrow outputs (N <= 4096), where
+//    128-token tiles would leave most SMs idle;
+//  * the tensor-core kernel with 128-token tiles beyond.
+int auto_algo(int64_t M, int64_t N, int64_t K) {
+  if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
+  if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
+  if (M <= 16 && K <= 65536 && !(K >= 8192 && M > 8)) return BITLINEAR_ALGO_DECODE;
+  if (M <= 128 && (M <= 32 || N <= 4096) && !(N <= 4096 && M > 96 && K < 8192)) return BITLINEAR_ALGO_BATCHED;
+  return BITLINEAR_ALGO_PREFILL;
 }
+
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
 // in shared memory next to the weights.
 constexpr int64_t kFusedMaxK = 16384;
@@ -159,7 +168,8 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
   if (st != BITLINEAR_OK) return st;
   if (M < 0 || M > kMaxDim) return BITLINEAR_ERR_SHAPE;
   if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
-  if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL)
+  if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL &&
+      algo != BITLINEAR_ALGO_BATCHED)
     return BITLINEAR_ERR_UNSUPPORTED;
   if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
   if (!xq || !x_scale || !y) return BITLINEAR_ERR_NULL;
@@ -167,15 +177,18 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
       (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
     return BITLINEAR_ERR_ALIGN;
   int use = algo;
-  if (use == BITLINEAR_ALGO_AUTO) use = auto_decode(M, N, K) ? BITLINEAR_ALGO_DECODE : BITLINEAR_ALGO_PREFILL;
+  if (use == BITLINEAR_ALGO_AUTO) use = auto_algo(M, N, K);
   if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
     return BITLINEAR_ERR_UNSUPPORTED;
   if (use == BITLINEAR_ALGO_PREFILL && K > kPrefillMaxK) return BITLINEAR_ERR_UNSUPPORTED;
+  if (use == BITLINEAR_ALGO_BATCHED && (K > kPrefillMaxK || M > 128)) return BITLINEAR_ERR_UNSUPPORTED;
   DeviceInfo dev;
   st = current_device(&dev);
   if (st != BITLINEAR_OK) return st;
   const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use == BITLINEAR_ALGO_BATCHED)
+    return from_cuda(launch_batched(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
   if (use == BITLINEAR_ALGO_DECODE) {
     const DecodeMatrix mat = {packed, w_scale, N, y, acc};
     return from_cuda(launch_decode(xq, x_scale, M, &mat, 1, K, pdl, dev, s));
@@ -227,16 +240,20 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
   DecodeMatrix dec[kMaxDecodeMats];
   int ndec = 0;
   for (int i = 0; i < num_weights; ++i)
-    if (auto_decode(M, mats[i].N, K)) dec[ndec++] = mats[i];
+    if (auto_algo(M, mats[i].N, K) == BITLINEAR_ALGO_DECODE) dec[ndec++] = mats[i];
   if (ndec > 0) {
     if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
     err = launch_decode(xq, x_scale, M, dec, ndec, K, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   for (int i = 0; i < num_weights; ++i) {
-    if (auto_decode(M, mats[i].N, K)) continue;
-    err = launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
-                         pdl, dev, s);
+    const int algo = auto_algo(M, mats[i].N, K);
+    if (algo == BITLINEAR_ALGO_DECODE) continue;
+    err = algo == BITLINEAR_ALGO_BATCHED
+              ? launch_batched(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
+                               mats[i].acc, pdl, dev, s)
+              : launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
+                               mats[i].acc, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   return BITLINEAR_OK;

@@ -84,8 +84,11 @@ struct PrefillParams {
   int32_t* acc;
   int* status;
   int M, N, K, KB;
-  int n_tile;      // multiple of 16, <= 256
-  int tiles_m, tiles_n, num_tiles;
+  int n_tile;      // multiple of 16, <= 256 (SWAP: 128 weight rows a tile)
+  int mma_n;       // MMA N = the rows of the shared-memory operand: n_tile, or (SWAP) tokens rounded up to 16
+  int tiles_m, tiles_n;
+  int splits;      // SWAP: K is split into this many ranges of KB k-steps (1 otherwise)
+  int num_tiles;   // work units: tiles_m * tiles_n * splits
 };
 
 struct SharedCtl {
@@ -322,13 +325,21 @@ __device__ __forceinline__ void store_weight_half(uint32_t row_addr, int r, int 
   }
 }
 
-__device__ __forceinline__ void tile_coords(const PrefillParams& p, int tile, int& m0, int& n0) {
+// Work unit -> first token row, first weight row and first k-block.
+__device__ __forceinline__ void tile_coords(const PrefillParams& p, int unit, int& m0, int& n0, int& kb0) {
+  const int tile = unit / p.splits;
+  kb0 = (unit - tile * p.splits) * p.KB;
   const int tm = tile % p.tiles_m;
   const int tn = tile / p.tiles_m;
   m0 = tm * kTileM;
   n0 = tn * p.n_tile;
 }
 
+// SWAP = false: A (TMEM) = 128 token rows, B (shared) = n_tile weight rows.
+// SWAP = true (few tokens): A = 128 weight rows, B = every token (M <= 128),
+// so the weights pass through the tensor cores once.  The loader is the same
+// (token rows 0 .. 127 of the activations, weight rows n0 .. n0 + 127).
+template <bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -393,21 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t b_bytes[kBRows];
     int ks = 0, tile = blockIdx.x;
     auto start_tile = [&]() {
-      int m0, n0;
-      tile_coords(p, tile, m0, n0);
+      int m0, n0, kb0;
+      tile_coords(p, tile, m0, n0, kb0);
 #pragma unroll
       for (int i = 0; i < kAPieces; ++i) {
         const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
         const int am = m0 + (idx >> 2);
         const bool in = am < p.M;
-        a_src[i] = p.xq + (int64_t)(in ? am : 0) * p.K + (idx & 3) * 16;
+        a_src[i] = p.xq + (int64_t)(in ? am : 0) * p.K + (int64_t)kb0 * kKStep + (idx & 3) * 16;
         a_bytes[i] = in ? 16u : 0u;  // rows past M read as zeros
       }
 #pragma unroll
       for (int j = 0; j < kBRows; ++j) {
         const int bn = n0 + v + j * kLoadThreads;
         const bool in = bn < p.N;
-        b_src[j] = p.packed + (in ? bn : 0);
+        b_src[j] = p.packed + (int64_t)kb0 * p.N + (in ? bn : 0);
         b_bytes[j] = in ? 16u : 0u;
       }
     };
@@ -451,9 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = cw / kGroupWarps;
     const int u = (cw % kGroupWarps) * 32 + lane;  // 0 .. 127
     const int nh = 2 * p.n_tile;                   // weight half-rows, <= 512
+    const int npieces = p.mma_n * 4;               // SWAP: 16-byte token pieces
     int cks = grp, ctile = blockIdx.x;             // k-step f as (tile, k-step in tile)
     while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
-    int n0 = (ctile / p.tiles_m) * p.n_tile;
+    int n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
     // Every k-step this group owns ends with its arrival on the stage's named
     // barrier -- after an abort too, without the work -- so the MMA warp's
     // barrier syncs, which cannot time out, always complete.
@@ -471,7 +483,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       tc_fence_after();  // the MMAs that read this stage are complete
       const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
-      {
+      if constexpr (SWAP) {
+        // Weights: row u of the tile (its 64 codes of this k-block) -> TMEM lane u.
+        const uint4 wv = ld_shared_v4(raw + kRawABytes + (uint32_t)(u * 16));
+        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
+                                (uint32_t)grp * kTmemAStageCols;
+        uint32_t cols[16];
+        codes_to_f16x8(wv.x, cols);
+        codes_to_f16x8(wv.y, cols + 8);
+        tmem_st16(t_addr, cols);
+        codes_to_f16x8(wv.z, cols);
+        codes_to_f16x8(wv.w, cols + 8);
+        tmem_st16(t_addr + 16u, cols);
+        // Tokens: piece q of token row r (16 int8) -> fp16 chunks 2q, 2q+1 of row r.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int pc = u + j * kGroupThreads;
+          if (pc >= npieces) continue;
+          const int row = pc >> 2, q = pc & 3;
+          const uint4 av = ld_shared_v4(raw + (uint32_t)(row * kKStep + ((q ^ ((row >> 1) & 3)) << 4)));
+          const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
+          const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t l0, h0, l1, h1;
+            i8x4_to_f16x4(aw[2 * half], l0, h0);
+            i8x4_to_f16x4(aw[2 * half + 1], l1, h1);
+            const int c = 2 * q + half;
+            st_shared_v4(row_addr + ((uint32_t)((c ^ (row & 7)) << 4)), l0, h0, l1, h1);
+          }
+        }
+      } else {
         // Activations: row u of the tile -> TMEM lane u, columns of stage grp.
         const uint32_t row_raw = raw + (uint32_t)(u * kKStep);
         const uint32_t sw = (uint32_t)((u >> 1) & 3);
@@ -490,18 +532,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st16(t_addr + (uint32_t)(16 * hpair), cols);
         }
-      }
 #pragma unroll
-      for (int j = 0; j < kHalvesPerThread; ++j) {
-        const int h = u + j * kGroupThreads;
-        if (h >= nh) continue;
-        const int row = h >> 1, half = h & 1;
-        const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
-        if (n0 + row < p.N) {
-          store_weight_half(row_addr, row, half, ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)));
-        } else {  // rows past N are zeros
+        for (int j = 0; j < kHalvesPerThread; ++j) {
+          const int h = u + j * kGroupThreads;
+          if (h >= nh) continue;
+          const int row = h >> 1, half = h & 1;
+          const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
+          if (n0 + row < p.N) {
+            store_weight_half(row_addr, row, half, ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)));
+          } else {  // rows past N are zeros
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) st_shared_v4(row_addr + (uint32_t)((4 * half + cc) << 4), 0u, 0u, 0u, 0u);
+            for (int cc = 0; cc < 4; ++cc) st_shared_v4(row_addr + (uint32_t)((4 * half + cc) << 4), 0u, 0u, 0u, 0u);
+          }
         }
       }
       tmem_st_wait();
@@ -513,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cks += kConvGroups;
       if (cks >= p.KB) {
         while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
-        n0 = (ctile / p.tiles_m) * p.n_tile;
+        n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -523,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // only after its in-flight MMAs had drained, which idled the tensor pipe
     // between k-steps; a named barrier does not.)
     {
-      const uint32_t idesc = make_idesc(kTileM, p.n_tile);
+      const uint32_t idesc = make_idesc(kTileM, p.mma_n);
       int stage = 0;
       bool ok = true;
       int it = 0;
@@ -566,12 +608,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sw = *p.sw;
     int it = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-      int m0, n0;
-      tile_coords(p, tile, m0, n0);
+      int m0, n0, kb0;
+      tile_coords(p, tile, m0, n0, kb0);
       const int slot = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl, p.status)) break;
       tc_fence_after();
+      if constexpr (SWAP) {
+        // TMEM lane = weight row n, column t = token t: y[t, n] for t < M
+        // (a warp writes 32 consecutive n of one token).
+        const int n = n0 + row;
+        const bool n_ok = n < p.N;
+        const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
+        for (int c = 0; c < p.mma_n; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(t_row + (uint32_t)c, r);
+          if (!n_ok) continue;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c + j;
+            if (t < p.M) {
+              const float a = __uint_as_float(r[j]);  // an exact integer
+              if (p.splits > 1) {
+                // a partial sum over this unit's K range: integer-valued fp32
+                // additions below 2^24 are exact in any order
+                atomicAdd(&p.y[(int64_t)t * p.N + n], a);
+              } else {
+                p.y[(int64_t)t * p.N + n] = __fdiv_rn(a, __fmul_rn(p.sx[t], sw));
+                if (p.acc) p.acc[(int64_t)t * p.N + n] = __float2int_rn(a);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.tmem_empty[slot]);  // one arrival per warp
+        continue;
+      }
       const int m = m0 + row;
       const bool row_ok = m < p.M;
       const float den = row_ok ? __fmul_rn(p.sx[m], sw) : 1.0f;
@@ -624,6 +697,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// After a split-K batched launch y holds acc (exact integers): y = acc / (sx * sw).
+__global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, int32_t* __restrict__ acc,
+                                                       const float* __restrict__ sx, const float* __restrict__ sw,
+                                                       int64_t M, int64_t N) {
+  pdl_wait_primary();
+  const float w = *sw;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M * N; i += (int64_t)gridDim.x * blockDim.x) {
+    const float a = y[i];
+    y[i] = __fdiv_rn(a, __fmul_rn(sx[i / N], w));
+    if (acc) acc[i] = __float2int_rn(a);
+  }
+}
+
 // Output-tile width: the multiple of 16 in 64..256 that minimises
 // (waves of tiles over the SMs) x (tile width + 64), preferring wider tiles.
 // Every k-step of a tile widens the 128 x 64 activation block whatever the
@@ -646,29 +732,15 @@ int choose_n_tile(int64_t M, int64_t N, int sms) {
 
 }  // namespace
 
-cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
-                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
-                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  PrefillParams p;
-  p.xq = xq;
-  p.sx = sx;
-  p.packed = reinterpret_cast<const uint4*>(packed);
-  p.sw = sw;
-  p.y = y;
-  p.acc = acc;
-  p.status = dev.status;
-  p.M = (int)M;
-  p.N = (int)N;
-  p.K = (int)K;
-  p.KB = (int)(K / kKStep);
-  p.n_tile = choose_n_tile(M, N, dev.num_sms);
-  p.tiles_m = (int)((M + kTileM - 1) / kTileM);
-  p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
-  p.num_tiles = p.tiles_m * p.tiles_n;
+namespace {
+
+template <bool SWAP>
+cudaError_t launch_impl(const PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   const size_t smem = (size_t)kSmemBytes + 1024;
   static thread_local int configured = -1;
   if (configured != dev.device) {
-    cudaError_t err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err =
+        cudaFuncSetAttribute(prefill_kernel<SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     configured = dev.device;
   }
@@ -683,7 +755,86 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<SWAP>, p);
+}
+
+PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
+                            int64_t N, int64_t K, float* y, int32_t* acc, const DeviceInfo& dev) {
+  PrefillParams p;
+  p.xq = xq;
+  p.sx = sx;
+  p.packed = reinterpret_cast<const uint4*>(packed);
+  p.sw = sw;
+  p.y = y;
+  p.acc = acc;
+  p.status = dev.status;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.KB = (int)(K / kKStep);
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+  p.n_tile = choose_n_tile(M, N, dev.num_sms);
+  p.mma_n = p.n_tile;
+  p.tiles_m = (int)((M + kTileM - 1) / kTileM);
+  p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
+  p.splits = 1;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  return launch_impl<false>(p, pdl, dev, stream);
+}
+
+// 1 <= M <= 128: 128-row weight tiles on the M side of the MMA, all tokens on
+// its N side (rounded up to 16; token rows past M are zeros).
+cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M < 1 || M > kTileM) return cudaErrorInvalidValue;
+  PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+  p.n_tile = kTileM;
+  p.mma_n = (int)((M + 15) / 16 * 16);
+  p.tiles_m = 1;
+  p.tiles_n = (int)((N + kTileM - 1) / kTileM);
+  // Split K (into a divisor of the k-block count, at most 16) when there are
+  // too few tiles to fill the SMs: minimise the k-steps of the busiest CTA.
+  const int KB = p.KB;
+  int best_s = 1;
+  int64_t best_cost = -1;
+  for (int sp = 1; sp <= 16 && sp <= KB; ++sp) {
+    if (KB % sp) continue;
+    const int64_t units = (int64_t)p.tiles_n * sp;
+    const int64_t waves = (units + dev.num_sms - 1) / dev.num_sms;
+    const int64_t cost = waves * (KB / sp) + (sp > 1 ? 4 : 0);  // + the zeroing and rescale passes
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = sp;
+    }
+  }
+  p.splits = best_s;
+  p.KB = KB / best_s;
+  p.num_tiles = p.tiles_n * best_s;
+  if (best_s == 1) return launch_impl<true>(p, pdl, dev, stream);
+  cudaError_t err = cudaMemsetAsync(y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
+  if (err != cudaSuccess) return err;
+  err = launch_impl<true>(p, false, dev, stream);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  const int64_t blocks = (M * N + 255) / 256;
+  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, batched_rescale, y, acc, sx, sw, M, N);
 }
 
 }  // namespace bitlinear

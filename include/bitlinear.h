@@ -130,10 +130,14 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *   y             device, fp32 [M, N] row-major, written.
  *   acc           device int32 [M, N] or NULL; when given it receives the raw
  *                 integer accumulators (for checking and debugging).
- * The kernel is chosen from M and N (BITLINEAR_ALGO_AUTO): the decode kernel
- * (packed weights bulk-copied into shared memory, dp4a on the 2-bit codes;
- * K <= 65536) for M <= 4, for M <= 16 when N < 32768 and for M <= 32 when
- * N <= 4096; the tcgen05 tensor-core kernel (K <= 131072) otherwise.
+ * The kernel is chosen from M, N and K (BITLINEAR_ALGO_AUTO): the decode
+ * kernel (packed weights bulk-copied into shared memory, dp4a on the 2-bit
+ * codes; K <= 65536) for M <= 4, and for M <= 16 (M <= 8 when K >= 8192)
+ * when N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
+ * MMA's M side, all tokens on its N side, K split over CTAs when the tiles
+ * are few) up to M = 32, and for N <= 4096 up to M = 96 (128 when
+ * K >= 8192); the tcgen05 kernel with 128-token tiles (K <= 131072)
+ * otherwise.
  */
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale,
@@ -143,7 +147,9 @@ bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64
 enum {
   BITLINEAR_ALGO_AUTO = 0,
   BITLINEAR_ALGO_DECODE = 1,   /* CUDA-core kernel, any M */
-  BITLINEAR_ALGO_PREFILL = 2   /* tcgen05 kernel, any M */
+  BITLINEAR_ALGO_PREFILL = 2,  /* tcgen05 kernel, any M: 128-token tiles */
+  BITLINEAR_ALGO_BATCHED = 3   /* tcgen05 kernel, 1 <= M <= 128: 128-row weight
+                                  tiles with every token in one tile */
 };
 
 enum {
@@ -183,7 +189,7 @@ typedef struct bitlinear_weight {
  * latency off the decode critical path; the matrices' CTAs share one grid.
  * Otherwise it runs bitlinear_quant_act, then one decode launch for the
  * matrices that bitlinear_forward's AUTO rule gives to the decode kernel and
- * one tensor-core launch for each of the others.
+ * one tensor-core launch (as that rule picks) for each of the others.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream).

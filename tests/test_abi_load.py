@@ -59,6 +59,7 @@ def test_forward_argument_errors(lib):
     assert f(U, A, 1, A, A, 64, 64, A, None, 0, 0, None) == -3             # misaligned xq
     assert f(A, A, 1, A, A, 64, 64, U, None, 0, 0, None) == -3             # misaligned y
     assert f(A, A, 1, A, A, 64, 64, A, None, 7, 0, None) == -4             # unknown algo
+    assert f(A, A, 129, A, A, 64, 64, A, None, 3, 0, None) == -4           # batched past 128 tokens
     assert f(A, A, 1, A, A, 64, 64, A, None, 0, 8, None) == -4             # unknown flag
     assert f(A, A, 0, A, A, 64, 64, A, None, 0, 0, None) == 0              # empty batch
 

@@ -45,6 +45,25 @@ def test_shapes(algo, M, N, K):
     full_parity(W, x, algo=algo)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 64), (2, 1, 128), (1, 80, 64), (3, 300, 192), (5, 1000, 640), (8, 153, 128),
+    (17, 2000, 256), (64, 512, 512), (100, 257, 320), (128, 130, 64), (16, 50000, 128),
+])
+def test_shapes_batched(M, N, K):
+    """The tensor-core kernel with weight rows on the MMA's M side (M <= 128)."""
+    W = synth.weight(N, K, 100 + N + K)
+    x = synth.activations(M, K, 200 + M + K, outlier_seed=300 + K)
+    full_parity(W, x, algo=bl.ALGO_BATCHED)
+
+
+@pytest.mark.parametrize("N,K", [(10240, 2560), (2560, 10240)])
+def test_batched_bitnet3b_m32(N, K):
+    """BitNet-3B FFN shapes at M = 32 through the batched kernel, every output."""
+    W = synth.weight(N, K, 21)
+    x = synth.activations(32, K, 22)
+    full_parity(W, x, algo=bl.ALGO_BATCHED)
+
+
 @pytest.mark.parametrize("M", [1, 4, 64])
 def test_pdl_flag(M):
     W = synth.weight(2000, 640, 7)
