@@ -433,6 +433,68 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
     return out
 
 
+def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
+    """BitNet-1.3B FFN sub-block (dim 2048, ffn 8192): RMSNorm -> act_quant ->
+    gate || up -> ReLU^2(gate) * up -> sub-norm -> act_quant -> down, as two
+    bitlinear_linear calls (the prologues fused), seeded as in the parity test;
+    one CUDA graph of `reps` sub-blocks over rotating weight copies (> 4x L2)."""
+    import torch
+    from bitlinear_w1_a8_gb300 import synth
+    s = synth.SEEDS["ffn_1b3"]
+    D, F = synth.DIM_1B3, synth.FFN_1B3
+    gamma = synth.uniform((D,), 0.5, 1.5, s["norm"]).to(dev)
+    gamma_sub = synth.uniform((F,), 0.5, 1.5, s["subnorm"]).to(dev)
+    ws = torch.empty(bl.bitlinear_quantize_weights_workspace(F, D), dtype=torch.uint8, device=dev)
+    base = []
+    for name, (N, K) in (("gate", (F, D)), ("up", (F, D)), ("down", (D, F))):
+        pk = torch.empty(bl.bitlinear_packed_bytes(N, K), dtype=torch.uint8, device=dev)
+        sc = torch.empty(1, dtype=torch.float32, device=dev)
+        bl.bitlinear_quantize_weights(synth.weight(N, K, s[name]).to(dev), pk, sc, ws)
+        base.append((pk, sc))
+    per = sum(p.numel() for p, _ in base)
+    copies = max(2, -(-4 * L2_BYTES // per))
+    sets = [base] + [[(p.clone(), sc) for p, sc in base] for _ in range(copies - 1)]
+    out = {"packed_bytes_per_block": per, "weight_copies": copies}
+    for M in Ms:
+        x = synth.activations(M, D, s["x"]).to(dev)
+        xq = torch.empty(M, D, dtype=torch.int8, device=dev)
+        sx = torch.empty(M, dtype=torch.float32, device=dev)
+        hq = torch.empty(M, F, dtype=torch.int8, device=dev)
+        hsx = torch.empty(M, dtype=torch.float32, device=dev)
+        yg = torch.empty(M, F, dtype=torch.float32, device=dev)
+        yu = torch.empty(M, F, dtype=torch.float32, device=dev)
+        yd = torch.empty(M, D, dtype=torch.float32, device=dev)
+
+        def block(i, st):
+            (g, sg), (u, su), (d, sd) = sets[i % copies]
+            bl.bitlinear_linear(x, [(g, sg, yg), (u, su, yu)], xq, sx, rms_weight=gamma, rms_eps=1e-6,
+                                flags=bl.FLAG_PDL, stream=st)
+            bl.bitlinear_linear(yg, [(d, sd, yd)], hq, hsx, mul=yu, rms_weight=gamma_sub, rms_eps=1e-6,
+                                flags=bl.FLAG_PDL, stream=st)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            block(0, stream)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    block(i, stream)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = reduce_max_ms(e0.elapsed_time(e1), dist, dev) / reps * 1e3
+        out[f"M{M}"] = {"us_per_block": round(us, 2), "packed_GBps": round(per / (us * 1e-6) / 1e9, 1),
+                        "tops": round(2.0 * M * (2 * F * D + D * F) / (us * 1e-6) / 1e12, 2)}
+        del g
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import bitlinear_w1_a8_gb300 as bl
@@ -647,6 +709,7 @@ def run_ours(args, rank, world, local_rank):
 
     prefill = None if args.no_prefill else measure_prefill(bl, dev, stream, dist)
     weight_set = None if args.no_weight_set else measure_weight_set(bl, dev, stream, dist)
+    ffn_1b3 = None if args.no_weight_set else measure_ffn_1b3(bl, dev, stream, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -692,6 +755,8 @@ def run_ours(args, rank, world, local_rank):
             line["prefill_m2048"] = prefill
         if weight_set:
             line["weight_set_3b"] = weight_set
+        if ffn_1b3:
+            line["ffn_1b3"] = ffn_1b3
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -21,9 +21,125 @@ namespace bitlinear {
 struct RowQuantScratch {
   unsigned long long buckets[kBuckets];
   unsigned long long digits[kSumDigits];
+  unsigned long long wlo[32], whi[32];  // per-warp 128-bit partial sums
   float red[32];
+  int ired[32];
   float inv;
 };
+
+// Exact sum of squares of the K values in hs (shared memory), rounded once to
+// the nearest double (ties to even).  Every thread of the block calls it.
+// v^2 = m^2 * 2^(2e - 300) (m the 24-bit significand, e the biased exponent,
+// subnormals e = 1).  Fast path: with E the largest exponent of the row,
+// every square of exponent e >= E - 32 is added as the integer m^2 << 2(e - E
+// + 32) < 2^112 into a 128-bit fixed-point sum (at most 2^15 values: < 2^127),
+// which is rounded to double directly.  If any nonzero value lies below that
+// window (|v| < max|v| / 2^32), the whole sum is taken again with one integer
+// bucket per exponent (warp_bucket_add / warp_fold_buckets, exact for every
+// input).  Both give the exact sum rounded once.
+static __device__ double block_sq_sum_exact(const float4* hs, int K4, RowQuantScratch& sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (int)(blockDim.x >> 5);
+  int emax = 0;
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    const float4 h = hs[i];
+    const uint32_t u[4] = {__float_as_uint(h.x), __float_as_uint(h.y), __float_as_uint(h.z), __float_as_uint(h.w)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t a = u[c] & 0x7fffffffu;
+      const int e = a ? max((int)(a >> 23), 1) : 0;
+      emax = max(emax, e);
+    }
+  }
+  emax = __reduce_max_sync(kFullMask, emax);
+  if (lane == 0) sc.ired[warp] = emax;
+  __syncthreads();
+  emax = 0;
+  for (int w = 0; w < nwarps; ++w) emax = max(emax, sc.ired[w]);
+  if (emax == 0) return 0.0;  // every value is zero (the same on every thread)
+  const int eb = max(emax - 32, 1);
+  unsigned __int128 acc = 0;
+  int slow = 0;
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    const float4 h = hs[i];
+    const uint32_t u[4] = {__float_as_uint(h.x), __float_as_uint(h.y), __float_as_uint(h.z), __float_as_uint(h.w)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t a = u[c] & 0x7fffffffu;
+      if (!a) continue;
+      const int e = max((int)(a >> 23), 1);
+      const uint64_t m = (a & 0x7fffffu) | ((a >> 23) ? 0x800000u : 0u);
+      if (e < eb) slow = 1;
+      else acc += ((unsigned __int128)(m * m)) << (2 * (e - eb));
+    }
+  }
+  uint64_t lo = (uint64_t)acc, hi = (uint64_t)(acc >> 64);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t olo = __shfl_xor_sync(kFullMask, lo, o), ohi = __shfl_xor_sync(kFullMask, hi, o);
+    lo += olo;
+    hi += ohi + (lo < olo ? 1u : 0u);
+  }
+  if (lane == 0) {
+    sc.wlo[warp] = lo;
+    sc.whi[warp] = hi;
+  }
+  slow = __syncthreads_or(slow);
+  if (slow) {
+    // exact for every input: one integer bucket per exponent
+    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
+    __syncthreads();
+    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
+      const int i = base + lane;
+      const float4 h = i < K4 ? hs[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float f[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        int b;
+        uint32_t m;
+        fp32_bucket(f[c], &b, &m);
+        warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
+      }
+    }
+    __syncthreads();
+    double S = 0.0;
+    if (warp == 0) S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
+    if (threadIdx.x == 0) sc.digits[0] = (unsigned long long)__double_as_longlong(S);
+    __syncthreads();
+    const double r = __longlong_as_double((long long)sc.digits[0]);
+    __syncthreads();
+    return r;
+  }
+  // every thread folds the per-warp sums (the same result everywhere)
+  lo = 0;
+  hi = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    const uint64_t a = sc.wlo[w];
+    lo += a;
+    hi += sc.whi[w] + (lo < a ? 1u : 0u);
+  }
+  __syncthreads();  // sc.wlo / whi / ired may be reused after this
+  // value = (hi:lo) * 2^(2 eb - 300), rounded to 53 bits, ties to even
+  const int P = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);  // top bit (lo != 0 here)
+  const unsigned __int128 W = ((unsigned __int128)hi << 64) | lo;
+  uint64_t mant;
+  int E = P + 2 * eb - 300;
+  if (P <= 52) {
+    mant = (uint64_t)(W << (52 - P));
+  } else {
+    const int sh = P - 52;
+    mant = (uint64_t)(W >> sh);
+    const unsigned __int128 rem = W & ((((unsigned __int128)1) << sh) - 1);
+    const unsigned __int128 half = ((unsigned __int128)1) << (sh - 1);
+    if (rem > half || (rem == half && (mant & 1ull))) {
+      mant += 1ull;
+      if (mant == (1ull << 53)) {
+        mant >>= 1;
+        E += 1;
+      }
+    }
+  }
+  return __longlong_as_double((long long)(((uint64_t)(E + 1023) << 52) | (mant & ((1ull << 52) - 1ull))));
+}
 
 // h = x, or h = (r*r)*u with r = max(x, 0) when the gating input u is given.
 __device__ __forceinline__ float4 gated4(const float4* __restrict__ xr, const float4* __restrict__ ur, int i) {
@@ -67,36 +183,14 @@ static __device__ __forceinline__ float quantize_row(const float* __restrict__ x
   const float4* xr = reinterpret_cast<const float4*>(x);
   const float4* ur = reinterpret_cast<const float4*>(mul);
   const bool norm = gamma != nullptr;
-  if (norm) {
-    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
-    __syncthreads();
-  }
   float amax = 0.0f;
   if (norm) {
-    // Warp-uniform trip count so that every lane joins the bucket aggregation.
-    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
-      const int i = base + (threadIdx.x & 31);
-      float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < K4) {
-        h = gated4(xr, ur, i);
-        hs[i] = h;
-      }
-      const float f[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        int b;
-        uint32_t m;
-        fp32_bucket(f[c], &b, &m);
-        warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
-      }
-    }
+    for (int i = threadIdx.x; i < K4; i += blockDim.x) hs[i] = gated4(xr, ur, i);
     __syncthreads();
-    if (threadIdx.x < 32) {
-      const double S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
-      if (threadIdx.x == 0) {
-        const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-        sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-      }
+    const double S = block_sq_sum_exact(hs, K4, sc);
+    if (threadIdx.x == 0) {
+      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
+      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
     }
     __syncthreads();
     const float inv = sc.inv;
@@ -172,38 +266,20 @@ static __device__ __forceinline__ float quantize_row_staged(bool gated, bool nor
                                                   const float4* us, const float4* gs, RowQuantScratch& sc,
                                                   int8_t* out, int* sumx) {
   const int K4 = K >> 2;
-  if (norm)
-    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   const float4* hsc = hs;
   const float4* usc = gated ? us : nullptr;
   float amax = 0.0f;
   if (norm) {
-    // Warp-uniform trip count so that every lane joins the bucket aggregation.
-    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
-      const int i = base + (threadIdx.x & 31);
-      float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < K4) {
-        h = gated4(hsc, usc, i);
-        hs[i] = h;
-      }
-      const float f[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        int b;
-        uint32_t m;
-        fp32_bucket(f[c], &b, &m);
-        warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
-      }
+    if (usc) {
+      for (int i = threadIdx.x; i < K4; i += blockDim.x) hs[i] = gated4(hsc, usc, i);
+      __syncthreads();
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const double S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
-      if (threadIdx.x == 0) {
-        const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-        sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-      }
+    const double S = block_sq_sum_exact(hs, K4, sc);
+    if (threadIdx.x == 0) {
+      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
+      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
     }
     __syncthreads();
     const float inv = sc.inv;

@@ -85,6 +85,42 @@ def test_prologues(M, K):
         np.testing.assert_array_equal(xq_g, xq_o)
 
 
+@pytest.mark.parametrize("kind", ["wide", "tiny_only", "zeros_and_subnormals"])
+@pytest.mark.parametrize("M", [1, 3])
+def test_rmsnorm_exact_sum_paths(kind, M):
+    """The RMSNorm sum of squares takes a 128-bit fast path when every value is
+    within 2^32 of the row maximum and an exponent-bucket path otherwise; both
+    must give the oracle's codes (act_quant kernel and the fused M = 1 launch)."""
+    K = 2048
+    g = torch.Generator().manual_seed(90 + M)
+    x = torch.randn(M, K, generator=g)
+    if kind == "wide":            # a few values far below max/2^32: the bucket path
+        x[:, 5] = 1e-12
+        x[:, 77] = -3e-20
+        x[:, 9] = 1e3
+    elif kind == "tiny_only":     # every value tiny, within the window of each other
+        x = x * 1e-30
+    else:                         # exact zeros and fp32 subnormals next to normal values
+        x[:, ::7] = 0.0
+        x[:, 3] = 1e-40
+        x[:, 11] = -7e-42
+    gamma = synth.uniform((K,), 0.5, 1.5, 91)
+    xq_o, sx_o = oracle.act_quant(x.numpy(), gamma=gamma.numpy(), eps=1e-6)
+    xq_g, sx_g, _ = gpu_act_quant(x, None, gamma, 1e-6)
+    np.testing.assert_array_equal(sx_g, sx_o)
+    np.testing.assert_array_equal(xq_g, xq_o)
+    if M == 1:
+        W = synth.weight(256, K, 92)
+        _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        y = torch.empty(1, 256, device="cuda")
+        xq = torch.zeros(1, K, dtype=torch.int8, device="cuda")
+        sx = torch.zeros(1, dtype=torch.float32, device="cuda")
+        bl.bitlinear_linear(x.cuda(), [(packed_d, sw_d, y)], xq, sx, rms_weight=gamma.cuda(), rms_eps=1e-6)
+        assert bl.bitlinear_device_status() == 0
+        np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
+        np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
+
+
 def test_edge_values():
     """Zero rows, tiny rows (eps path), rounding ties, subnormals, huge values."""
     K, N = 128, 96
