@@ -66,15 +66,15 @@ constexpr int64_t kPrefillMaxK = 131072;
 //    tokens: M <= 4 always, M <= 16 unless K is long (K >= 8192: M <= 8) or the
 //    output very wide (N >= 32768, e.g. a 50000-row LM head);
 //  * the batched tensor-core kernel (weight rows on the MMA's M side, all
-//    tokens in one tile, K split when tiles are few) up to M = 32, and up to
-//    M = 96 (128 for K >= 8192) for narrow outputs (N <= 4096), where
-//    128-token tiles would leave most SMs idle;
-//  * the tensor-core kernel with 128-token tiles beyond.
+//    tokens in one tile) for narrow outputs (N <= 4096) up to M = 128 -- from
+//    M = 64 when K >= 8192;
+//  * the tensor-core kernel with 128-token tiles otherwise (both tensor-core
+//    kernels split K over CTAs when their tiles fill less than half the SMs).
 int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
   if (M <= 16 && K <= 65536 && !(K >= 8192 && M > 8)) return BITLINEAR_ALGO_DECODE;
-  if (M <= 128 && (M <= 32 || N <= 4096) && !(N <= 4096 && M > 96 && K < 8192)) return BITLINEAR_ALGO_BATCHED;
+  if (M <= 128 && N <= 4096 && (M >= 64 || K < 8192)) return BITLINEAR_ALGO_BATCHED;
   return BITLINEAR_ALGO_PREFILL;
 }
 

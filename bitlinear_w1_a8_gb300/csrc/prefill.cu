@@ -656,6 +656,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(t_row + (uint32_t)c, r);
         const int n = n0 + c;
         if (!row_ok || n >= p.N) continue;
+        if (p.splits > 1) {
+          // a partial sum over this unit's K range (exact integer-valued fp32 adds)
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (n + j < p.N) atomicAdd(yrow + n + j, __uint_as_float(r[j]));
+          continue;
+        }
         float yv[16];
         int av[16];
 #pragma unroll
@@ -710,25 +717,6 @@ __global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, in
   }
 }
 
-// Output-tile width: the multiple of 16 in 64..256 that minimises
-// (waves of tiles over the SMs) x (tile width + 64), preferring wider tiles.
-// Every k-step of a tile widens the 128 x 64 activation block whatever the
-// width, so the width carries a fixed cost of about 64 weight columns.
-int choose_n_tile(int64_t M, int64_t N, int sms) {
-  const int64_t tiles_m = (M + kTileM - 1) / kTileM;
-  int best = kMaxTileN;
-  int64_t best_cost = -1;
-  for (int nt = kMaxTileN; nt >= 64; nt -= 16) {
-    const int64_t tiles = tiles_m * ((N + nt - 1) / nt);
-    const int64_t waves = (tiles + sms - 1) / sms;
-    const int64_t cost = waves * (nt + 64);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = nt;
-    }
-  }
-  return best;
-}
 
 }  // namespace
 
@@ -758,6 +746,59 @@ cudaError_t launch_impl(const PrefillParams& p, bool pdl, const DeviceInfo& dev,
   return cudaLaunchKernelEx(&cfg, prefill_kernel<SWAP>, p);
 }
 
+// Split K (into a divisor of the k-block count, at most 16) when there are
+// too few tiles to fill the SMs: minimise the k-steps of the busiest CTA.
+// With a split, y is zeroed first, every unit adds its integer-valued partial
+// sums into y, and a rescale pass divides by sx * sw.
+int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out) {
+  int best_s = 1;
+  int64_t best_cost = -1;
+  // Only when at most half the SMs have a tile: the zeroing, the atomics and
+  // the rescale pass cost a pass over y each.
+  // A split must keep every unit in one wave and at least 8 k-steps long: each
+  // unit pays a pipeline fill and one atomic add per output of its tile.
+  for (int sp = 1; sp <= 16 && sp <= KB && (sp == 1 || 2 * tiles <= num_sms); ++sp) {
+    if (KB % sp) continue;
+    if (sp > 1 && (tiles * sp > num_sms || KB / sp < 8)) continue;
+    const int64_t units = tiles * sp;
+    const int64_t waves = (units + num_sms - 1) / num_sms;
+    const int64_t cost = waves * (KB / sp) + (sp > 1 ? 4 : 0);  // + the zeroing and rescale passes
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = sp;
+    }
+  }
+  if (cost_out) *cost_out = best_cost;
+  return best_s;
+}
+
+template <bool SWAP>
+cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  const int KB = p.KB;
+  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  const int best_s = best_split(tiles, KB, dev.num_sms, nullptr);
+  p.splits = best_s;
+  p.KB = KB / best_s;
+  p.num_tiles = (int)(tiles * best_s);
+  if (best_s == 1) return launch_impl<SWAP>(p, pdl, dev, stream);
+  const int64_t M = p.M, N = p.N;
+  cudaError_t err = cudaMemsetAsync(p.y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
+  if (err != cudaSuccess) return err;
+  err = launch_impl<SWAP>(p, false, dev, stream);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  const int64_t blocks = (M * N + 255) / 256;
+  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, batched_rescale, p.y, p.acc, p.sx, p.sw, M, N);
+}
+
 PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
                             int64_t N, int64_t K, float* y, int32_t* acc, const DeviceInfo& dev) {
   PrefillParams p;
@@ -781,13 +822,27 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
-  p.n_tile = choose_n_tile(M, N, dev.num_sms);
+  // Tile width and K split together: the fewest (k-steps of the busiest CTA)
+  // x (tile width + 64), the +64 being the activation widening of a k-step.
+  {
+    const int64_t tiles_m = (M + kTileM - 1) / kTileM;
+    int64_t best = -1;
+    p.n_tile = kMaxTileN;
+    for (int nt = kMaxTileN; nt >= 64; nt -= 16) {
+      int64_t ksteps = 0;
+      const int64_t tiles = tiles_m * ((N + nt - 1) / nt);
+      const int sp = best_split(tiles, p.KB, dev.num_sms, &ksteps);
+      const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        p.n_tile = nt;
+      }
+    }
+  }
   p.mma_n = p.n_tile;
   p.tiles_m = (int)((M + kTileM - 1) / kTileM);
   p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
-  p.splits = 1;
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  return launch_impl<false>(p, pdl, dev, stream);
+  return launch_split<false>(p, pdl, dev, stream);
 }
 
 // 1 <= M <= 128: 128-row weight tiles on the M side of the MMA, all tokens on
@@ -801,40 +856,7 @@ cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const u
   p.mma_n = (int)((M + 15) / 16 * 16);
   p.tiles_m = 1;
   p.tiles_n = (int)((N + kTileM - 1) / kTileM);
-  // Split K (into a divisor of the k-block count, at most 16) when there are
-  // too few tiles to fill the SMs: minimise the k-steps of the busiest CTA.
-  const int KB = p.KB;
-  int best_s = 1;
-  int64_t best_cost = -1;
-  for (int sp = 1; sp <= 16 && sp <= KB; ++sp) {
-    if (KB % sp) continue;
-    const int64_t units = (int64_t)p.tiles_n * sp;
-    const int64_t waves = (units + dev.num_sms - 1) / dev.num_sms;
-    const int64_t cost = waves * (KB / sp) + (sp > 1 ? 4 : 0);  // + the zeroing and rescale passes
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_s = sp;
-    }
-  }
-  p.splits = best_s;
-  p.KB = KB / best_s;
-  p.num_tiles = p.tiles_n * best_s;
-  if (best_s == 1) return launch_impl<true>(p, pdl, dev, stream);
-  cudaError_t err = cudaMemsetAsync(y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
-  if (err != cudaSuccess) return err;
-  err = launch_impl<true>(p, false, dev, stream);
-  if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  const int64_t blocks = (M * N + 255) / 256;
-  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, batched_rescale, y, acc, sx, sw, M, N);
+  return launch_split<true>(p, pdl, dev, stream);
 }
 
 }  // namespace bitlinear

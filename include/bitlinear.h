@@ -134,10 +134,11 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  * kernel (packed weights bulk-copied into shared memory, dp4a on the 2-bit
  * codes; K <= 65536) for M <= 4, and for M <= 16 (M <= 8 when K >= 8192)
  * when N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
- * MMA's M side, all tokens on its N side, K split over CTAs when the tiles
- * are few) up to M = 32, and for N <= 4096 up to M = 96 (128 when
- * K >= 8192); the tcgen05 kernel with 128-token tiles (K <= 131072)
- * otherwise.
+ * MMA's M side, all tokens on its N side) for N <= 4096 and M <= 128 (from
+ * M = 64 when K >= 8192); the tcgen05 kernel with 128-token tiles
+ * (K <= 131072) otherwise.  Both tensor-core kernels split K over CTAs when
+ * their tiles fill less than half of the SMs (y is then zeroed, accumulated
+ * and rescaled in place: three passes on the stream).
  */
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale,

@@ -56,6 +56,18 @@ def test_shapes_batched(M, N, K):
     full_parity(W, x, algo=bl.ALGO_BATCHED)
 
 
+@pytest.mark.parametrize("algo,M,N,K", [
+    (bl.ALGO_PREFILL, 130, 300, 2048), (bl.ALGO_PREFILL, 256, 640, 4096), (bl.ALGO_PREFILL, 40, 2560, 1024),
+    (bl.ALGO_BATCHED, 64, 200, 8192), (bl.ALGO_BATCHED, 5, 1000, 4096),
+])
+def test_split_k(algo, M, N, K):
+    """Few tiles: K is split over CTAs, partial sums are added into y and
+    rescaled in place; acc and y must match the oracle as without a split."""
+    W = synth.weight(N, K, 110 + K)
+    x = synth.activations(M, K, 111 + M)
+    full_parity(W, x, algo=algo)
+
+
 @pytest.mark.parametrize("N,K", [(10240, 2560), (2560, 10240)])
 def test_batched_bitnet3b_m32(N, K):
     """BitNet-3B FFN shapes at M = 32 through the batched kernel, every output."""
