@@ -122,15 +122,18 @@ def _stream(stream):
 
 
 def _need(t, dtype, name, shape=None):
-    import torch
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    try:  # the common case in one expression; the detailed checks only on failure
+        if t.is_cuda and t.dtype == dtype and t.is_contiguous() and (shape is None or t.shape == shape):
+            return
+    except AttributeError:
+        pass
+    if not getattr(t, "is_cuda", False):
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def bitlinear_abi_version() -> int:
@@ -157,7 +160,7 @@ def bitlinear_quantize_weights(W, packed, w_scale, workspace, stream=None):
     import torch
     _need(W, torch.float32, "W")
     N, K = W.shape
-    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
     _need(w_scale, torch.float32, "w_scale")
     _need(workspace, torch.uint8, "workspace")
     _check(load_library().bitlinear_quantize_weights(
@@ -172,7 +175,7 @@ def bitlinear_quantize_weights_noalloc(W, packed, w_scale, stream=None):
     import torch
     _need(W, torch.float32, "W")
     N, K = W.shape
-    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
     _need(w_scale, torch.float32, "w_scale")
     _check(load_library().bitlinear_quantize_weights_noalloc(
         _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _stream(stream)),
@@ -203,7 +206,7 @@ def bitlinear_forward_ex(xq, x_scale, packed, w_scale, N: int, y, acc=None,
     _need(xq, torch.int8, "xq")
     M, K = xq.shape
     _need(x_scale, torch.float32, "x_scale", (M,))
-    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
     _need(w_scale, torch.float32, "w_scale")
     _need(y, torch.float32, "y", (M, N))
     if acc is not None:
@@ -219,7 +222,7 @@ def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=
     _need(xq, torch.int8, "xq")
     M, K = xq.shape
     _need(x_scale, torch.float32, "x_scale", (M,))
-    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
     _need(w_scale, torch.float32, "w_scale")
     _need(y, torch.float32, "y", (M, N))
     if acc is not None:
@@ -272,7 +275,7 @@ def bitlinear_linear(x, weights, xq, x_scale, mul=None, rms_weight=None, rms_eps
         packed, w_scale, y = w[0], w[1], w[2]
         acc = w[3] if len(w) > 3 else None
         N = y.shape[1]
-        _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+        _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
         _need(w_scale, torch.float32, "w_scale")
         _need(y, torch.float32, "y", (M, N))
         if acc is not None:
