@@ -279,13 +279,17 @@ def measured_peak_tensor():
         return 1900.0, "fallback"
 
 
-PREFILL_SOURCES = ["bitlinear_w1_a8_gb300/csrc/prefill.cu", "bitlinear_w1_a8_gb300/csrc/common.cuh"]
+PREFILL_SOURCES = ["bitlinear_w1_a8_gb300/csrc/prefill.cu", "bitlinear_w1_a8_gb300/csrc/tc_util.cuh",
+                   "bitlinear_w1_a8_gb300/csrc/common.cuh"]
 
 
 def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
     """BitNet-3B prefill GEMM, M = 2048 tokens, both FFN shapes, on the tensor-core
-    kernel: TOPS = 2*M*N*K / launch time, back-to-back launches in a CUDA graph over
-    rotating copies of inputs and outputs (working set > L2)."""
+    kernels: TOPS = 2*M*N*K / launch time, back-to-back calls in a CUDA graph over
+    rotating copies of inputs and outputs (working set > L2).  The headline is
+    bitlinear_forward's AUTO path (the kernel with 128-token tiles); "wide" is
+    bitlinear_forward_ws with BITLINEAR_ALGO_WIDE (the activations widened once
+    into the workspace, then the contraction kernel; both launches timed)."""
     import torch
     from bitlinear_w1_a8_gb300 import synth
     s = synth.SEEDS["prefill"]
@@ -310,33 +314,46 @@ def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
         for q in xq:
             bl.bitlinear_quant_act(xd, q, sx)
         ys = [torch.empty(M, N, dtype=torch.float32, device=dev) for _ in range(copies)]
+        fws = torch.empty(bl.bitlinear_forward_workspace(M, K), dtype=torch.uint8, device=dev)
         del W, xd
 
-        def body(i, st):
+        def time_path(body):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                body(0, stream)
+                torch.cuda.synchronize(dev)
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(launches):
+                        body(i, stream)
+                g.replay()
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = reduce_max_ms(e0.elapsed_time(e1), dist, dev) / launches
+            tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+            return {"us_per_launch": round(ms * 1e3, 3), "tops": round(tops, 2),
+                    "frac_of_fp16_peak": round(tops / peak, 4)}
+
+        def wide(i, st):
+            j = i % copies
+            bl.bitlinear_forward_ws(xq[j], sx, packed[j], sw, N, ys[j], workspace=fws, algo=bl.ALGO_WIDE,
+                                    flags=bl.FLAG_PDL, stream=st)
+
+        def tiles128(i, st):
             j = i % copies
             bl.bitlinear_forward_ex(xq[j], sx, packed[j], sw, N, ys[j], algo=bl.ALGO_PREFILL, stream=st)
 
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            body(0, stream)
-            torch.cuda.synchronize(dev)
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(launches):
-                    body(i, stream)
-            g.replay()
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = reduce_max_ms(e0.elapsed_time(e1), dist, dev) / launches
-        tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-        out[name] = {"M": M, "N": N, "K": K, "us_per_launch": round(ms * 1e3, 3),
-                     "tops": round(tops, 2), "frac_of_fp16_peak": round(tops / peak, 4),
-                     "rotating_copies": copies}
-        del packed, xq, ys
+        r = {"M": M, "N": N, "K": K, "rotating_copies": copies}
+        r.update(time_path(tiles128))
+        r["path"] = "bitlinear_forward (AUTO: 128-token tiles)"
+        r["wide"] = time_path(wide)
+        r["wide"]["path"] = "bitlinear_forward_ws, BITLINEAR_ALGO_WIDE (widen pre-pass + contraction, both timed)"
+        out[name] = r
+        del packed, xq, ys, fws
         torch.cuda.empty_cache()
     tot_ops = sum(2.0 * v["M"] * v["N"] * v["K"] for v in out.values())
     tot_us = sum(v["us_per_launch"] for v in out.values())

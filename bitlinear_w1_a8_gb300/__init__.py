@@ -16,16 +16,17 @@ __all__ = [
     "bitlinear_abi_version", "bitlinear_status_string", "bitlinear_packed_bytes",
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
+    "bitlinear_forward_workspace", "bitlinear_forward_ws",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
     "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax", "BitLinearWeight",
     "EXPORTED_SYMBOLS",
-    "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "ALGO_BATCHED", "FLAG_PDL",
+    "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "ALGO_BATCHED", "ALGO_WIDE", "FLAG_PDL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libbitlinear.so")
 
-ALGO_AUTO, ALGO_DECODE, ALGO_PREFILL, ALGO_BATCHED = 0, 1, 2, 3
+ALGO_AUTO, ALGO_DECODE, ALGO_PREFILL, ALGO_BATCHED, ALGO_WIDE = 0, 1, 2, 3, 4
 FLAG_PDL = 1
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_ALIGN", -4: "ERR_UNSUPPORTED",
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_abi_version", "bitlinear_status_string", "bitlinear_packed_bytes",
     "bitlinear_quantize_weights_workspace", "bitlinear_quantize_weights",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
+    "bitlinear_forward_workspace", "bitlinear_forward_ws",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
     "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax",
 )
@@ -87,6 +89,11 @@ def load_library(path: str | None = None):
     lib.bitlinear_forward_ex.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, vp, ctypes.c_int,
                                          ctypes.c_int, vp]
     lib.bitlinear_forward_ex.restype = st
+    lib.bitlinear_forward_workspace.argtypes = [i64, i64]
+    lib.bitlinear_forward_workspace.restype = sz
+    lib.bitlinear_forward_ws.argtypes = [vp, vp, i64, vp, vp, i64, i64, vp, vp, ctypes.c_int,
+                                         ctypes.c_int, vp, sz, vp]
+    lib.bitlinear_forward_ws.restype = st
     lib.bitlinear_quantize_weights_noalloc.argtypes = [vp, i64, i64, vp, vp, vp]
     lib.bitlinear_quantize_weights_noalloc.restype = st
     lib.bitlinear_selftest_wait_timeout.argtypes = [i64, vp]
@@ -214,6 +221,33 @@ def bitlinear_forward_ex(xq, x_scale, packed, w_scale, N: int, y, acc=None,
     _check(load_library().bitlinear_forward_ex(
         _ptr(xq), _ptr(x_scale), M, _ptr(packed), _ptr(w_scale), N, K, _ptr(y), _ptr(acc),
         int(algo), int(flags), _stream(stream)), "bitlinear_forward_ex")
+
+
+def bitlinear_forward_workspace(M: int, K: int) -> int:
+    """Bytes of device workspace bitlinear_forward_ws needs for M tokens of K."""
+    return int(load_library().bitlinear_forward_workspace(int(M), int(K)))
+
+
+def bitlinear_forward_ws(xq, x_scale, packed, w_scale, N: int, y, acc=None, workspace=None,
+                         algo: int = ALGO_AUTO, flags: int = 0, stream=None):
+    """bitlinear_forward_ex with a device workspace (a uint8 CUDA tensor of at
+    least bitlinear_forward_workspace(M, K) bytes; one is allocated on xq's
+    device when None is given)."""
+    import torch
+    _need(xq, torch.int8, "xq")
+    M, K = xq.shape
+    _need(x_scale, torch.float32, "x_scale", (M,))
+    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(w_scale, torch.float32, "w_scale")
+    _need(y, torch.float32, "y", (M, N))
+    if acc is not None:
+        _need(acc, torch.int32, "acc", (M, N))
+    if workspace is None:
+        workspace = torch.empty(((M + 15) // 16 * 16) * K * 2, dtype=torch.uint8, device=xq.device)
+    _need(workspace, torch.uint8, "workspace")
+    _check(load_library().bitlinear_forward_ws(
+        _ptr(xq), _ptr(x_scale), M, _ptr(packed), _ptr(w_scale), N, K, _ptr(y), _ptr(acc),
+        int(algo), int(flags), _ptr(workspace), workspace.numel(), _stream(stream)), "bitlinear_forward_ws")
 
 
 def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=None):

@@ -26,7 +26,7 @@ NVCC_FLAGS = ARCH + [
     "-prec-div=true", "-prec-sqrt=true",
     "-I", INCLUDE, "-I", CSRC,
 ]
-SOURCES = ["abi.cu", "wquant.cu", "aquant.cu", "decode.cu", "prefill.cu", "argmax.cu"]
+SOURCES = ["abi.cu", "wquant.cu", "aquant.cu", "decode.cu", "prefill.cu", "wide.cu", "argmax.cu"]
 
 
 def _nvcc() -> str:

@@ -11,6 +11,12 @@ cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, 
 cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// wide.cu: activations widened once into `workspace`, 128 weight rows x up to
+// 192 tokens per tile.
+size_t wide_workspace_bytes(int64_t M, int64_t K);
+cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
+                        int64_t N, int64_t K, float* y, int32_t* acc, void* workspace, bool pdl,
+                        const DeviceInfo& dev, cudaStream_t stream);
 }  // namespace bitlinear
 
 namespace bitlinear {
@@ -159,34 +165,46 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
                                     static_cast<cudaStream_t>(stream)));
 }
 
-bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, int64_t M,
-                                      const uint8_t* packed, const float* w_scale, int64_t N,
-                                      int64_t K, float* y, int32_t* acc, int algo, int flags,
-                                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M, const uint8_t* packed,
+                              const float* w_scale, int64_t N, int64_t K, float* y, int32_t* acc, int algo,
+                              int flags, void* workspace, size_t workspace_bytes, void* stream) {
   if (!packed || !w_scale) return BITLINEAR_ERR_NULL;
   bitlinear_status st = check_nk(N, K);
   if (st != BITLINEAR_OK) return st;
   if (M < 0 || M > kMaxDim) return BITLINEAR_ERR_SHAPE;
   if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
   if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL &&
-      algo != BITLINEAR_ALGO_BATCHED)
+      algo != BITLINEAR_ALGO_BATCHED && algo != BITLINEAR_ALGO_WIDE)
     return BITLINEAR_ERR_UNSUPPORTED;
   if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
   if (!xq || !x_scale || !y) return BITLINEAR_ERR_NULL;
   if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) || (acc && !aligned16(acc)) ||
       (reinterpret_cast<uintptr_t>(x_scale) & 3u) || (reinterpret_cast<uintptr_t>(w_scale) & 3u))
     return BITLINEAR_ERR_ALIGN;
+  const bool have_ws = workspace && workspace_bytes >= wide_workspace_bytes(M, K);
+  if (algo == BITLINEAR_ALGO_WIDE && !have_ws) return BITLINEAR_ERR_WORKSPACE;
+  if (have_ws && !aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
   int use = algo;
+  // AUTO never picks WIDE: on GB300 the 128-token-tile kernel measured faster
+  // on the BitNet-3B prefill shapes (M = 2048: 130 vs 142 us for K = 2560 ->
+  // N = 10240, 148 vs 177 us for K = 10240 -> N = 2560, pre-pass included).
   if (use == BITLINEAR_ALGO_AUTO) use = auto_algo(M, N, K);
   if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
     return BITLINEAR_ERR_UNSUPPORTED;
-  if (use == BITLINEAR_ALGO_PREFILL && K > kPrefillMaxK) return BITLINEAR_ERR_UNSUPPORTED;
+  if ((use == BITLINEAR_ALGO_PREFILL || use == BITLINEAR_ALGO_WIDE) && K > kPrefillMaxK)
+    return BITLINEAR_ERR_UNSUPPORTED;
   if (use == BITLINEAR_ALGO_BATCHED && (K > kPrefillMaxK || M > 128)) return BITLINEAR_ERR_UNSUPPORTED;
   DeviceInfo dev;
   st = current_device(&dev);
   if (st != BITLINEAR_OK) return st;
   const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use == BITLINEAR_ALGO_WIDE)
+    return from_cuda(launch_wide(xq, x_scale, M, packed, w_scale, N, K, y, acc, workspace, pdl, dev, s));
   if (use == BITLINEAR_ALGO_BATCHED)
     return from_cuda(launch_batched(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
   if (use == BITLINEAR_ALGO_DECODE) {
@@ -194,6 +212,30 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
     return from_cuda(launch_decode(xq, x_scale, M, &mat, 1, K, pdl, dev, s));
   }
   return from_cuda(launch_prefill(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, int64_t M,
+                                      const uint8_t* packed, const float* w_scale, int64_t N,
+                                      int64_t K, float* y, int32_t* acc, int algo, int flags,
+                                      void* stream) {
+  return forward_impl(xq, x_scale, M, packed, w_scale, N, K, y, acc, algo, flags, nullptr, 0, stream);
+}
+
+size_t bitlinear_forward_workspace(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0 || M > kMaxDim || K > kMaxDim) return 0;
+  return wide_workspace_bytes(M, K);
+}
+
+bitlinear_status bitlinear_forward_ws(const int8_t* xq, const float* x_scale, int64_t M,
+                                      const uint8_t* packed, const float* w_scale, int64_t N,
+                                      int64_t K, float* y, int32_t* acc, int algo, int flags,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(xq, x_scale, M, packed, w_scale, N, K, y, acc, algo, flags, workspace, workspace_bytes,
+                      stream);
 }
 
 bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,

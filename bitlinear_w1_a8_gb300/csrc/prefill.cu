@@ -14,17 +14,17 @@
 // sum exactly while |acc| < 2^24 (|acc| <= 127*K, K <= 131072 here).  The
 // int32 result is therefore bit-exact.
 //
-// CTA roles (one persistent CTA per SM, 21 warps):
+// CTA roles (one persistent CTA per SM, 25 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
-//   warps 4-15  converters, three groups of four: group g widens the raw
-//               tiles of every third k-step to fp16 in stage g -- the
+//   warps 4-19  converters, four groups of four: group g widens the raw
+//               tiles of every fourth k-step to fp16 in stage g -- the
 //               activations into TMEM (one row per lane), the weights into
 //               shared memory in the 128-byte-swizzled K-major layout
-//   warps 16-19 loaders: copy raw tiles from global memory into an 8-deep
+//   warps 20-23 loaders: copy raw tiles from global memory into an 8-deep
 //               shared-memory ring with 16-byte cp.async; each thread's
 //               copies arrive on the slot's barrier as they land, so the
 //               whole ring can be in flight
-//   warp 20     allocates TMEM; one lane issues tcgen05.mma
+//   warp 24     allocates TMEM; one lane issues tcgen05.mma
 // Every hand-off between roles is one mbarrier arrival per warp, except
 // "stage full" (converters -> MMA warp), which is a named barrier per stage.
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
@@ -38,9 +38,12 @@
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
 #include "common.cuh"
+#include "tc_util.cuh"
 
 namespace bitlinear {
 namespace {
+
+using namespace tc;
 
 constexpr int kStages = 4;                       // fp16 operand stages read by the MMA
 constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring
@@ -57,12 +60,12 @@ constexpr int kEpiWarps = 4;
 constexpr int kConvGroups = kStages;                // group g converts the k-steps f with f % kStages == g
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;     // 128
-constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 12
+constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 16
 constexpr int kLoadWarps = 4;
 constexpr int kLoadThreads = kLoadWarps * 32;       // 128
-constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 16
-constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 20
-constexpr int kThreads = (kMmaWarp + 1) * 32;       // 672
+constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 20
+constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 24
+constexpr int kThreads = (kMmaWarp + 1) * 32;       // 800
 constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
@@ -73,7 +76,6 @@ constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow t
 constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
 static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget");
 static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
-constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s
 
 struct PrefillParams {
   const int8_t* xq;
@@ -101,216 +103,6 @@ struct SharedCtl {
   uint32_t tmem_base;
   int abort_flag;
 };
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_timer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of parity `parity` to complete.  Returns false
-// if the CTA is aborting (another role timed out) or this wait timed out.
-__device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, SharedCtl* ctl,
-                                       int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u) {
-      if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
-      if (global_timer() - t0 > kTimeoutNs) {
-        atomicExch(&ctl->abort_flag, 1);
-        atomicExch(status, (int)BITLINEAR_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-// Bounded wait that ignores the abort flag: used to drain this thread's own
-// in-flight MMAs before TMEM is freed.
-__device__ __noinline__ void mbar_drain(unsigned long long* bar, uint32_t parity, int* status) {
-  const unsigned long long t0 = global_timer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((i & 63u) == 0u && global_timer() - t0 > kTimeoutNs) {
-      atomicExch(status, (int)BITLINEAR_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-// Named barriers 1 .. kStages: stage s is full once its converter group's
-// warps have arrived and the MMA warp syncs.
-__device__ __forceinline__ void named_bar_arrive(int id, int count) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// D (TMEM) (+)= A (TMEM: lane m holds row m, column c fp16 k = 2c, 2c + 1) x B (smem)
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// This warp's 32 lanes (one row each) <- 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void mma_commit(unsigned long long* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-// Arrive on an mbarrier once every cp.async this thread issued so far has
-// completed (the arrival does not raise the expected count).
-__device__ __forceinline__ void cp_async_arrive(unsigned long long* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-// 16-byte global -> shared asynchronous copy; src_bytes = 0 writes zeros and
-// reads nothing.  Completion: cp_async_arrive (or cp.async.wait_all) of the
-// issuing thread.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset), tile base 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3fffu);          // start address
-  d |= (uint64_t)1u << 16;                          // leading byte offset (unused for SW128 K-major)
-  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
-  d |= (uint64_t)1u << 46;                          // descriptor version (sm_100 family)
-  d |= (uint64_t)2u << 61;                          // swizzle mode: 128 B
-  return d;
-}
-
-// Instruction descriptor: kind::f16, A = B = fp16, D = fp32, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
-  return (1u << 4)                       // D format fp32
-         | (0u << 7) | (0u << 10)        // A, B format fp16
-         | ((uint32_t)(n >> 3) << 17)    // N / 8
-         | ((uint32_t)(m >> 4) << 24);   // M / 16
-}
-
-// Order of k inside the fp16 tiles.  Both operands list the k of every group
-// of four in the order (0, 2, 1, 3); a dot product does not depend on the order
-// of its terms (and these partial sums are exact integers), and this order lets
-// the weight codes be widened without shifting each pair into place.
-
-// int8 x4 (k0..k3) -> fp16x2 words (k0, k2) and (k1, k3), exactly: bias the
-// bytes to b + 128, place them in the mantissa of fp16 1024 (0x6400), subtract
-// 1152.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = v ^ 0x80808080u;
-  lo = hsub2(prmt(u, 0x64646464u, 0x4240u), 0x64806480u);
-  hi = hsub2(prmt(u, 0x64646464u, 0x4341u), 0x64806480u);
-}
-
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-// 32-bit packed word (16 codes; k = 16w + b + 4t sits in byte b at bit 2t) ->
-// 8 fp16x2 words of code - 1 in the order above.  (word >> 8b') & (3 << 2t) in
-// both 16-bit halves, ORed into fp16 1024 (0x6400), is 1024 + c * 4^t; scaling
-// by 4^-t and subtracting 1024 * 4^-t + 1 gives c - 1 (all steps exact).
-__device__ __forceinline__ void codes_to_f16x8(uint32_t w, uint32_t out[8]) {
-  const uint32_t w8 = w >> 8;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t mask = 0x00030003u << (2 * t);
-    const uint32_t scale = t == 0 ? 0x3C003C00u : t == 1 ? 0x34003400u : t == 2 ? 0x2C002C00u : 0x24002400u;
-    const uint32_t bias = t == 0 ? 0xE401E401u : t == 1 ? 0xDC04DC04u : t == 2 ? 0xD410D410u : 0xCC40CC40u;
-    out[2 * t] = hfma2((w & mask) | 0x64006400u, scale, bias);       // bytes 0, 2: k = 4t, 4t + 2
-    out[2 * t + 1] = hfma2((w8 & mask) | 0x64006400u, scale, bias);  // bytes 1, 3: k = 4t + 1, 4t + 3
-  }
-}
 
 // Half of a packed chunk (words 2*half, 2*half+1: k = 32*half .. 32*half+31)
 // -> fp16 chunks 4*half .. 4*half+3 of weight row r.
@@ -427,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t parity = 0;
     for (int f = 0; f < total; ++f) {
       {
-        if (!mbar_wait(&ctl.raw_empty[slot], parity ^ 1u, &ctl, p.status)) break;
+        if (!mbar_wait(&ctl.raw_empty[slot], parity ^ 1u, &ctl.abort_flag, p.status)) break;
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
 #pragma unroll
         for (int i = 0; i < kAPieces; ++i) {
@@ -467,15 +259,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
     int n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
     // Every k-step this group owns ends with its arrival on the stage's named
-    // barrier -- after an abort too, without the work -- so the MMA warp's
-    // barrier syncs, which cannot time out, always complete.
+    // barrier, after an abort too (without the work), and never before the
+    // stage's previous MMAs were committed (a wait that ignores the abort flag;
+    // the MMA warp keeps committing after an abort): so each phase of the
+    // barrier holds one k-step's converters and the MMA warp's sync of that
+    // k-step, and the MMA warp's syncs, which cannot time out, always complete.
     bool live = true;
     for (int f = grp; f < total; f += kConvGroups) {
       const int slot = f % kRawStages;
       const uint32_t use = (uint32_t)(f / kRawStages);
       const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
-      live = live && mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl, p.status) &&
-             mbar_wait(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl, p.status);
+      const bool stage_free = mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl.abort_flag, p.status);
+      live = live && stage_free && mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl.abort_flag, p.status);
       if (!live) {
         named_bar_arrive(1 + grp, kGroupThreads + 32);
         continue;
@@ -563,30 +358,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp takes each stage's named barrier; lane 0 issues.  (An
     // mbarrier wait or any shared-memory load by the issuing thread returned
     // only after its in-flight MMAs had drained, which idled the tensor pipe
-    // between k-steps; a named barrier does not.)
+    // between k-steps; a named barrier does not.)  After an abort the warp
+    // still syncs and commits every k-step (issuing nothing), so the
+    // converters, which wait for those commits, stay in step with it.
     {
       const uint32_t idesc = make_idesc(kTileM, p.mma_n);
       int stage = 0;
-      bool ok = true;
+      bool aborted = false;
       int it = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
         const int slot = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        if (lane == 0) ok = mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl, p.status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        // lane 0 decides for the warp
+        bool ab = aborted || *reinterpret_cast<volatile int*>(&ctl.abort_flag) != 0;
+        if (!ab && lane == 0) ab = !mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl.abort_flag, p.status);
+        aborted = __shfl_sync(0xffffffffu, ab ? 1 : 0, 0) != 0;
         const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kMaxTileN);
         for (int ks = 0; ks < p.KB; ++ks) {
           named_bar_sync(1 + stage, kGroupThreads + 32);
           if (lane == 0) {
-            tc_fence_after();
-            const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
-            const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
+            if (!aborted) {
+              tc_fence_after();
+              const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
+              const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
 #pragma unroll
-            for (int kk = 0; kk < kKStep / 16; ++kk) {
-              // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
-              mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
-                         (ks | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < kKStep / 16; ++kk) {
+                // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
+                mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
+                           (ks | kk) != 0 ? 1u : 0u);
+              }
             }
             mma_commit(&ctl.empty[stage]);
           }
@@ -612,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(p, tile, m0, n0, kb0);
       const int slot = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
-      if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl, p.status)) break;
+      if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl.abort_flag, p.status)) break;
       tc_fence_after();
       if constexpr (SWAP) {
         // TMEM lane = weight row n, column t = token t: y[t, n] for t < M
@@ -772,6 +572,11 @@ int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out) {
   return best_s;
 }
 
+}  // namespace
+cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float* sw, int64_t M, int64_t N,
+                           const DeviceInfo& dev, cudaStream_t stream);
+namespace {
+
 template <bool SWAP>
 cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   const int KB = p.KB;
@@ -786,17 +591,7 @@ cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cuda
   if (err != cudaSuccess) return err;
   err = launch_impl<SWAP>(p, false, dev, stream);
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  const int64_t blocks = (M * N + 255) / 256;
-  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, batched_rescale, p.y, p.acc, p.sx, p.sw, M, N);
+  return launch_rescale(p.y, p.acc, p.sx, p.sw, M, N, dev, stream);
 }
 
 PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
@@ -817,6 +612,23 @@ PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const 
 }
 
 }  // namespace
+
+// After a split-K launch y holds the exact integer sums: y = y / (sx * sw) in
+// place (and acc = y when acc is not NULL), launched as a dependent kernel.
+cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float* sw, int64_t M, int64_t N,
+                           const DeviceInfo& dev, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  const int64_t blocks = (M * N + 255) / 256;
+  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, batched_rescale, y, acc, sx, sw, M, N);
+}
 
 cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,

@@ -149,8 +149,12 @@ enum {
   BITLINEAR_ALGO_AUTO = 0,
   BITLINEAR_ALGO_DECODE = 1,   /* CUDA-core kernel, any M */
   BITLINEAR_ALGO_PREFILL = 2,  /* tcgen05 kernel, any M: 128-token tiles */
-  BITLINEAR_ALGO_BATCHED = 3   /* tcgen05 kernel, 1 <= M <= 128: 128-row weight
+  BITLINEAR_ALGO_BATCHED = 3,  /* tcgen05 kernel, 1 <= M <= 128: 128-row weight
                                   tiles with every token in one tile */
+  BITLINEAR_ALGO_WIDE = 4      /* tcgen05 kernel, any M, bitlinear_forward_ws only:
+                                  the activations widened once to fp16 in the
+                                  workspace, 128-row weight tiles x up to 192
+                                  tokens */
 };
 
 enum {
@@ -167,6 +171,35 @@ bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, in
                                       const uint8_t* packed, const float* w_scale,
                                       int64_t N, int64_t K, float* y, int32_t* acc,
                                       int algo, int flags, void* stream);
+
+/*
+ * Workspace of bitlinear_forward_ws: 2 * K * (M rounded up to 16) bytes (0 for
+ * M <= 0 or K <= 0).
+ */
+size_t bitlinear_forward_workspace(int64_t M, int64_t K);
+
+/*
+ * bitlinear_forward_ex with a caller-provided device workspace (16-byte
+ * aligned, at least bitlinear_forward_workspace(M, K) bytes; its contents
+ * are scratch, overwritten on the stream).  It enables BITLINEAR_ALGO_WIDE,
+ * the tensor-core path for many tokens ("Hesper.Models.BitNet" page, section
+ * "Architecture": a full-sequence forward runs every BitLinear on all tokens
+ * at once): a pre-pass widens xq once to fp16 in the workspace, laid out as
+ * the MMA's shared-memory operand, so the contraction kernel only widens the
+ * 2-bit weight codes (into tensor memory) and bulk-copies the token tiles.
+ * Results are bit-identical to every other algorithm.  BITLINEAR_ALGO_AUTO
+ * follows bitlinear_forward's rule and does not pick WIDE (measured slower
+ * than the 128-token-tile kernel on the BitNet-3B prefill shapes); the other
+ * algorithms ignore the workspace.
+ * Errors: as bitlinear_forward_ex; BITLINEAR_ERR_WORKSPACE when
+ * BITLINEAR_ALGO_WIDE is asked for without a large enough workspace;
+ * BITLINEAR_ERR_ALIGN for a misaligned workspace.
+ */
+bitlinear_status bitlinear_forward_ws(const int8_t* xq, const float* x_scale, int64_t M,
+                                      const uint8_t* packed, const float* w_scale,
+                                      int64_t N, int64_t K, float* y, int32_t* acc,
+                                      int algo, int flags, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /* One weight matrix of a bitlinear_linear call. */
 typedef struct bitlinear_weight {

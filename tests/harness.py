@@ -52,13 +52,21 @@ def gpu_act_quant(x, mul=None, gamma=None, eps=1e-6):
     return xq2.cpu().numpy(), sx.cpu().numpy(), (xq2, sx)
 
 
-def gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=bl.ALGO_AUTO, flags=0):
-    M = xq_d.shape[0]
+def gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=bl.ALGO_AUTO, flags=0, workspace=False):
+    """bitlinear_forward_ex, or with workspace=True (always for ALGO_WIDE)
+    bitlinear_forward_ws with a canary-guarded workspace."""
+    M, K = xq_d.shape
     y, yfull = guarded(M * N, torch.float32, 1234.5)
     acc, afull = guarded(M * N, torch.int32, -99)
     y2, acc2 = y.view(M, N), acc.view(M, N)
-    bl.bitlinear_forward_ex(xq_d, sx_d, packed_d, sw_d, N, y2, acc2, algo=algo, flags=flags)
-    assert bl.bitlinear_device_status() == 0
+    if workspace or algo == bl.ALGO_WIDE:
+        ws, wfull = guarded(bl.bitlinear_forward_workspace(M, K), torch.uint8, 0x3C)
+        bl.bitlinear_forward_ws(xq_d, sx_d, packed_d, sw_d, N, y2, acc2, workspace=ws, algo=algo, flags=flags)
+        assert bl.bitlinear_device_status() == 0
+        check_canary(wfull, 0x3C)
+    else:
+        bl.bitlinear_forward_ex(xq_d, sx_d, packed_d, sw_d, N, y2, acc2, algo=algo, flags=flags)
+        assert bl.bitlinear_device_status() == 0
     check_canary(yfull, 1234.5)
     check_canary(afull, -99)
     return acc2.cpu().numpy(), y2.cpu().numpy()
@@ -77,7 +85,7 @@ def max_rel_err(y_gpu, y_ref):
 Y_RTOL = 1e-5
 
 
-def full_parity(W, x, mul=None, gamma=None, eps=1e-6, algo=bl.ALGO_AUTO, flags=0):
+def full_parity(W, x, mul=None, gamma=None, eps=1e-6, algo=bl.ALGO_AUTO, flags=0, workspace=False):
     """Every stage of the library against the oracle on the same inputs."""
     N, K = W.shape
     Wn, xn = W.numpy(), x.numpy()
@@ -93,7 +101,7 @@ def full_parity(W, x, mul=None, gamma=None, eps=1e-6, algo=bl.ALGO_AUTO, flags=0
     np.testing.assert_array_equal(sx_g, sx_o)
     np.testing.assert_array_equal(xq_g, xq_o)
     acc_o, y_o = oracle.forward(xq_o, sx_o, packed_o, sw_o, N, K)
-    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=algo, flags=flags)
+    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=algo, flags=flags, workspace=workspace)
     np.testing.assert_array_equal(acc_g, acc_o)
     assert max_rel_err(y_g, y_o) <= Y_RTOL
     return dict(acc=acc_g, y=y_g, y_ref=y_o)

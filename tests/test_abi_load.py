@@ -64,6 +64,20 @@ def test_forward_argument_errors(lib):
     assert f(A, A, 0, A, A, 64, 64, A, None, 0, 0, None) == 0              # empty batch
 
 
+def test_forward_ws_argument_errors(lib):
+    f = lib.bitlinear_forward_ws
+    ws = bl.bitlinear_forward_workspace(17, 128)
+    assert ws == 32 * 128 * 2 and bl.bitlinear_forward_workspace(0, 128) == 0
+    assert bl.bitlinear_forward_workspace(2048, 10240) == 2048 * 10240 * 2
+    assert f(A, A, 17, A, A, 64, 128, A, None, 4, 0, None, ws, None) == -7      # WIDE, no workspace
+    assert f(A, A, 17, A, A, 64, 128, A, None, 4, 0, A, ws - 16, None) == -7    # too small
+    assert f(A, A, 17, A, A, 64, 128, A, None, 4, 0, U, ws, None) == -3         # misaligned workspace
+    assert f(A, A, 17, A, A, 64, 100, A, None, 4, 0, A, ws, None) == -2         # K % 64
+    assert f(A, A, 17, A, A, 64, 128, A, None, 9, 0, A, ws, None) == -4         # unknown algo
+    assert f(A, A, 0, A, A, 64, 128, A, None, 4, 0, None, 0, None) == 0         # empty batch
+    assert lib.bitlinear_forward_ex(A, A, 17, A, A, 64, 128, A, None, 4, 0, None) == -7  # WIDE needs _ws
+
+
 def test_quant_act_argument_errors(lib):
     f = lib.bitlinear_quant_act
     assert f(None, None, 1, 64, None, 1e-6, A, A, None) == -1

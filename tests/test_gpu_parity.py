@@ -56,9 +56,33 @@ def test_shapes_batched(M, N, K):
     full_parity(W, x, algo=bl.ALGO_BATCHED)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 64), (2, 1, 128), (1, 80, 64), (3, 300, 192), (5, 1000, 640), (8, 153, 128), (16, 128, 64),
+    (17, 2000, 256), (33, 153, 128), (64, 512, 512), (100, 257, 320), (130, 257, 320), (197, 257, 640),
+    (300, 2000, 1024), (16, 50000, 128), (3000, 96, 64),
+])
+def test_shapes_wide(M, N, K):
+    """The tensor-core kernel fed by activations widened once into the
+    workspace (bitlinear_forward_ws): ragged token and weight tiles, K splits,
+    and a canary-guarded workspace."""
+    W = synth.weight(N, K, 100 + N + K)
+    x = synth.activations(M, K, 200 + M + K, outlier_seed=300 + K)
+    full_parity(W, x, algo=bl.ALGO_WIDE)
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 300, 2048), (256, 640, 4096), (300, 2000, 1024)])
+def test_forward_ws_auto_and_pdl(M, N, K):
+    """AUTO through bitlinear_forward_ws, and the PDL flag on the WIDE path."""
+    W = synth.weight(N, K, 120 + K)
+    x = synth.activations(M, K, 121 + M)
+    full_parity(W, x, workspace=True)
+    full_parity(W, x, algo=bl.ALGO_WIDE, flags=bl.FLAG_PDL)
+
+
 @pytest.mark.parametrize("algo,M,N,K", [
     (bl.ALGO_PREFILL, 130, 300, 2048), (bl.ALGO_PREFILL, 256, 640, 4096), (bl.ALGO_PREFILL, 40, 2560, 1024),
     (bl.ALGO_BATCHED, 64, 200, 8192), (bl.ALGO_BATCHED, 5, 1000, 4096),
+    (bl.ALGO_WIDE, 130, 300, 2048), (bl.ALGO_WIDE, 200, 1000, 4096), (bl.ALGO_WIDE, 1, 1, 32768),
 ])
 def test_split_k(algo, M, N, K):
     """Few tiles: K is split over CTAs, partial sums are added into y and
@@ -199,7 +223,7 @@ def test_decode_m1_full_size(name, N, K, seed_key):
     full_parity(W, x, flags=bl.FLAG_PDL)
 
 
-def _sampled_parity(W, x, rows, cols, algo):
+def _sampled_parity(W, x, rows, cols, algo, workspace=False):
     """Whole GPU path at full size; the oracle computes the sampled outputs only."""
     N, K = W.shape
     Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
@@ -210,25 +234,28 @@ def _sampled_parity(W, x, rows, cols, algo):
     xq_g, sx_g, (xq_d, sx_d) = gpu_act_quant(x)
     np.testing.assert_array_equal(xq_g, xq_o)
     np.testing.assert_array_equal(sx_g, sx_o)
-    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=algo)
+    acc_g, y_g = gpu_forward(xq_d, sx_d, packed_d, sw_d, N, algo=algo, workspace=workspace)
     acc_o, y_o = oracle.forward(xq_o[rows], sx_o[rows], oracle.pack(Wq_o[cols]), sw_o, len(cols), K)
     np.testing.assert_array_equal(acc_g[np.ix_(rows, cols)], acc_o)
     assert max_rel_err(y_g[np.ix_(rows, cols)], y_o) <= Y_RTOL
     return acc_g, y_g
 
 
+@pytest.mark.parametrize("path", ["tiles128", "wide"])
 @pytest.mark.parametrize("name,N,K,seed", [("up_shape", synth.FFN_3B, synth.DIM_3B, "W_up_shape"),
                                             ("down_shape", synth.DIM_3B, synth.FFN_3B, "W_down_shape")])
-def test_prefill_m2048_sampled(name, N, K, seed):
+def test_prefill_m2048_sampled(name, N, K, seed, path):
     """BitNet-3B prefill GEMM, M=2048: sampled rows x columns against the oracle,
-    spread over every output tile, plus the last row and column."""
+    spread over every output tile, plus the last row and column; through
+    bitlinear_forward (AUTO: 128-token tiles) and through bitlinear_forward_ws
+    with BITLINEAR_ALGO_WIDE (the activations widened once)."""
     s = synth.SEEDS["prefill"]
     W = synth.weight(N, K, s[seed])
     x = synth.activations(2048, K, s["x"])
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([rng.choice(2048, 24, replace=False), [0, 127, 128, 2047]]))
     cols = np.unique(np.concatenate([rng.choice(N, 160, replace=False), [0, 255, 256, N - 1]]))
-    _sampled_parity(W, x, rows, cols, bl.ALGO_AUTO)
+    _sampled_parity(W, x, rows, cols, bl.ALGO_WIDE if path == "wide" else bl.ALGO_AUTO, workspace=(path == "wide"))
 
 
 @pytest.mark.parametrize("M", [1, 512])
