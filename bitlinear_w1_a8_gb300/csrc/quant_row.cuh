@@ -256,7 +256,13 @@ static __device__ __forceinline__ void stage_row(const float* __restrict__ x, co
   const float4* xr = reinterpret_cast<const float4*>(x);
   const float4* ur = reinterpret_cast<const float4*>(mul);
   const float4* gr = reinterpret_cast<const float4*>(gamma);
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+  // Every CTA of a decode launch stages the same row: each starts at its own
+  // 128-byte line (rotated by CTA), so the CTAs' first requests spread over
+  // the L2 slices instead of all hitting the row's first lines at once.
+  const int rot = (int)((blockIdx.x * 296u) % (unsigned)K4) & ~7;
+  for (int j = threadIdx.x; j < K4; j += blockDim.x) {
+    int i = j + rot;
+    if (i >= K4) i -= K4;
     cp_async16_row(hs + i, xr + i);
     if (ur) cp_async16_row(us + i, ur + i);
     if (gr) cp_async16_row(gs + i, gr + i);

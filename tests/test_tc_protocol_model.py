@@ -1,5 +1,5 @@
-"""CPU model of the synchronisation protocol of the tensor-core kernel that
-streams widened token tiles (csrc/wide.cu), checked under random schedules.
+"""CPU model of the synchronisation protocol of the two persistent tcgen05
+kernels (csrc/wide.cu, csrc/prefill.cu), checked under random schedules.
 
 The kernel's MMA warp waits on named barriers (bar.sync cannot time out), so
 the protocol itself must make every sync complete: each phase of a barrier must
@@ -10,9 +10,13 @@ mbarrier rings with phase parity and named barriers with the hardware's
 arrival counting, with random delays and an abort injected at random times,
 and asserts: no deadlock, every MMA sync phase holds the four converter warps
 of its own k-step, and no mbarrier wait can alias a later phase.  A negative
-control (one barrier per converter group instead of one per TMEM stage, an
-earlier draft that hung on the GPU) must fail.  The ring sizes are read from
-the kernel source, so the model follows the kernel's constants.
+control (one barrier per converter group instead of one per stage, an earlier
+draft that hung on the GPU) must fail.  The ring sizes are read from the kernel
+sources, so the model follows the kernels' constants.  The two kernels differ
+in what frees a ring slot: in wide.cu the MMAs of the slot's previous k-step
+(one commit frees slot and stage); in prefill.cu the converter warps that
+widened the slot's previous k-step (the raw slot is free once they have read
+it).
 """
 import os
 import random
@@ -22,6 +26,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "bitlinear_w1_a8_gb300", "csrc", "wide.cu")
+SRC_PREFILL = os.path.join(ROOT, "bitlinear_w1_a8_gb300", "csrc", "prefill.cu")
 
 
 def _const(text, name):
@@ -44,7 +49,18 @@ def kernel_constants():
     # the barrier of k-step f and the waits, as the kernel writes them
     assert "named_bar_arrive(1 + f % kWStages" in text and "named_bar_sync(1 + stage" in text
     assert "const int prev = f - kWStages;" in text and "const int prev = f - kRing;" in text
-    return dict(ring=ring, done=done, stages=stages, groups=groups, gw=group_warps, loaders=loaders)
+    return dict(ring=ring, done=done, stages=stages, groups=groups, gw=group_warps, loaders=loaders, gate="mma")
+
+
+def prefill_constants():
+    text = open(SRC_PREFILL).read()
+    c = dict(ring=int(_const(text, "kRawStages")), done=int(_const(text, "kDoneRing")),
+             stages=int(_const(text, "kStages")), groups=int(_const(text, "kConvGroups")),
+             gw=int(_const(text, "kGroupWarps")), loaders=int(_const(text, "kLoadWarps")), gate="conv")
+    assert "named_bar_arrive(1 + stage, kGroupThreads + 32);" in text and "named_bar_sync(1 + stage" in text
+    assert "const int prev = f - kStages;" in text and "const int stage = f % kStages;" in text
+    assert "mbar_wait(&ctl.raw_empty[slot]" in text
+    return c
 
 
 class MBar:
@@ -81,11 +97,18 @@ def simulate(c, total, seed, abort_at=None, barrier_of=None):
                 w["released"] = B["members"]
             B["count"], B["members"], B["waiters"] = 0, [], []
 
+    raw_empty = [MBar() for _ in range(ring)]  # prefill: converter warps of the slot's k-step arrived
+    raw_arrivals = {}
+
     def loader(li):
         for f in range(li, total, loaders):
             if f >= ring:
                 prev = f - ring
-                while not done[prev % done_n].done(prev // done_n):
+                if c["gate"] == "mma":
+                    freed = lambda: done[prev % done_n].done(prev // done_n)
+                else:
+                    freed = lambda: raw_empty[prev % ring].done(prev // ring)
+                while not freed():
                     if st["abort"]:
                         return
                     yield
@@ -113,6 +136,11 @@ def simulate(c, total, seed, abort_at=None, barrier_of=None):
                     yield
             for _ in range(rnd.randint(0, 3)):
                 yield
+            if live and c["gate"] == "conv":  # one arrival per warp once the raw slot has been read
+                raw_arrivals[f] = raw_arrivals.get(f, 0) + 1
+                if raw_arrivals[f] == gw:
+                    assert raw_empty[f % ring].completed == f // ring
+                    raw_empty[f % ring].completed += 1
             arrive(barrier_of(f), ("conv", f))
 
     def mma():
@@ -158,6 +186,14 @@ def simulate(c, total, seed, abort_at=None, barrier_of=None):
 @pytest.fixture(scope="module")
 def consts():
     return kernel_constants()
+
+
+@pytest.mark.parametrize("total", list(range(1, 21)) + [48, 83])
+def test_prefill_protocol_completes_and_phases_match(total):
+    c = prefill_constants()
+    for seed in range(6):
+        simulate(c, total, seed)
+        simulate(c, total, 3000 + seed, abort_at=random.Random(seed).randint(1, 300))
 
 
 @pytest.mark.parametrize("total", list(range(1, 25)) + [40, 97])
