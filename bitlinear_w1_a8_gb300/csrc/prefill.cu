@@ -17,25 +17,24 @@
 // CTA roles (one persistent CTA per SM, 25 warps):
 //   warps 0-3   epilogue: TMEM -> registers -> y = acc/(sx*sw) -> global
 //   warps 4-19  converters, four groups of four: group g widens the raw
-//               tiles of every fourth k-step f to fp16 in stage f % 4 -- the
+//               tiles of every fourth k-step to fp16 in stage g -- the
 //               activations into TMEM (one row per lane), the weights into
 //               shared memory in the 128-byte-swizzled K-major layout
 //   warps 20-23 loaders: copy raw tiles from global memory into an 8-deep
 //               shared-memory ring with 16-byte cp.async; each thread's
 //               copies arrive on the slot's barrier as they land, so the
 //               whole ring can be in flight
-//   warp 24     allocates TMEM; one lane issues tcgen05.mma and one
-//               tcgen05.commit per k-step (which frees the stage)
+//   warp 24     allocates TMEM; one lane issues tcgen05.mma
 // Every hand-off between roles is one mbarrier arrival per warp, except
 // "stage full" (converters -> MMA warp), which is a named barrier per stage.
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
 // so the widened activations never pass through shared memory, whose
 // bandwidth the weight stores, the raw copies and the MMA's reads of B share.
-// Shared memory holds four fp16 weight stages (n_tile x 64, n_tile <= 192) and
-// eight raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM holds two
+// Shared memory holds kStages fp16 weight stages (n_tile x 64) and kRawStages
+// raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM holds two
 // 128 x n_tile fp32 accumulators, so the epilogue of one tile overlaps the
-// MMAs of the next, and four 128 x 64 fp16 activation stages.  Every mbarrier
-// wait is bounded by the global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
+// MMAs of the next, and kStages 128 x 64 fp16 activation stages.  Every mbarrier wait is bounded by the
+// global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
 #include "common.cuh"
@@ -46,14 +45,10 @@ namespace {
 
 using namespace tc;
 
-// Six stages of 160-wide tiles measured slower than four of 192-wide ones
-// (150 vs 131 us at M = 2048, K = 2560 -> N = 10240): the k-step time did not
-// change, so it is not the stages' commit round trip that sets it.
 constexpr int kStages = 4;                       // fp16 operand stages read by the MMA
 constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring
 constexpr int kTileM = 128;
 constexpr int kMaxTileN = 192;                   // multiple of 16; TMEM holds 2 x 192 + 4 x 32 columns
-constexpr int kDoneRing = 16;                    // kstep_done barriers: flat k-step f uses f % 16
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
 constexpr int kBBytes = kMaxTileN * 128;         // 26 KB of fp16 weights per stage
 constexpr int kStageBytes = kBBytes;             // (the fp16 activations of a stage live in TMEM)
@@ -62,7 +57,7 @@ constexpr int kRawBBytes = kMaxTileN * 16;       // 3.25 KB of packed codes
 constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
-constexpr int kConvGroups = 4;                      // group g converts the k-steps f with f % 4 == g
+constexpr int kConvGroups = kStages;                // group g converts the k-steps f with f % kStages == g
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;     // 128
 constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 16
@@ -76,8 +71,6 @@ static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per conve
 static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
 static_assert(kThreads * 80 <= 65536, "80 registers a thread for one CTA per SM");
 static_assert(kStages + 1 <= 16, "named barriers 1 .. kStages");
-static_assert((kDoneRing & (kDoneRing - 1)) == 0 && kDoneRing > kStages,
-              "a kstep_done barrier is reused only after its waiters are past");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
 constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
@@ -101,8 +94,7 @@ struct PrefillParams {
 };
 
 struct SharedCtl {
-  unsigned long long kstep_done[kDoneRing];  // the MMAs of flat k-step f are complete (tcgen05.commit):
-                                            // stage f % kStages is free; "full" is named barrier 1 + stage
+  unsigned long long empty[kStages];  // stage s consumed (tcgen05.commit); "full" is named barrier 1 + s
   unsigned long long raw_full[kRawStages];
   unsigned long long raw_empty[kRawStages];
   unsigned long long tmem_full[2];
@@ -151,7 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage_base = (raw_addr + 1023u) & ~1023u;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDoneRing; ++s) mbar_init(&ctl.kstep_done[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl.empty[s], 1);
+    }
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(&ctl.raw_full[s], kLoadThreads);
       mbar_init(&ctl.raw_empty[s], kGroupWarps);
@@ -251,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
   } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
     // ------------------------------------------------------------------ converters
-    // Group g (4 warps) converts the flat k-steps f = g, g + 4, ... into stage
-    // f % kStages, so the groups work on different k-steps at once.  Thread u of a
+    // Group g (4 warps) converts the flat k-steps f = g, g + kStages, ... into
+    // stage g, so the groups work on different k-steps at once.  Thread u of a
     // group widens activation row u (its warp's TMEM lanes are rows 32(u/32)
     // ..) and weight half-rows u + 128j (half h of row r: k = 32h .. 32h+31 of
     // the row's packed chunk).
@@ -264,36 +258,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cks = grp, ctile = blockIdx.x;             // k-step f as (tile, k-step in tile)
     while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
     int n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
-    // Every k-step f this group owns ends with its arrival on named barrier
-    // 1 + f % kStages (one barrier per stage), after an abort too (without the
-    // work), and never before the MMAs of k-step f - kStages, the stage's
-    // previous user, were committed (a wait that ignores the abort flag; the
-    // MMA warp keeps committing after an abort).  The MMA warp syncs that
-    // barrier for k-step f - kStages before it commits it, so each phase of a
+    // Every k-step this group owns ends with its arrival on the stage's named
+    // barrier, after an abort too (without the work), and never before the
+    // stage's previous MMAs were committed (a wait that ignores the abort flag;
+    // the MMA warp keeps committing after an abort): so each phase of the
     // barrier holds one k-step's converters and the MMA warp's sync of that
     // k-step, and the MMA warp's syncs, which cannot time out, always complete.
     bool live = true;
     for (int f = grp; f < total; f += kConvGroups) {
       const int slot = f % kRawStages;
       const uint32_t use = (uint32_t)(f / kRawStages);
-      const int stage = f % kStages;
-      const int prev = f - kStages;  // the stage's previous k-step
-      const bool stage_free =
-          prev < 0 || mbar_wait_lockstep(&ctl.kstep_done[prev & (kDoneRing - 1)], (uint32_t)((prev / kDoneRing) & 1),
-                                         &ctl.abort_flag, p.status);
+      const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
+      const bool stage_free = mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl.abort_flag, p.status);
       live = live && stage_free && mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl.abort_flag, p.status);
       if (!live) {
-        named_bar_arrive(1 + stage, kGroupThreads + 32);
+        named_bar_arrive(1 + grp, kGroupThreads + 32);
         continue;
       }
       const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
       tc_fence_after();  // the MMAs that read this stage are complete
-      const uint32_t b_tile = stage_base + (uint32_t)stage * kStageBytes;
+      const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
       if constexpr (SWAP) {
         // Weights: row u of the tile (its 64 codes of this k-block) -> TMEM lane u.
         const uint4 wv = ld_shared_v4(raw + kRawABytes + (uint32_t)(u * 16));
         const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
-                                (uint32_t)stage * kTmemAStageCols;
+                                (uint32_t)grp * kTmemAStageCols;
         uint32_t cols[16];
         codes_to_f16x8(wv.x, cols);
         codes_to_f16x8(wv.y, cols + 8);
@@ -320,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // Activations: row u of the tile -> TMEM lane u, columns of the stage.
+        // Activations: row u of the tile -> TMEM lane u, columns of stage grp.
         const uint32_t row_raw = raw + (uint32_t)(u * kKStep);
         const uint32_t sw = (uint32_t)((u >> 1) & 3);
         const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
-                                (uint32_t)stage * kTmemAStageCols;
+                                (uint32_t)grp * kTmemAStageCols;
 #pragma unroll
         for (int hpair = 0; hpair < 2; ++hpair) {  // pieces 2h, 2h+1 -> columns 16h .. 16h+15
           uint32_t cols[16];
@@ -357,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.raw_empty[slot]);  // one arrival per warp
-      named_bar_arrive(1 + stage, kGroupThreads + 32);
+      named_bar_arrive(1 + grp, kGroupThreads + 32);
       cks += kConvGroups;
       if (cks >= p.KB) {
         while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
@@ -375,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const uint32_t idesc = make_idesc(kTileM, p.mma_n);
       int stage = 0;
-      int f = 0;  // flat k-step
       bool aborted = false;
       int it = 0;
       for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
@@ -400,11 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (ks | kk) != 0 ? 1u : 0u);
               }
             }
-            mma_commit(&ctl.kstep_done[f & (kDoneRing - 1)]);
+            mma_commit(&ctl.empty[stage]);
           }
           __syncwarp();
           if (++stage == kStages) stage = 0;
-          ++f;
         }
         if (lane == 0) mma_commit(&ctl.tmem_full[slot]);
       }

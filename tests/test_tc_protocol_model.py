@@ -53,14 +53,17 @@ def kernel_constants():
 
 
 def prefill_constants():
+    """prefill.cu: four stages, converter group g = stage g = named barrier
+    1 + g, and the stage's commit barrier empty[g] (phase f / 4 for k-step f)."""
     text = open(SRC_PREFILL).read()
-    c = dict(ring=int(_const(text, "kRawStages")), done=int(_const(text, "kDoneRing")),
-             stages=int(_const(text, "kStages")), groups=int(_const(text, "kConvGroups")),
-             gw=int(_const(text, "kGroupWarps")), loaders=int(_const(text, "kLoadWarps")), gate="conv")
-    assert "named_bar_arrive(1 + stage, kGroupThreads + 32);" in text and "named_bar_sync(1 + stage" in text
-    assert "const int prev = f - kStages;" in text and "const int stage = f % kStages;" in text
+    stages = int(_const(text, "kStages"))
+    assert _const(text, "kConvGroups") == "kStages"
+    assert "named_bar_arrive(1 + grp, kGroupThreads + 32);" in text and "named_bar_sync(1 + stage" in text
+    assert "mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u" in text and "mma_commit(&ctl.empty[stage]);" in text
     assert "mbar_wait(&ctl.raw_empty[slot]" in text
-    return c
+    # empty[g] serves the k-steps f with f % stages == g: a done ring of `stages` barriers
+    return dict(ring=int(_const(text, "kRawStages")), done=stages, stages=stages, groups=stages,
+                gw=int(_const(text, "kGroupWarps")), loaders=int(_const(text, "kLoadWarps")), gate="conv")
 
 
 class MBar:
