@@ -176,10 +176,15 @@ bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M,
   bitlinear_status st = check_nk(N, K);
   if (st != BITLINEAR_OK) return st;
   if (M < 0 || M > kMaxDim) return BITLINEAR_ERR_SHAPE;
+  // y holds M * N floats; below 2^40 every tile and work-unit count of the
+  // kernels fits in 32 bits.
+  if (M * N >= ((int64_t)1 << 40)) return BITLINEAR_ERR_SHAPE;
   if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
   if (algo != BITLINEAR_ALGO_AUTO && algo != BITLINEAR_ALGO_DECODE && algo != BITLINEAR_ALGO_PREFILL &&
       algo != BITLINEAR_ALGO_BATCHED && algo != BITLINEAR_ALGO_WIDE)
     return BITLINEAR_ERR_UNSUPPORTED;
+  // the WIDE pre-pass indexes the 16-byte chunks of a k-block plane (8 per row) in 32 bits
+  if (algo == BITLINEAR_ALGO_WIDE && (M + 15) / 16 * 16 * 8 > (int64_t)0x7fffffff) return BITLINEAR_ERR_UNSUPPORTED;
   if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL
   if (!xq || !x_scale || !y) return BITLINEAR_ERR_NULL;
   if (!aligned16(xq) || !aligned16(packed) || !aligned16(y) || (acc && !aligned16(acc)) ||
@@ -251,6 +256,7 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
     if (!w.packed || !w.w_scale) return BITLINEAR_ERR_NULL;
     const bitlinear_status st = check_nk(w.N, K);
     if (st != BITLINEAR_OK) return st;
+    if (M * w.N >= ((int64_t)1 << 40)) return BITLINEAR_ERR_SHAPE;  // as bitlinear_forward
     if (!aligned16(w.packed) || (reinterpret_cast<uintptr_t>(w.w_scale) & 3u)) return BITLINEAR_ERR_ALIGN;
   }
   if (M == 0) return BITLINEAR_OK;  // empty batch: the M-sized buffers may be NULL

@@ -27,8 +27,8 @@
  *    only enqueues work: results are ready when the stream reaches them.
  *  - Argument errors are reported synchronously, before anything is enqueued:
  *    a NULL required pointer, a non-positive N or K, a negative M, K not a
- *    multiple of 64, a pointer not aligned to 16 bytes, or a too small
- *    workspace.  M == 0 is a valid empty batch and enqueues nothing.
+ *    multiple of 64, M * N >= 2^40 or N * K >= 2^40, a pointer not aligned to
+ *    16 bytes, or a too small workspace.  M == 0 is a valid empty batch and enqueues nothing.
  *  - A failed launch returns BITLINEAR_ERR_CUDA.  Every wait inside a kernel
  *    is bounded; a wait that runs out records BITLINEAR_ERR_TIMEOUT in a
  *    per-device status word that bitlinear_device_status() reports.

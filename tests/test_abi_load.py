@@ -61,6 +61,7 @@ def test_forward_argument_errors(lib):
     assert f(A, A, 1, A, A, 64, 64, A, None, 7, 0, None) == -4             # unknown algo
     assert f(A, A, 129, A, A, 64, 64, A, None, 3, 0, None) == -4           # batched past 128 tokens
     assert f(A, A, 1, A, A, 64, 64, A, None, 0, 8, None) == -4             # unknown flag
+    assert f(A, A, 1 << 20, A, A, 1 << 20, 64, A, None, 0, 0, None) == -2  # M * N >= 2^40
     assert f(A, A, 0, A, A, 64, 64, A, None, 0, 0, None) == 0              # empty batch
 
 
@@ -74,6 +75,8 @@ def test_forward_ws_argument_errors(lib):
     assert f(A, A, 17, A, A, 64, 128, A, None, 4, 0, U, ws, None) == -3         # misaligned workspace
     assert f(A, A, 17, A, A, 64, 100, A, None, 4, 0, A, ws, None) == -2         # K % 64
     assert f(A, A, 17, A, A, 64, 128, A, None, 9, 0, A, ws, None) == -4         # unknown algo
+    big = 1 << 28                                                                # 8 * M >= 2^31
+    assert f(A, A, big, A, A, 64, 64, A, None, 4, 0, A, big * 64 * 2, None) == -4
     assert f(A, A, 0, A, A, 64, 128, A, None, 4, 0, None, 0, None) == 0         # empty batch
     assert lib.bitlinear_forward_ex(A, A, 17, A, A, 64, 128, A, None, 4, 0, None) == -7  # WIDE needs _ws
 
