@@ -453,8 +453,10 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
 def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
     """BitNet-1.3B FFN sub-block (dim 2048, ffn 8192): RMSNorm -> act_quant ->
     gate || up -> ReLU^2(gate) * up -> sub-norm -> act_quant -> down, as two
-    bitlinear_linear calls (the prologues fused), seeded as in the parity test;
-    one CUDA graph of `reps` sub-blocks over rotating weight copies (> 4x L2)."""
+    bitlinear_linear_ws calls (the prologues fused; with a workspace, so the
+    WIDE kernel takes the matrices its AUTO rule gives it), seeded as in the
+    parity test; one CUDA graph of `reps` sub-blocks over rotating weight
+    copies (> 4x L2)."""
     import torch
     from bitlinear_w1_a8_gb300 import synth
     s = synth.SEEDS["ffn_1b3"]
@@ -481,13 +483,14 @@ def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
         yg = torch.empty(M, F, dtype=torch.float32, device=dev)
         yu = torch.empty(M, F, dtype=torch.float32, device=dev)
         yd = torch.empty(M, D, dtype=torch.float32, device=dev)
+        fws = torch.empty(bl.bitlinear_forward_workspace(M, F), dtype=torch.uint8, device=dev)
 
         def block(i, st):
             (g, sg), (u, su), (d, sd) = sets[i % copies]
-            bl.bitlinear_linear(x, [(g, sg, yg), (u, su, yu)], xq, sx, rms_weight=gamma, rms_eps=1e-6,
-                                flags=bl.FLAG_PDL, stream=st)
-            bl.bitlinear_linear(yg, [(d, sd, yd)], hq, hsx, mul=yu, rms_weight=gamma_sub, rms_eps=1e-6,
-                                flags=bl.FLAG_PDL, stream=st)
+            bl.bitlinear_linear_ws(x, [(g, sg, yg), (u, su, yu)], xq, sx, fws, rms_weight=gamma, rms_eps=1e-6,
+                                   flags=bl.FLAG_PDL, stream=st)
+            bl.bitlinear_linear_ws(yg, [(d, sd, yd)], hq, hsx, fws, mul=yu, rms_weight=gamma_sub, rms_eps=1e-6,
+                                   flags=bl.FLAG_PDL, stream=st)
 
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):

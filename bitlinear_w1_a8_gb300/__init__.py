@@ -18,7 +18,8 @@ __all__ = [
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
     "bitlinear_forward_workspace", "bitlinear_forward_ws",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
-    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax", "BitLinearWeight",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_linear_ws", "bitlinear_argmax",
+    "BitLinearWeight",
     "EXPORTED_SYMBOLS",
     "ALGO_AUTO", "ALGO_DECODE", "ALGO_PREFILL", "ALGO_BATCHED", "ALGO_WIDE", "FLAG_PDL",
 ]
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
     "bitlinear_forward_workspace", "bitlinear_forward_ws",
     "bitlinear_device_status", "bitlinear_quantize_weights_noalloc",
-    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_argmax",
+    "bitlinear_selftest_wait_timeout", "bitlinear_linear", "bitlinear_linear_ws", "bitlinear_argmax",
 )
 
 _lib = None
@@ -101,6 +102,9 @@ def load_library(path: str | None = None):
     lib.bitlinear_linear.argtypes = [vp, vp, i64, i64, vp, ctypes.c_double, ctypes.POINTER(BitLinearWeight),
                                      ctypes.c_int, vp, vp, ctypes.c_int, vp]
     lib.bitlinear_linear.restype = st
+    lib.bitlinear_linear_ws.argtypes = [vp, vp, i64, i64, vp, ctypes.c_double, ctypes.POINTER(BitLinearWeight),
+                                        ctypes.c_int, vp, vp, ctypes.c_int, vp, sz, vp]
+    lib.bitlinear_linear_ws.restype = st
     lib.bitlinear_argmax.argtypes = [vp, i64, i64, vp, vp]
     lib.bitlinear_argmax.restype = st
     lib.bitlinear_device_status.argtypes = [vp, ctypes.c_int]
@@ -288,22 +292,8 @@ def bitlinear_selftest_wait_timeout(limit_ns: int, stream=None):
            "bitlinear_selftest_wait_timeout")
 
 
-def bitlinear_linear(x, weights, xq, x_scale, mul=None, rms_weight=None, rms_eps: float = 1e-6,
-                     flags: int = 0, stream=None):
-    """act_quant + forward for 1..4 matrices sharing the input x [M, K].
-
-    weights: sequence of (packed, w_scale, y) or (packed, w_scale, y, acc) tuples of
-    CUDA tensors (y [M, N] fp32, acc [M, N] int32 or None).
-    """
+def _weight_array(weights, M, K):
     import torch
-    _need(x, torch.float32, "x")
-    M, K = x.shape
-    _need(xq, torch.int8, "xq", (M, K))
-    _need(x_scale, torch.float32, "x_scale", (M,))
-    if mul is not None:
-        _need(mul, torch.float32, "mul", (M, K))
-    if rms_weight is not None:
-        _need(rms_weight, torch.float32, "rms_weight", (K,))
     arr = (BitLinearWeight * len(weights))()
     for i, w in enumerate(weights):
         packed, w_scale, y = w[0], w[1], w[2]
@@ -316,6 +306,46 @@ def bitlinear_linear(x, weights, xq, x_scale, mul=None, rms_weight=None, rms_eps
             _need(acc, torch.int32, "acc", (M, N))
         arr[i] = BitLinearWeight(packed.data_ptr(), w_scale.data_ptr(), N, y.data_ptr(),
                                  acc.data_ptr() if acc is not None else None)
+    return arr
+
+
+def _linear_inputs(x, xq, x_scale, mul, rms_weight):
+    import torch
+    _need(x, torch.float32, "x")
+    M, K = x.shape
+    _need(xq, torch.int8, "xq", (M, K))
+    _need(x_scale, torch.float32, "x_scale", (M,))
+    if mul is not None:
+        _need(mul, torch.float32, "mul", (M, K))
+    if rms_weight is not None:
+        _need(rms_weight, torch.float32, "rms_weight", (K,))
+    return M, K
+
+
+def bitlinear_linear(x, weights, xq, x_scale, mul=None, rms_weight=None, rms_eps: float = 1e-6,
+                     flags: int = 0, stream=None):
+    """act_quant + forward for 1..4 matrices sharing the input x [M, K].
+
+    weights: sequence of (packed, w_scale, y) or (packed, w_scale, y, acc) tuples of
+    CUDA tensors (y [M, N] fp32, acc [M, N] int32 or None).
+    """
+    M, K = _linear_inputs(x, xq, x_scale, mul, rms_weight)
+    arr = _weight_array(weights, M, K)
     _check(load_library().bitlinear_linear(
         _ptr(x), _ptr(mul), M, K, _ptr(rms_weight), float(rms_eps), arr, len(weights), _ptr(xq),
         _ptr(x_scale), int(flags), _stream(stream)), "bitlinear_linear")
+
+
+def bitlinear_linear_ws(x, weights, xq, x_scale, workspace, mul=None, rms_weight=None, rms_eps: float = 1e-6,
+                        flags: int = 0, stream=None):
+    """bitlinear_linear with a device workspace (uint8 CUDA tensor of at least
+    bitlinear_forward_workspace(M, K) bytes, or None)."""
+    import torch
+    M, K = _linear_inputs(x, xq, x_scale, mul, rms_weight)
+    arr = _weight_array(weights, M, K)
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+    _check(load_library().bitlinear_linear_ws(
+        _ptr(x), _ptr(mul), M, K, _ptr(rms_weight), float(rms_eps), arr, len(weights), _ptr(xq),
+        _ptr(x_scale), int(flags), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)), "bitlinear_linear_ws")

@@ -15,7 +15,7 @@ cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const u
 // 192 tokens per tile.
 size_t wide_workspace_bytes(int64_t M, int64_t K);
 cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
-                        int64_t N, int64_t K, float* y, int32_t* acc, void* workspace, bool pdl,
+                        int64_t N, int64_t K, float* y, int32_t* acc, void* workspace, bool widen, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream);
 }  // namespace bitlinear
 
@@ -82,6 +82,17 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 16 && K <= 65536 && !(K >= 8192 && M > 8)) return BITLINEAR_ALGO_DECODE;
   if (M <= 128 && N <= 4096 && (M >= 64 || K < 8192)) return BITLINEAR_ALGO_BATCHED;
   return BITLINEAR_ALGO_PREFILL;
+}
+
+// With a workspace, AUTO takes the WIDE kernel for narrow outputs at medium
+// token counts, where it measured faster on GB300 (hot L2, pre-pass included;
+// WIDE vs the AUTO kernel): N = 2560, K = 10240: 1.40 / 1.19 / 1.41 / 1.09x at
+// M = 128 / 256 / 512 / 1024; N = K = 2560: 1.29 / 1.71 / 1.03x at M = 128 /
+// 256 / 512 (0.89x at 1024); N = 2048, K = 8192: 1.39 / 1.38 / 1.38 / 1.06x;
+// wide outputs (N = 8192, 10240) and M = 2048: 0.79 - 1.00x.
+bool wide_wins(int64_t M, int64_t N, int64_t K) {
+  if (N > 4096 || M < 128 || M > 1024) return false;
+  return K >= 8192 || M <= 512;
 }
 
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
@@ -194,10 +205,10 @@ bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M,
   if (algo == BITLINEAR_ALGO_WIDE && !have_ws) return BITLINEAR_ERR_WORKSPACE;
   if (have_ws && !aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
   int use = algo;
-  // AUTO never picks WIDE: on GB300 the 128-token-tile kernel measured faster
-  // on the BitNet-3B prefill shapes (M = 2048: 130 vs 142 us for K = 2560 ->
-  // N = 10240, 148 vs 177 us for K = 10240 -> N = 2560, pre-pass included).
-  if (use == BITLINEAR_ALGO_AUTO) use = auto_algo(M, N, K);
+  if (use == BITLINEAR_ALGO_AUTO) {
+    use = auto_algo(M, N, K);
+    if (use != BITLINEAR_ALGO_DECODE && have_ws && K <= kPrefillMaxK && wide_wins(M, N, K)) use = BITLINEAR_ALGO_WIDE;
+  }
   if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
     return BITLINEAR_ERR_UNSUPPORTED;
   if ((use == BITLINEAR_ALGO_PREFILL || use == BITLINEAR_ALGO_WIDE) && K > kPrefillMaxK)
@@ -209,7 +220,7 @@ bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M,
   const bool pdl = (flags & BITLINEAR_FLAG_PDL) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use == BITLINEAR_ALGO_WIDE)
-    return from_cuda(launch_wide(xq, x_scale, M, packed, w_scale, N, K, y, acc, workspace, pdl, dev, s));
+    return from_cuda(launch_wide(xq, x_scale, M, packed, w_scale, N, K, y, acc, workspace, true, pdl, dev, s));
   if (use == BITLINEAR_ALGO_BATCHED)
     return from_cuda(launch_batched(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
   if (use == BITLINEAR_ALGO_DECODE) {
@@ -243,9 +254,13 @@ bitlinear_status bitlinear_forward_ws(const int8_t* xq, const float* x_scale, in
                       stream);
 }
 
-bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,
-                                  const float* rms_weight, double rms_eps, const bitlinear_weight* weights,
-                                  int num_weights, int8_t* xq, float* x_scale, int flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_t K, const float* rms_weight,
+                             double rms_eps, const bitlinear_weight* weights, int num_weights, int8_t* xq,
+                             float* x_scale, int flags, void* workspace, size_t workspace_bytes, void* stream) {
   if (!weights) return BITLINEAR_ERR_NULL;
   if (num_weights < 1 || num_weights > kMaxDecodeMats) return BITLINEAR_ERR_SHAPE;
   if (M < 0 || M > kMaxDim || K <= 0 || K % 64 != 0 || K > 32768) return BITLINEAR_ERR_SHAPE;
@@ -268,6 +283,9 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
     if (!weights[i].y) return BITLINEAR_ERR_NULL;
     if (!aligned16(weights[i].y) || (weights[i].acc && !aligned16(weights[i].acc))) return BITLINEAR_ERR_ALIGN;
   }
+  if (workspace && workspace_bytes < wide_workspace_bytes(M, K)) return BITLINEAR_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return BITLINEAR_ERR_ALIGN;
+  const bool have_ws = workspace != nullptr && (M + 15) / 16 * 16 * 8 <= (int64_t)0x7fffffff;
   DeviceInfo dev;
   bitlinear_status st = current_device(&dev);
   if (st != BITLINEAR_OK) return st;
@@ -294,18 +312,46 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
     err = launch_decode(xq, x_scale, M, dec, ndec, K, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
+  bool widened = false;  // the workspace holds this call's xq once a WIDE launch has widened it
   for (int i = 0; i < num_weights; ++i) {
     const int algo = auto_algo(M, mats[i].N, K);
     if (algo == BITLINEAR_ALGO_DECODE) continue;
-    err = algo == BITLINEAR_ALGO_BATCHED
-              ? launch_batched(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
-                               mats[i].acc, pdl, dev, s)
-              : launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
-                               mats[i].acc, pdl, dev, s);
+    if (have_ws && wide_wins(M, mats[i].N, K)) {
+      err = launch_wide(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
+                        workspace, !widened, pdl, dev, s);
+      widened = true;
+    } else {
+      err = algo == BITLINEAR_ALGO_BATCHED
+                ? launch_batched(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
+                                 mats[i].acc, pdl, dev, s)
+                : launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
+                                 mats[i].acc, pdl, dev, s);
+    }
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   return BITLINEAR_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,
+                                  const float* rms_weight, double rms_eps, const bitlinear_weight* weights,
+                                  int num_weights, int8_t* xq, float* x_scale, int flags, void* stream) {
+  return linear_impl(x, mul, M, K, rms_weight, rms_eps, weights, num_weights, xq, x_scale, flags, nullptr, 0,
+                     stream);
+}
+
+bitlinear_status bitlinear_linear_ws(const float* x, const float* mul, int64_t M, int64_t K,
+                                     const float* rms_weight, double rms_eps, const bitlinear_weight* weights,
+                                     int num_weights, int8_t* xq, float* x_scale, int flags, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return linear_impl(x, mul, M, K, rms_weight, rms_eps, weights, num_weights, xq, x_scale, flags, workspace,
+                     workspace_bytes, stream);
+}
+
+
 
 bitlinear_status bitlinear_argmax(const float* y, int64_t M, int64_t N, int32_t* index, void* stream) {
   if (M < 0 || M > kMaxDim || N <= 0 || N > 0x7fffffffLL) return BITLINEAR_ERR_SHAPE;

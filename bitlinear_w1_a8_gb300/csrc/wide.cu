@@ -431,8 +431,10 @@ size_t wide_workspace_bytes(int64_t M, int64_t K) {
   return (size_t)((M + 15) / 16 * 16) * (size_t)K * 2u;
 }
 
+// widen = false: the workspace already holds this xq (an earlier launch on the
+// stream widened it), so only the contraction kernel is launched.
 cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
-                        int64_t N, int64_t K, float* y, int32_t* acc, void* workspace, bool pdl,
+                        int64_t N, int64_t K, float* y, int32_t* acc, void* workspace, bool widen, bool pdl,
                         const DeviceInfo& dev, cudaStream_t stream) {
   if (M < 1 || N < 1 || K < kKStep || K % kKStep) return cudaErrorInvalidValue;
   const int64_t Mp = (M + 15) / 16 * 16;
@@ -481,7 +483,7 @@ cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint
     err = cudaMemsetAsync(y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
     if (err != cudaSuccess) return err;
   }
-  {
+  if (widen) {
     const int m32 = (int)M, mp32 = (int)Mp, k32 = (int)K;
     uint4* xw = static_cast<uint4*>(workspace);
     void* args[] = {(void*)&xq, (void*)&m32, (void*)&mp32, (void*)&k32, (void*)&xw};

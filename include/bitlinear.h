@@ -188,9 +188,11 @@ size_t bitlinear_forward_workspace(int64_t M, int64_t K);
  * the MMA's shared-memory operand, so the contraction kernel only widens the
  * 2-bit weight codes (into tensor memory) and bulk-copies the token tiles.
  * Results are bit-identical to every other algorithm.  BITLINEAR_ALGO_AUTO
- * follows bitlinear_forward's rule and does not pick WIDE (measured slower
- * than the 128-token-tile kernel on the BitNet-3B prefill shapes); the other
- * algorithms ignore the workspace.
+ * follows bitlinear_forward's rule, except that it takes WIDE for narrow
+ * outputs at medium token counts -- N <= 4096 and 128 <= M <= 1024 (M <= 512
+ * when K < 8192) -- where it measured 1.03-1.71x faster on GB300 (BitNet-3B
+ * q/k/v/o and down, BitNet-1.3B down shapes); for wide outputs and M = 2048 the
+ * other kernels measured faster.  The other algorithms ignore the workspace.
  * Errors: as bitlinear_forward_ex; BITLINEAR_ERR_WORKSPACE when
  * BITLINEAR_ALGO_WIDE is asked for without a large enough workspace;
  * BITLINEAR_ERR_ALIGN for a misaligned workspace.
@@ -232,6 +234,20 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
                                   const float* rms_weight, double rms_eps,
                                   const bitlinear_weight* weights, int num_weights,
                                   int8_t* xq, float* x_scale, int flags, void* stream);
+
+/*
+ * bitlinear_linear with an optional device workspace (NULL: exactly
+ * bitlinear_linear; otherwise 16-byte aligned and at least
+ * bitlinear_forward_workspace(M, K) bytes, else BITLINEAR_ERR_WORKSPACE).
+ * Matrices that bitlinear_forward_ws's AUTO rule gives to the WIDE kernel use
+ * it; the activations are widened into the workspace once per call, shared by
+ * those matrices.  Results are bit-identical to bitlinear_linear.
+ */
+bitlinear_status bitlinear_linear_ws(const float* x, const float* mul, int64_t M, int64_t K,
+                                     const float* rms_weight, double rms_eps,
+                                     const bitlinear_weight* weights, int num_weights,
+                                     int8_t* xq, float* x_scale, int flags,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the library's own device scratch array used by
  * bitlinear_quantize_weights_noalloc. */

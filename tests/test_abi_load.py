@@ -81,6 +81,17 @@ def test_forward_ws_argument_errors(lib):
     assert lib.bitlinear_forward_ex(A, A, 17, A, A, 64, 128, A, None, 4, 0, None) == -7  # WIDE needs _ws
 
 
+def test_linear_ws_argument_errors(lib):
+    f = lib.bitlinear_linear_ws
+    w = bl.BitLinearWeight(A, A, 64, A, None)
+    arr = (bl.BitLinearWeight * 1)(w)
+    ws = bl.bitlinear_forward_workspace(200, 128)
+    assert f(A, None, 200, 128, None, 1e-6, arr, 1, A, A, 0, A, ws - 16, None) == -7   # too small
+    assert f(A, None, 200, 128, None, 1e-6, arr, 1, A, A, 0, U, ws, None) == -3        # misaligned
+    assert f(A, None, 0, 128, None, 1e-6, arr, 1, A, A, 0, None, 0, None) == 0         # empty batch
+    assert f(A, None, 200, 100, None, 1e-6, arr, 1, A, A, 0, A, ws, None) == -2        # K % 64
+
+
 def test_quant_act_argument_errors(lib):
     f = lib.bitlinear_quant_act
     assert f(None, None, 1, 64, None, 1e-6, A, A, None) == -1

@@ -334,9 +334,14 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 128, (5,), None),                   # tiny
     (3, 640, (500, 77), None),              # M > 1: act_quant + one decode launch for both
     (130, 320, (257, 100), "norm"),         # tensor-core path per matrix
+    (200, 1024, (300, 1000, 2000), None),   # WIDE region (with ws): three matrices, one pre-pass
+    (256, 8192, (2048,), "gated+norm"),     # a 1.3B FFN down call in the WIDE region
 ])
-def test_linear_matches_oracle(M, K, Ns, prolog):
-    """bitlinear_linear (act_quant + forward for matrices sharing one input) against the oracle."""
+@pytest.mark.parametrize("ws", [False, True])
+def test_linear_matches_oracle(M, K, Ns, prolog, ws):
+    """bitlinear_linear (act_quant + forward for matrices sharing one input) against the oracle;
+    with ws, bitlinear_linear_ws with a canary-guarded workspace (the WIDE kernel takes the
+    matrices its AUTO rule gives it, widening the activations once for all of them)."""
     x = synth.activations(M, K, 60 + K, outlier_seed=61 + K)
     mul = synth.activations(M, K, 62 + K) if prolog and "gated" in prolog else None
     gamma = synth.uniform((K,), 0.5, 1.5, 63 + K) if prolog and "norm" in prolog else None
@@ -353,9 +358,16 @@ def test_linear_matches_oracle(M, K, Ns, prolog):
         mats.append((packed_d, sw_d, y, acc))
     xq = torch.zeros(M, K, dtype=torch.int8, device="cuda")
     sx = torch.zeros(M, dtype=torch.float32, device="cuda")
-    bl.bitlinear_linear(x.cuda(), mats, xq, sx, mul=None if mul is None else mul.cuda(),
-                        rms_weight=None if gamma is None else gamma.cuda(), rms_eps=1e-6, flags=bl.FLAG_PDL)
+    kw = dict(mul=None if mul is None else mul.cuda(), rms_weight=None if gamma is None else gamma.cuda(),
+              rms_eps=1e-6, flags=bl.FLAG_PDL)
+    if ws:
+        wsp, wfull = guarded(bl.bitlinear_forward_workspace(M, K), torch.uint8, 0x3C)
+        bl.bitlinear_linear_ws(x.cuda(), mats, xq, sx, wsp, **kw)
+    else:
+        bl.bitlinear_linear(x.cuda(), mats, xq, sx, **kw)
     assert bl.bitlinear_device_status() == 0
+    if ws:
+        check_canary(wfull, 0x3C)
     np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
     np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
     for (packed_d, sw_d, y, acc), (acc_o, y_o) in zip(mats, refs):
