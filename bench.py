@@ -374,7 +374,7 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
     packed bytes, > 4x L2).  One step = every BitLinear call of one decode step
     of M tokens in block order -- [q||k||v], [o], [gate||up], [down] per layer,
     then the LM head and the greedy token (bitlinear_argmax, 4 bytes a token)
-    -- each a bitlinear_linear call on seeded synthetic inputs
+    -- each a bitlinear_linear_ws call (one shared workspace) on seeded synthetic inputs
     (attention and residuals are not part of this path), replayed as one CUDA
     graph with PDL."""
     import torch
@@ -413,16 +413,18 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
         yq, yk, yv = (torch.empty(M, D, dtype=torch.float32, device=dev) for _ in range(3))
         yu = torch.empty(M, F, dtype=torch.float32, device=dev)
         token = torch.empty(M, dtype=torch.int32, device=dev)
+        fws = torch.empty(bl.bitlinear_forward_workspace(M, F), dtype=torch.uint8, device=dev)
 
         def step(s):
             for mats in layers:
                 (q, sq, _), (k, sk, _), (v, sv, _), (o, so, _), (g, sg, _), (u, su, _), (d, sd, _) = mats
-                bl.bitlinear_linear(xa, [(q, sq, yq), (k, sk, yk), (v, sv, yv)], xq_a, sx_a,
-                                    flags=bl.FLAG_PDL, stream=s)
-                bl.bitlinear_linear(xa, [(o, so, ys[D])], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
-                bl.bitlinear_linear(xa, [(g, sg, ys[F]), (u, su, yu)], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
-                bl.bitlinear_linear(xb, [(d, sd, ys[D])], xq_b, sx_b, flags=bl.FLAG_PDL, stream=s)
-            bl.bitlinear_linear(xa, [(head_pk, head_sc, ys[V])], xq_a, sx_a, flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear_ws(xa, [(q, sq, yq), (k, sk, yk), (v, sv, yv)], xq_a, sx_a, fws,
+                                       flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear_ws(xa, [(o, so, ys[D])], xq_a, sx_a, fws, flags=bl.FLAG_PDL, stream=s)
+                bl.bitlinear_linear_ws(xa, [(g, sg, ys[F]), (u, su, yu)], xq_a, sx_a, fws, flags=bl.FLAG_PDL,
+                                       stream=s)
+                bl.bitlinear_linear_ws(xb, [(d, sd, ys[D])], xq_b, sx_b, fws, flags=bl.FLAG_PDL, stream=s)
+            bl.bitlinear_linear_ws(xa, [(head_pk, head_sc, ys[V])], xq_a, sx_a, fws, flags=bl.FLAG_PDL, stream=s)
             bl.bitlinear_argmax(ys[V], token, stream=s)
 
         g = torch.cuda.CUDAGraph()

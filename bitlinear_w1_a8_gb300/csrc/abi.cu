@@ -86,13 +86,16 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
 
 // With a workspace, AUTO takes the WIDE kernel for narrow outputs at medium
 // token counts, where it measured faster on GB300 (hot L2, pre-pass included;
-// WIDE vs the AUTO kernel): N = 2560, K = 10240: 1.40 / 1.19 / 1.41 / 1.09x at
-// M = 128 / 256 / 512 / 1024; N = K = 2560: 1.29 / 1.71 / 1.03x at M = 128 /
-// 256 / 512 (0.89x at 1024); N = 2048, K = 8192: 1.39 / 1.38 / 1.38 / 1.06x;
-// wide outputs (N = 8192, 10240) and M = 2048: 0.79 - 1.00x.
+// WIDE vs the AUTO kernel, at M = 32 / 64 / 96 / 128 / 256 / 512 / 1024):
+//   N = 2560, K = 10240: 1.10 / 1.25 / 1.33 / 1.40 / 1.19 / 1.41 / 1.09x
+//   N = 2048, K = 8192:  1.21 / 1.23 / 1.26 / 1.39 / 1.38 / 1.38 / 1.06x
+//   N = K = 2560:        0.93 / 1.03 / 1.10 / 1.29 / 1.71 / 1.03 / 0.89x
+//   N = K = 2048:        0.85 / 0.96 / 1.26 (M <= 96 measured)
+// and for wide outputs (N = 8192, 10240) and at M = 2048: 0.67 - 1.00x.
 bool wide_wins(int64_t M, int64_t N, int64_t K) {
-  if (N > 4096 || M < 128 || M > 1024) return false;
-  return K >= 8192 || M <= 512;
+  if (N > 4096 || M > 1024) return false;
+  if (K >= 8192) return M >= 32;
+  return M >= 96 && M <= 512;
 }
 
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
