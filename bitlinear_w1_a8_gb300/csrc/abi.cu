@@ -92,9 +92,12 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
 //   N = K = 2560:        0.93 / 1.03 / 1.10 / 1.29 / 1.71 / 1.03 / 0.89x
 //   N = K = 2048:        0.85 / 0.96 / 1.26 (M <= 96 measured)
 // and for wide outputs (N = 8192, 10240) and at M = 2048: 0.67 - 1.00x.
+// In a whole BitNet-3B token step (cold weights, the pre-pass one more launch
+// on the chain) the down projections at M = 32 made the step 1.8 % slower
+// (at M = 64, 0.8 % faster): long K starts at M = 64.
 bool wide_wins(int64_t M, int64_t N, int64_t K) {
   if (N > 4096 || M > 1024) return false;
-  if (K >= 8192) return M >= 32;
+  if (K >= 8192) return M >= 64;
   return M >= 96 && M <= 512;
 }
 

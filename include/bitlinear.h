@@ -189,7 +189,7 @@ size_t bitlinear_forward_workspace(int64_t M, int64_t K);
  * 2-bit weight codes (into tensor memory) and bulk-copies the token tiles.
  * Results are bit-identical to every other algorithm.  BITLINEAR_ALGO_AUTO
  * follows bitlinear_forward's rule, except that it takes WIDE for narrow
- * outputs at medium token counts -- N <= 4096 and 32 <= M <= 1024 when
+ * outputs at medium token counts -- N <= 4096 and 64 <= M <= 1024 when
  * K >= 8192, 96 <= M <= 512 otherwise -- where it measured 1.03-1.71x faster
  * on GB300 (BitNet-3B q/k/v/o and down, BitNet-1.3B down shapes); for wide
  * outputs and at M = 2048 the other kernels measured faster.  The other algorithms ignore the workspace.
