@@ -20,13 +20,17 @@
 //               tiles of every fourth k-step to fp16 in stage g -- the
 //               activations into TMEM (one row per lane), the weights into
 //               shared memory in the 128-byte-swizzled K-major layout
-//   warps 20-23 loaders: copy raw tiles from global memory into an 8-deep
-//               shared-memory ring with 16-byte cp.async; each thread's
-//               copies arrive on the slot's barrier as they land, so the
-//               whole ring can be in flight
+//   warps 20-23 loader: one thread of warp 20 fills an 8-deep shared-memory
+//               ring, per k-step one TMA tensor copy of the 128 x 64 int8
+//               activation tile (64-byte swizzle) and one bulk copy of the
+//               packed codes, completing on the slot's barrier; warps 21-23
+//               only reach the final barrier (16-byte cp.async from 128
+//               loader threads had bounded the 192-wide k-step: 130.7 ->
+//               121.3 us at M = 2048, K = 2560 -> N = 10240)
 //   warp 24     allocates TMEM; one lane issues tcgen05.mma
-// Every hand-off between roles is one mbarrier arrival per warp, except
-// "stage full" (converters -> MMA warp), which is a named barrier per stage.
+// Every hand-off between roles is one mbarrier arrival per warp (raw slot
+// full: the loader's arrive.expect_tx plus the copies' transaction bytes),
+// except "stage full" (converters -> MMA warp), a named barrier per stage.
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
 // so the widened activations never pass through shared memory, whose
 // bandwidth the weight stores, the raw copies and the MMA's reads of B share.
@@ -37,6 +41,8 @@
 // global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
 // status word, every role leaves its loop, the MMA warp waits (bounded) for
 // its own MMAs, frees TMEM and the kernel returns.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "tc_util.cuh"
 
@@ -78,6 +84,7 @@ static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget")
 static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
 
 struct PrefillParams {
+  CUtensorMap tmap_a;  // xq [M, K] int8: 64 x 128 boxes, 64-byte swizzle (the raw ring's layout)
   const int8_t* xq;
   const float* sx;
   const uint4* packed;
@@ -147,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&ctl.raw_full[s], kLoadThreads);
+      mbar_init(&ctl.raw_full[s], 1);
       mbar_init(&ctl.raw_empty[s], kGroupWarps);
     }
     for (int s = 0; s < 2; ++s) {
@@ -172,77 +179,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
-    // ------------------------------------------------------------------ loaders
-    // Copy each raw k-step (128 x 64 int8 activations, n_tile x 16 B packed
-    // codes) into the raw ring with 16-byte cp.async (coalesced: a warp covers
-    // 8 activation rows or 32 weight rows); a slot is handed over once every
-    // loader thread's copies into it have landed.
-    // Source addresses are set once per tile and advanced per k-step: with
-    // one loader warp per scheduler, index arithmetic would otherwise set the
-    // pace.
-    const int v = threadIdx.x - kLoadWarp0 * 32;  // 0 .. 127
-    constexpr int kAPieces = kTileM * kKStep / 16 / kLoadThreads;  // activation pieces per thread
-    constexpr int kBRows = (kMaxTileN + kLoadThreads - 1) / kLoadThreads;  // weight rows per thread
-    const int8_t* a_src[kAPieces];
-    uint32_t a_bytes[kAPieces], a_dst[kAPieces];
-    // Raw activation row r keeps its 16-byte piece q at r*64 + 16*(q ^ ((r/2) % 4)),
-    // so a quarter-warp reading one piece of 8 consecutive rows hits 8 bank groups.
-#pragma unroll
-    for (int i = 0; i < kAPieces; ++i) {
-      const int idx = v + i * kLoadThreads, row = idx >> 2, q = idx & 3;
-      a_dst[i] = (uint32_t)(row * kKStep + ((q ^ ((row >> 1) & 3)) << 4));
-    }
-    const uint4* b_src[kBRows];
-    uint32_t b_bytes[kBRows];
-    int ks = 0, tile = blockIdx.x;
-    auto start_tile = [&]() {
-      int m0, n0, kb0;
-      tile_coords(p, tile, m0, n0, kb0);
-#pragma unroll
-      for (int i = 0; i < kAPieces; ++i) {
-        const int idx = v + i * kLoadThreads;  // 16-byte piece: row idx/4, piece idx%4
-        const int am = m0 + (idx >> 2);
-        const bool in = am < p.M;
-        a_src[i] = p.xq + (int64_t)(in ? am : 0) * p.K + (int64_t)kb0 * kKStep + (idx & 3) * 16;
-        a_bytes[i] = in ? 16u : 0u;  // rows past M read as zeros
-      }
-#pragma unroll
-      for (int j = 0; j < kBRows; ++j) {
-        const int bn = n0 + v + j * kLoadThreads;
-        const bool in = bn < p.N;
-        b_src[j] = p.packed + (int64_t)kb0 * p.N + (in ? bn : 0);
-        b_bytes[j] = in ? 16u : 0u;
-      }
-    };
-    if (total > 0) start_tile();
-    int slot = 0;
-    uint32_t parity = 0;
-    for (int f = 0; f < total; ++f) {
-      {
-        if (!mbar_wait(&ctl.raw_empty[slot], parity ^ 1u, &ctl.abort_flag, p.status)) break;
+    // ------------------------------------------------------------------ loader
+    // One thread per k-step: arms the slot's barrier with the bytes of both
+    // copies, then one TMA tensor copy brings the 128 x 64 int8 activation
+    // tile (64-byte swizzle: piece q of row r at q ^ ((r / 2) % 4); rows past
+    // M read as zeros) and one bulk copy the packed codes of the tile's rows.
+    if (warp == kLoadWarp0 && lane == 0) {
+      int ks = 0, tile = blockIdx.x;
+      int m0 = 0, n0 = 0, kb0 = 0;
+      uint32_t code_bytes = 0;
+      auto start_tile = [&]() {
+        tile_coords(p, tile, m0, n0, kb0);
+        const int rows = p.N - n0 < p.n_tile ? p.N - n0 : p.n_tile;  // rows past N are not read
+        code_bytes = (uint32_t)rows * 16u;
+      };
+      if (total > 0) start_tile();
+      int last = -1;
+      for (int f = 0; f < total; ++f) {
+        const int slot = f % kRawStages;
+        const uint32_t use = (uint32_t)(f / kRawStages);
+        if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl.abort_flag, p.status)) break;
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
-#pragma unroll
-        for (int i = 0; i < kAPieces; ++i) {
-          cp_async16(raw + a_dst[i], a_src[i], a_bytes[i]);
-          a_src[i] += kKStep;
-        }
-#pragma unroll
-        for (int j = 0; j < kBRows; ++j) {
-          const int row = v + j * kLoadThreads;
-          if (row < p.n_tile) cp_async16(raw + kRawABytes + (uint32_t)(row * 16), b_src[j], b_bytes[j]);
-          b_src[j] += p.N;
-        }
-        // this thread's arrival on raw_full lands once its copies above have
-        cp_async_arrive(&ctl.raw_full[slot]);
+        mbar_arrive_expect_tx(&ctl.raw_full[slot], (uint32_t)kRawABytes + code_bytes);
+        const int kx = (kb0 + ks) * kKStep;  // a multiple of 64 bytes
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(raw), "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kx), "r"(m0),
+              "r"(smem_u32(&ctl.raw_full[slot]))
+            : "memory");
+        bulk_copy_g2s(raw + kRawABytes, p.packed + ((int64_t)(kb0 + ks) * p.N + n0), code_bytes, &ctl.raw_full[slot]);
+        last = f;
         if (++ks == p.KB) {
           ks = 0;
           tile += gridDim.x;
           if (f + 1 < total) start_tile();
         }
-        if (++slot == kRawStages) { slot = 0; parity ^= 1u; }
       }
+      // No copy may outlive the CTA: wait (bounded) for the last fills.
+      for (int f = last; f >= 0 && f > last - kRawStages; --f)
+        mbar_drain(&ctl.raw_full[f % kRawStages], (uint32_t)((f / kRawStages) & 1), p.status);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
+    __syncwarp();
   } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
     // ------------------------------------------------------------------ converters
     // Group g (4 warps) converts the flat k-steps f = g, g + kStages, ... into
@@ -594,9 +571,37 @@ cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cuda
   return launch_rescale(p.y, p.acc, p.sx, p.sw, M, N, dev, stream);
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
 PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
                             int64_t N, int64_t K, float* y, int32_t* acc, const DeviceInfo& dev) {
   PrefillParams p;
+  p.KB = 0;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K};
+    const cuuint32_t box[2] = {(cuuint32_t)kKStep, (cuuint32_t)kTileM};
+    const cuuint32_t estr[2] = {1, 1};
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || fn(&p.tmap_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(xq), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      p.KB = -1;  // reported by the launchers
+  }
   p.xq = xq;
   p.sx = sx;
   p.packed = reinterpret_cast<const uint4*>(packed);
@@ -607,7 +612,7 @@ PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const 
   p.M = (int)M;
   p.N = (int)N;
   p.K = (int)K;
-  p.KB = (int)(K / kKStep);
+  if (p.KB != -1) p.KB = (int)(K / kKStep);
   return p;
 }
 
@@ -634,6 +639,7 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+  if (p.KB < 0) return cudaErrorNotSupported;
   // Tile width and K split together: the fewest (k-steps of the busiest CTA)
   // x (tile width + 64), the +64 being the activation widening of a k-step.
   {
@@ -664,6 +670,7 @@ cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const u
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   if (M < 1 || M > kTileM) return cudaErrorInvalidValue;
   PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+  if (p.KB < 0) return cudaErrorNotSupported;
   p.n_tile = kTileM;
   p.mma_n = (int)((M + 15) / 16 * 16);
   p.tiles_m = 1;

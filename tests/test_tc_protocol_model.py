@@ -61,9 +61,11 @@ def prefill_constants():
     assert "named_bar_arrive(1 + grp, kGroupThreads + 32);" in text and "named_bar_sync(1 + stage" in text
     assert "mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u" in text and "mma_commit(&ctl.empty[stage]);" in text
     assert "mbar_wait(&ctl.raw_empty[slot]" in text
+    # one loader thread issues every k-step's copies
+    assert "if (warp == kLoadWarp0 && lane == 0) {" in text and "for (int f = 0; f < total; ++f) {" in text
     # empty[g] serves the k-steps f with f % stages == g: a done ring of `stages` barriers
     return dict(ring=int(_const(text, "kRawStages")), done=stages, stages=stages, groups=stages,
-                gw=int(_const(text, "kGroupWarps")), loaders=int(_const(text, "kLoadWarps")), gate="conv")
+                gw=int(_const(text, "kGroupWarps")), loaders=1, gate="conv")
 
 
 class MBar:
