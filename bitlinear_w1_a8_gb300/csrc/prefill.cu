@@ -67,14 +67,12 @@ constexpr int kConvGroups = kStages;                // group g converts the k-st
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;     // 128
 constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 16
-constexpr int kLoadWarps = 4;
-constexpr int kLoadThreads = kLoadWarps * 32;       // 128
+constexpr int kLoadWarps = 4;                       // warp 20 loads; 21-23 keep the warp layout
 constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 20
 constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 24
 constexpr int kThreads = (kMmaWarp + 1) * 32;       // 800
 constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
-static_assert((kTileM * kKStep / 16) % kLoadThreads == 0, "activation pieces split evenly over the loaders");
 static_assert(kThreads * 80 <= 65536, "80 registers a thread for one CTA per SM");
 static_assert(kStages + 1 <= 16, "named barriers 1 .. kStages");
 constexpr uint32_t kTmemCols = 512;
