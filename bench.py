@@ -30,6 +30,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -108,27 +110,173 @@ class OracleStep:
         o.forward(xq, sx, self.p_d, self.sw_d, self.nd, self.F)   # down
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(jobs, results):
+    """Process of OraclePool: runs oracle decode steps (or a prefill row slice)
+    over the row slices it was given, as the parent asks."""
+    import oracle
+    while True:
+        job = jobs.get()
+        if job is None:
+            return
+        kind, payload = job
+        t0 = time.perf_counter()
+        if kind == "decode":
+            x_a, x_b, parts, steps = payload
+            for _ in range(steps):
+                xq, sx = oracle.act_quant(x_a)
+                for p_u, sw_u, nu, D in parts["up"]:
+                    oracle.forward(xq, sx, p_u, sw_u, nu, D)   # gate
+                    oracle.forward(xq, sx, p_u, sw_u, nu, D)   # up
+                xq, sx = oracle.act_quant(x_b)
+                for p_d, sw_d, nd, F in parts["down"]:
+                    oracle.forward(xq, sx, p_d, sw_d, nd, F)
+        else:  # "prefill": a slice of output columns for a block of token rows
+            xq, sx, p, sw, n, k = payload
+            oracle.forward(xq, sx, p, sw, n, k)
+        results.put(time.perf_counter() - t0)
+
+
+class OraclePool:
+    """The oracle on every host core: one spawned process per core, each over a
+    disjoint slice of the output rows (processes are started with `spawn`, so
+    none is forked from a process that has used the GPU)."""
+
+    def __init__(self, inp, row_fraction: float = 1.0, cores: int | None = None):
+        import multiprocessing as mp
+        import oracle
+        self.cores = cores or host_cores()
+        D, F = inp["D"], inp["F"]
+        Wq_u, sw_u, _ = oracle.weight_quant(inp["W_up_shape"].numpy())
+        Wq_d, sw_d, _ = oracle.weight_quant(inp["W_down_shape"].numpy())
+        nu = max(1, int(F * row_fraction))
+        nd = max(1, int(D * row_fraction))
+        self.bytes = 2 * oracle.packed_bytes(nu, D) + oracle.packed_bytes(nd, F)
+        self.x_a, self.x_b = inp["x_a"].numpy(), inp["x_b"].numpy()
+        self.parts = []
+        for c in range(self.cores):
+            u0, u1 = nu * c // self.cores, nu * (c + 1) // self.cores
+            d0, d1 = nd * c // self.cores, nd * (c + 1) // self.cores
+            self.parts.append({
+                "up": [(oracle.pack(Wq_u[u0:u1]), sw_u, u1 - u0, D)] if u1 > u0 else [],
+                "down": [(oracle.pack(Wq_d[d0:d1]), sw_d, d1 - d0, F)] if d1 > d0 else []})
+        self.row_fraction = row_fraction
+        ctx = mp.get_context("spawn")
+        self.jobs = [ctx.Queue() for _ in range(self.cores)]
+        self.results = ctx.Queue()
+        self.procs = [ctx.Process(target=_oracle_worker, args=(self.jobs[c], self.results), daemon=True)
+                      for c in range(self.cores)]
+        for p in self.procs:
+            p.start()
+        self.run_decode(1)  # every worker has imported the oracle and touched its slice
+
+    def _gather(self, n, timeout_s: float = 900.0):
+        """n results from the workers; raises if a worker died or time ran out."""
+        import queue
+        out, t_end = [], time.monotonic() + timeout_s
+        while len(out) < n:
+            try:
+                out.append(self.results.get(timeout=1.0))
+            except queue.Empty:
+                dead = [p.exitcode for p in self.procs if not p.is_alive()]
+                if dead or time.monotonic() > t_end:
+                    self.close()
+                    raise RuntimeError(f"oracle pool: worker exit codes {dead}, "
+                                       f"{len(out)} of {n} results")
+        return out
+
+    def run_decode(self, steps: int) -> float:
+        """Wall seconds for `steps` decode steps over all cores."""
+        t0 = time.perf_counter()
+        for c in range(self.cores):
+            self.jobs[c].put(("decode", (self.x_a, self.x_b, self.parts[c], steps)))
+        self._gather(self.cores)
+        return time.perf_counter() - t0
+
+    def run_prefill_slice(self, xq, sx, Wq, sw) -> float:
+        """Wall seconds for the forward of token rows xq against every row of Wq,
+        the output columns split over the cores."""
+        import oracle
+        N, K = Wq.shape
+        jobs = []
+        for c in range(self.cores):
+            n0, n1 = N * c // self.cores, N * (c + 1) // self.cores
+            if n1 > n0:
+                jobs.append((c, (xq, sx, oracle.pack(Wq[n0:n1]), sw, n1 - n0, K)))
+        t0 = time.perf_counter()
+        for c, payload in jobs:
+            self.jobs[c].put(("prefill", payload))
+        self._gather(len(jobs))
+        return time.perf_counter() - t0
+
+    def close(self):
+        for q in self.jobs:
+            q.put(None)
+        for p in self.procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.terminate()
+
+
 def cpu_baseline(inp, seconds: float):
+    """The oracle as it stands on the host: every core (the reported value),
+    one core beside it, and a 64-token slice of the M = 2048 prefill shapes on
+    every core, extrapolated to 2048 tokens."""
+    import oracle
+    from bitlinear_w1_a8_gb300 import synth
     step = OracleStep(inp)
-    n = 0
+    n1 = 0
     t0 = time.perf_counter()
     while True:
         step.run()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or n >= 10000:
+        n1 += 1
+        el1 = time.perf_counter() - t0
+        if el1 >= seconds / 2 or n1 >= 10000:
             break
-    return {"value": round(step.bytes * n / el / 1e9, 6), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"{n} full decode steps (act_quant x2 + gate/up/down forwards over "
-                      f"{step.bytes} packed bytes each) in {el:.1f} s, single-threaded C oracle"}
+    one_core = step.bytes * n1 / el1 / 1e9
+    pool = OraclePool(inp)
+    try:
+        steps = max(3, int(seconds / 2 * n1 / el1 * pool.cores * 0.8))
+        el = pool.run_decode(steps)
+        value = step.bytes * steps / el / 1e9
+        # prefill: 64 of the 2048 token rows, both FFN shapes, all cores
+        s = synth.SEEDS["prefill"]
+        D, F = synth.DIM_3B, synth.FFN_3B
+        rows, M = 64, 2048
+        x = synth.activations(rows, F, s["x"]).numpy()
+        pre = {}
+        for name, N, K, seed in (("up_shape", F, D, s["W_up_shape"]), ("down_shape", D, F, s["W_down_shape"])):
+            Wq, sw, _ = oracle.weight_quant(synth.weight(N, K, seed).numpy())
+            xq, sx = oracle.act_quant(np.ascontiguousarray(x[:, :K]))
+            t_slice = pool.run_prefill_slice(xq, sx, Wq, sw)
+            pre[name] = {"tokens_timed": rows, "seconds": round(t_slice, 3),
+                         "tops_extrapolated": round(2.0 * rows * N * K / t_slice / 1e12, 6),
+                         "seconds_for_2048_extrapolated": round(t_slice * M / rows, 2)}
+    finally:
+        pool.close()
+    return {"value": round(value, 6), "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+            "sample": f"{steps} full decode steps (act_quant x2 + gate/up/down forwards over {step.bytes} "
+                      f"packed bytes each) in {el:.1f} s on {pool.cores} host cores, one process per core "
+                      f"over disjoint output rows",
+            "one_core": {"value": round(one_core, 6), "unit": UNIT, "cores": 1,
+                         "sample": f"{n1} full decode steps in {el1:.1f} s, single-threaded"},
+            "prefill_m2048_slice": dict(pre, note="64 of 2048 tokens on every core; the per-token work is "
+                                                  "the same for every token, so 2048 tokens take 32x as long "
+                                                  "(extrapolated, not run)")}
 
 
 def run_reference(args, rank, world):
-    """The oracle, as it stands, timed on host cores (rank 0 only).  Each step is
-    a bounded sample of the decode step: both act_quant calls and the three
-    forwards over the leading fraction of the output rows, the fraction chosen
-    so that the whole run takes about a minute whatever --steps is."""
+    """The oracle, as it stands, timed on every host core (rank 0 only).  Each
+    step is a bounded sample of the decode step: both act_quant calls and the
+    three forwards over the leading fraction of the output rows (split over the
+    cores), the fraction chosen so that the whole run takes about a minute
+    whatever --steps is."""
     if rank != 0:
         return 0
     inp = workload_inputs()
@@ -136,26 +284,28 @@ def run_reference(args, rank, world):
     t0 = time.perf_counter()
     probe.run()
     t_probe = max(time.perf_counter() - t0, 1e-6)
-    budget = 60.0 / max(1, args.steps + min(max(args.warmup, 0), 3))
-    frac = min(1.0, max(1.0 / inp["F"], budget / (t_probe * 64)))
-    step = OracleStep(inp, row_fraction=frac)
+    cores = host_cores()
     warm = min(max(args.warmup, 0), 3)
-    for _ in range(warm):
-        step.run()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step.run()
-    el = time.perf_counter() - t0
-    value = step.bytes * args.steps / el / 1e9
-    sample = (f"{args.steps} steps, each act_quant x2 + gate/up/down over the first "
-              f"{frac:.4%} of output rows ({step.bytes} packed bytes), single-threaded C oracle")
+    budget = 60.0 / max(1, args.steps + warm)
+    frac = min(1.0, max(1.0 / inp["F"], budget * cores / (t_probe * 64)))
+    pool = OraclePool(inp, row_fraction=frac, cores=cores)
+    try:
+        if warm:
+            pool.run_decode(warm)
+        el = pool.run_decode(args.steps)
+    finally:
+        pool.close()
+    value = pool.bytes * args.steps / el / 1e9
+    sample = (f"{args.steps} steps, each act_quant x2 + gate/up/down over the first {frac:.4%} of output "
+              f"rows ({pool.bytes} packed bytes), the C oracle on {cores} host cores (one process per core "
+              f"over disjoint rows)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": warm,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "sample_row_fraction": round(frac, 6)},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -225,6 +375,15 @@ def reduce_max_ms(ms: float, dist=None, device=None) -> float:
     return float(t.item())
 
 
+def device_lead(stream, us: float = 100.0):
+    """Queue a short device-side spin on `stream` ahead of a start event, so the
+    host's submission of the timed work overlaps it and the events bracket
+    device execution only (the spin itself lies before the start event)."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2000))  # ~us microseconds at ~2 GHz
+
+
 def whole_job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
     """Aggregate throughput: every rank's bytes over the slowest rank's time."""
     return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
@@ -279,6 +438,34 @@ def measured_peak_tensor():
         return 1900.0, "fallback"
 
 
+def measure_int8_peak(dev, n: int = 8192, reps: int = 10):
+    """Dense int8 tensor throughput as a library GEMM sees it on this GPU:
+    torch._int_mm (int8 x int8 -> int32, cuBLASLt) on n^3, best of `reps`
+    launches timed with CUDA events (the way the pool's bf16 peak is taken
+    with torch.matmul)."""
+    import torch
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev).t()
+        torch._int_mm(a, b)
+        torch.cuda.synchronize(dev)
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(a, b)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return {"tops": round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 2),
+                "method": f"torch._int_mm int8 x int8 -> int32 (cuBLASLt), {n}^3, best of {reps}, CUDA events"}
+    except Exception as e:  # an int8 GEMM the library does not offer on this GPU
+        return {"tops": None, "method": f"torch._int_mm unavailable: {type(e).__name__}: {e}"[:200]}
+
+
 PREFILL_SOURCES = ["bitlinear_w1_a8_gb300/csrc/prefill.cu", "bitlinear_w1_a8_gb300/csrc/tc_util.cuh",
                    "bitlinear_w1_a8_gb300/csrc/common.cuh"]
 
@@ -329,6 +516,7 @@ def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
                 torch.cuda.synchronize(dev)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
+                device_lead(stream)
                 e0.record(stream)
                 g.replay()
                 e1.record(stream)
@@ -358,12 +546,17 @@ def measure_prefill(bl, dev, stream, dist, M=2048, launches=30):
     tot_ops = sum(2.0 * v["M"] * v["N"] * v["K"] for v in out.values())
     tot_us = sum(v["us_per_launch"] for v in out.values())
     achieved = tot_ops / (tot_us * 1e-6) / 1e12
+    int8 = measure_int8_peak(dev)
     out["roofline"] = {"kernel": "prefill_kernel (tcgen05 kind::f16, exact int8 x ternary)",
                        "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                        "traffic": ncu_traffic(PREFILL_SOURCES, "prefill_m2048_bitnet3b_ncu.txt"),
                        "note": "int8-equivalent ops (2*M*N*K) per launch / launch time; no int8 "
-                               "tcgen05 MMA exists on sm_103a, so the dense fp16 peak is the roofline"}
+                               "tcgen05 MMA exists on sm_103a (ptxas rejects kind::i8), so the kernel "
+                               "runs exact kind::f16 MMAs and the dense fp16 peak is the roofline",
+                       "int8_peak": dict(int8, frac=(round(achieved / int8["tops"], 4) if int8["tops"] else None),
+                                         note="the dense int8 rate a library GEMM reaches on this GPU; "
+                                              "frac = this kernel's int8-equivalent rate over it")}
     return out
 
 
@@ -438,6 +631,7 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
             torch.cuda.synchronize(dev)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            device_lead(stream)
             e0.record(stream)
             for _ in range(reps):
                 g.replay()
@@ -506,6 +700,7 @@ def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
             torch.cuda.synchronize(dev)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            device_lead(stream)
             e0.record(stream)
             g.replay()
             e1.record(stream)
@@ -607,7 +802,12 @@ def run_ours(args, rank, world, local_rank):
                     for i in range(k % R):
                         step(i, stream)
 
-    # warm-up
+    # warm-up: every graph the timed region replays is replayed (and so
+    # uploaded) here first, then the requested warm-up steps run
+    with torch.cuda.stream(stream):
+        g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
     run_steps(max(3, args.warmup))
     torch.cuda.synchronize(dev)
 
@@ -623,6 +823,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    device_lead(stream)
     ev0.record(stream)
     run_steps(args.steps)
     ev1.record(stream)
@@ -642,6 +843,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
+    device_lead(stream)
     a0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(alt_reps):
@@ -671,6 +873,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    device_lead(stream)
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(reps):

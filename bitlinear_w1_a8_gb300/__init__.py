@@ -9,6 +9,7 @@ If the library has not been built, importing works but every call raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 __all__ = [
@@ -158,8 +159,10 @@ def bitlinear_status_string(status: int) -> str:
         return STATUS.get(status, "unknown status")
 
 
+@functools.lru_cache(maxsize=256)
 def bitlinear_packed_bytes(N: int, K: int) -> int:
-    return int(load_library().bitlinear_packed_bytes(N, K))
+    """Bytes of the packed layout of an [N, K] matrix (asked of the library)."""
+    return int(load_library().bitlinear_packed_bytes(int(N), int(K)))
 
 
 def bitlinear_quantize_weights_workspace(N: int, K: int) -> int:
@@ -171,7 +174,7 @@ def bitlinear_quantize_weights(W, packed, w_scale, workspace, stream=None):
     import torch
     _need(W, torch.float32, "W")
     N, K = W.shape
-    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
     _need(w_scale, torch.float32, "w_scale")
     _need(workspace, torch.uint8, "workspace")
     _check(load_library().bitlinear_quantize_weights(
@@ -186,7 +189,7 @@ def bitlinear_quantize_weights_noalloc(W, packed, w_scale, stream=None):
     import torch
     _need(W, torch.float32, "W")
     N, K = W.shape
-    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
     _need(w_scale, torch.float32, "w_scale")
     _check(load_library().bitlinear_quantize_weights_noalloc(
         _ptr(W), N, K, _ptr(packed), _ptr(w_scale), _stream(stream)),
@@ -217,7 +220,7 @@ def bitlinear_forward_ex(xq, x_scale, packed, w_scale, N: int, y, acc=None,
     _need(xq, torch.int8, "xq")
     M, K = xq.shape
     _need(x_scale, torch.float32, "x_scale", (M,))
-    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
     _need(w_scale, torch.float32, "w_scale")
     _need(y, torch.float32, "y", (M, N))
     if acc is not None:
@@ -227,6 +230,7 @@ def bitlinear_forward_ex(xq, x_scale, packed, w_scale, N: int, y, acc=None,
         int(algo), int(flags), _stream(stream)), "bitlinear_forward_ex")
 
 
+@functools.lru_cache(maxsize=256)
 def bitlinear_forward_workspace(M: int, K: int) -> int:
     """Bytes of device workspace bitlinear_forward_ws needs for M tokens of K."""
     return int(load_library().bitlinear_forward_workspace(int(M), int(K)))
@@ -235,23 +239,23 @@ def bitlinear_forward_workspace(M: int, K: int) -> int:
 def bitlinear_forward_ws(xq, x_scale, packed, w_scale, N: int, y, acc=None, workspace=None,
                          algo: int = ALGO_AUTO, flags: int = 0, stream=None):
     """bitlinear_forward_ex with a device workspace (a uint8 CUDA tensor of at
-    least bitlinear_forward_workspace(M, K) bytes; one is allocated on xq's
-    device when None is given)."""
+    least bitlinear_forward_workspace(M, K) bytes, or None: then no algorithm
+    that needs one is chosen, and asking for ALGO_WIDE raises)."""
     import torch
     _need(xq, torch.int8, "xq")
     M, K = xq.shape
     _need(x_scale, torch.float32, "x_scale", (M,))
-    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
     _need(w_scale, torch.float32, "w_scale")
     _need(y, torch.float32, "y", (M, N))
     if acc is not None:
         _need(acc, torch.int32, "acc", (M, N))
-    if workspace is None:
-        workspace = torch.empty(((M + 15) // 16 * 16) * K * 2, dtype=torch.uint8, device=xq.device)
-    _need(workspace, torch.uint8, "workspace")
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
     _check(load_library().bitlinear_forward_ws(
         _ptr(xq), _ptr(x_scale), M, _ptr(packed), _ptr(w_scale), N, K, _ptr(y), _ptr(acc),
-        int(algo), int(flags), _ptr(workspace), workspace.numel(), _stream(stream)), "bitlinear_forward_ws")
+        int(algo), int(flags), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)), "bitlinear_forward_ws")
 
 
 def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=None):
@@ -260,7 +264,7 @@ def bitlinear_forward(xq, x_scale, packed, w_scale, N: int, y, acc=None, stream=
     _need(xq, torch.int8, "xq")
     M, K = xq.shape
     _need(x_scale, torch.float32, "x_scale", (M,))
-    _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+    _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
     _need(w_scale, torch.float32, "w_scale")
     _need(y, torch.float32, "y", (M, N))
     if acc is not None:
@@ -299,7 +303,7 @@ def _weight_array(weights, M, K):
         packed, w_scale, y = w[0], w[1], w[2]
         acc = w[3] if len(w) > 3 else None
         N = y.shape[1]
-        _need(packed, torch.uint8, "packed", (N * ((K + 63) // 64) * 16,))  # bitlinear_packed_bytes
+        _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
         _need(w_scale, torch.float32, "w_scale")
         _need(y, torch.float32, "y", (M, N))
         if acc is not None:

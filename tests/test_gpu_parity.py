@@ -431,7 +431,11 @@ def test_lm_head_greedy_token(M):
     idx = _gpu_argmax(y_g)
     np.testing.assert_array_equal(idx, oracle.argmax(y_g))
     Wq, sw_o, _ = oracle.weight_quant(W.numpy())
+    assert sw == sw_o
     acc_o, y_o = oracle.forward(xq, sx, oracle.pack(Wq), sw_o, N, K)
+    # the head's integer accumulators, every one of the 50000 per token
+    np.testing.assert_array_equal(acc_g, acc_o)
+    assert max_rel_err(y_g, y_o) <= Y_RTOL
     for m in range(M):
         best = y_o[m].max()
         assert y_o[m, idx[m]] >= best - Y_RTOL * abs(best)
