@@ -5,36 +5,46 @@
 // page, section "Performance (BitNet-3B on A100)": 870 of 883 ms per token go
 // to the 32 layers, i.e. to streaming the 2-bit weights once per token).
 //
-// At M = 1 the kernel is bound by HBM: every packed byte is read exactly once
-// and does 4 weights of work.  Design:
+// At M = 1 every packed byte is read exactly once and does 4 weights of work;
+// calls run back to back, each waiting for the previous one's output.  Design:
 //  * grid: about one CTA per SM per launch (CTA c of a matrix owns rows
 //    [c*N/G, (c+1)*N/G); the matrices of one launch -- q, k, v or gate, up,
-//    which share one input -- split the SMs in proportion to their bytes), and
-//    each CTA uses at most half of an SM (512 threads of <= 64 registers, about
-//    100 KB of shared memory), so under programmatic dependent launch the
-//    next launch's CTAs become resident while this one runs;
-//  * first thing, before griddepcontrol.wait, a CTA bulk-copies all of its
-//    weights (one copy per k-block plane: its rows are contiguous there) into
-//    shared memory -- the packed weights never come from the previous kernel,
-//    so they stream from HBM while the previous kernel finishes, through the
-//    copy engine rather than the load/store path;
-//  * after the wait, the token group's int8 activations are staged in shared
-//    memory (or, in the fused mode, the fp32 row is staged and quantised there
-//    by every CTA), one memory round trip;
-//  * a chunk holds 64 codes c = Wq+1; with w one 32-bit word,
-//    w & (0x03030303 << 2s) holds the codes of k = 16w'+4s .. +3 scaled by
-//    4^s, so one mask and one dp4a (unsigned x signed) add 4^s * sum c*x; the
-//    four partial sums are combined with exact shifts, and subtracting the
-//    row sum of x gives sum Wq*x (the ternary add/sub) exactly;
-//  * partial sums of a row meet in shared memory (int32 atomics, exact in
-//    any order), then one thread per row rescales.
+//    which share one input -- split the SMs in proportion to their rows), and
+//    each CTA uses at most half of an SM (512 threads of <= 64 registers,
+//    <= ~110 KB of shared memory), so under programmatic dependent launch the
+//    next launch's CTAs are resident while this one runs;
+//  * first thing, before griddepcontrol.wait, warp 0 bulk-copies all of the
+//    CTA's weights (one copy per k-block plane: its rows are contiguous
+//    there), and the RMSNorm gamma when there is one, into shared memory --
+//    they never come from the previous kernel, so they stream from HBM while
+//    the previous kernel finishes;
+//  * after the wait (fused mode, M = 1) every thread loads its share of the
+//    fp32 row straight into registers -- one memory round trip -- applies
+//    the optional gating and RMSNorm there, and the row is quantised with two
+//    block barriers (the absmax, then the codes in shared memory); with int8
+//    input (M tokens) the token rows are staged with cp.async;
+//  * dots: the CTA's (k-block, row) chunks are dealt out to the 512 threads
+//    flat, in the order of the weight planes (chunk c = kb * R + r), so every
+//    thread gets the same number of chunks and a warp reads 32 consecutive
+//    16-byte chunks of one plane while its lanes share the activation slice
+//    (a shared-memory broadcast).  Per 32-bit code word w, the masks
+//    w & (0x03030303 << 2s) (s = 0..3) hold four codes scaled by 4^s, so one
+//    dp4a (unsigned x signed) per mask adds 4^s * sum c*x; the four sums are
+//    combined with exact shifts and subtracting the row sum of x gives
+//    sum Wq*x (the ternary add/sub) exactly.  On GB300 the dp4a pipe accepts
+//    about 32 per clock per SM, which bounds this phase;
+//  * each chunk's sum meets its row's others in shared memory (an int32
+//    atomic, exact in any order), then one thread per row rescales.
 #include "quant_row.cuh"
 
 namespace bitlinear {
 namespace {
 
 constexpr int kDecThreads = 512;
+constexpr int kDecWarps = kDecThreads / 32;
 constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr int kMaxWeightBytes = 96 * 1024;  // weight planes a CTA holds in shared memory
+constexpr int kMaxNJ = 8;                   // fused mode: K <= kDecThreads * 4 * kMaxNJ
 
 struct DecodeMat {
   const uint8_t* packed;
@@ -47,8 +57,8 @@ struct DecodeMat {
 };
 
 struct DecodeParams {
-  // int8 input (fused == 0): xq_in, sx_in.  fp32 input (fused == 1, M == 1):
-  // x, mul, gamma, eps; every CTA quantises the row itself and CTA 0 writes
+  // int8 input (not fused): xq_in, sx_in.  fp32 input (fused, M == 1): x,
+  // mul, gamma, eps; every CTA quantises the row itself and CTA 0 writes
   // xq_out, sx_out when they are given.
   const int8_t* xq_in;
   const float* sx_in;
@@ -58,11 +68,12 @@ struct DecodeParams {
   double eps;
   int8_t* xq_out;
   float* sx_out;
-  int fused;
   int* status;
   int M, K, KB;
-  int rows_max;  // max rows of a CTA over all matrices: sizes the shared-memory carve-up
-  uint32_t w_off;  // byte offset of the weight planes in dynamic shared memory
+  int rows_max;     // max rows of a CTA over all matrices
+  uint32_t off_xs;  // byte offsets in dynamic shared memory: int8 activations,
+  uint32_t off_red; //   int32 row sums,
+  uint32_t off_gs;  //   gamma (fused RMSNorm); the weight planes start at 0
   int nmats;
   DecodeMat mats[kMaxDecodeMats];
 };
@@ -108,9 +119,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-
-constexpr int kMaxWeightBytes = 96 * 1024;  // weight planes a CTA holds in shared memory
-
 __device__ __forceinline__ void expect_tx(unsigned long long* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
@@ -120,13 +128,164 @@ __device__ __forceinline__ void bulk_copy(void* dst_smem, const void* src, uint3
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
 }
+// 16-byte load through L2 only (the row was written by the previous kernel).
+__device__ __forceinline__ float4 ld_cg4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+// sum_k c_k x_k over one 16-byte chunk (64 codes) and its 64 activations
+__device__ __forceinline__ int chunk_dot(const uint4 wv, const int4* xp) {
+  int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  const uint32_t cw[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const int4 xv = xp[wi];
+    a0 = dp4a_us(cw[wi] & 0x03030303u, xv.x, a0);
+    a1 = dp4a_us(cw[wi] & 0x0C0C0C0Cu, xv.y, a1);
+    a2 = dp4a_us(cw[wi] & 0x30303030u, xv.z, a2);
+    a3 = dp4a_us(cw[wi] & 0xC0C0C0C0u, xv.w, a3);
+  }
+  // a_s is an exact multiple of 4^s: the shifts are exact
+  return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+}
 
-// Dynamic shared memory: xs[MT][K] int8 activations, red[MT][rows_max] int32
-// partial sums, (fused mode) the staged fp32 row, gating input and gamma, and
-// at w_off the CTA's weight planes: plane kb holds rows r0 .. r1 as R
-// consecutive 16-byte chunks.
-template <int MT, bool FUSED>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodeParams p) {
+// Fused-mode quantisation of one token row held in registers: thread t owns
+// the float4 elements e = t + 512 j (j < NJ, e < K/4) of the row, taken in a
+// CTA-dependent rotation (by whole 128-byte lines) so that the CTAs' first
+// requests spread over the L2 slices.  Writes the int8 codes to xs (shared)
+// and, when out is not NULL, to out (global); adds sum_k xq[k] to *sumx.
+// Returns sx.  Every thread of the block calls it.
+template <int NJ>
+__device__ float quantize_row_regs(const float* __restrict__ x, const float* __restrict__ mul, bool norm,
+                                   const float4* gs, double eps, int K, unsigned long long* wbar, int* status,
+                                   RowQuantScratch& sc, int8_t* xs, int8_t* out, int* sumx) {
+  const int t = threadIdx.x, lane = t & 31;
+  const int K4 = K >> 2;
+  const int rot = (int)((blockIdx.x * 296u) % (unsigned)K4) & ~7;
+  int idx[NJ];
+  bool ok[NJ];
+  float4 h[NJ];
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int e = t + j * kDecThreads;
+    ok[j] = e < K4;
+    int i = e + rot;
+    if (i >= K4) i -= K4;
+    idx[j] = ok[j] ? i : 0;
+    h[j] = ok[j] ? ld_cg4(x4 + idx[j]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (mul) {
+    // h = (r*r)*u with r = max(g, 0): the ReLU^2 gating of the FFN
+    const float4* u4 = reinterpret_cast<const float4*>(mul);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (!ok[j]) continue;
+      const float4 u = ld_cg4(u4 + idx[j]);
+      float r;
+      r = fmaxf(h[j].x, 0.0f); h[j].x = __fmul_rn(__fmul_rn(r, r), u.x);
+      r = fmaxf(h[j].y, 0.0f); h[j].y = __fmul_rn(__fmul_rn(r, r), u.y);
+      r = fmaxf(h[j].z, 0.0f); h[j].z = __fmul_rn(__fmul_rn(r, r), u.z);
+      r = fmaxf(h[j].w, 0.0f); h[j].w = __fmul_rn(__fmul_rn(r, r), u.w);
+    }
+  }
+  if (norm) {
+    // RMSNorm: inv = fp32(1 / sqrt(S/K + eps)) in fp64 from the exact sum S
+    int e = 0;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (ok[j])
+        e = max(max(e, max(fp32_exponent(__float_as_uint(h[j].x)), fp32_exponent(__float_as_uint(h[j].y)))),
+                max(fp32_exponent(__float_as_uint(h[j].z)), fp32_exponent(__float_as_uint(h[j].w))));
+    const int emax = block_max_exponent(e, sc);
+    double S = 0.0;
+    if (emax != 0) {
+      U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
+      int slow = 0;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (!ok[j]) continue;
+        sq_window_add(__float_as_uint(h[j].x), emax, A, slow);
+        sq_window_add(__float_as_uint(h[j].y), emax, A, slow);
+        sq_window_add(__float_as_uint(h[j].z), emax, A, slow);
+        sq_window_add(__float_as_uint(h[j].w), emax, A, slow);
+      }
+      if (!block_windows(A, slow, emax, sc, &S)) {
+        zero_buckets(sc);
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const float4 v = ok[j] ? h[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+          bucket_sq_add(v.x, sc);
+          bucket_sq_add(v.y, sc);
+          bucket_sq_add(v.z, sc);
+          bucket_sq_add(v.w, sc);
+        }
+        S = bucket_fold(sc);
+      }
+    }
+    // one thread takes the fp64 steps (fp64 is slow on this GPU), the block
+    // picks the result up after a barrier
+    if (t == 0) {
+      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
+      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
+    }
+    __syncthreads();
+    const float inv = sc.inv;
+    // gamma came with the weights (bounded wait; on timeout the status word
+    // says so and the outputs are not written)
+    bar_wait(wbar, status);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (!ok[j]) continue;
+      const float4 g = gs[idx[j]];
+      h[j].x = __fmul_rn(__fmul_rn(h[j].x, inv), g.x);
+      h[j].y = __fmul_rn(__fmul_rn(h[j].y, inv), g.y);
+      h[j].z = __fmul_rn(__fmul_rn(h[j].z, inv), g.z);
+      h[j].w = __fmul_rn(__fmul_rn(h[j].w, inv), g.w);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h[j].x), fabsf(h[j].y)), fmaxf(fabsf(h[j].z), fabsf(h[j].w))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
+  if (lane == 0) sc.red[t >> 5] = amax;
+  __syncthreads();
+  amax = sc.red[0];
+#pragma unroll
+  for (int w = 1; w < kDecWarps; ++w) amax = fmaxf(amax, sc.red[w]);
+  const float s = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
+  int qsum = 0;
+  int* xs32 = reinterpret_cast<int*>(xs);
+  int* xo32 = reinterpret_cast<int*>(out);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    if (!ok[j]) continue;
+    const float f[4] = {h[j].x, h[j].y, h[j].z, h[j].w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int v = __float2int_rn(__fmul_rn(f[q], s));
+      v = v < -128 ? -128 : (v > 127 ? 127 : v);
+      qsum += v;
+      word |= ((uint32_t)v & 0xffu) << (8 * q);
+    }
+    xs32[idx[j]] = (int)word;
+    if (out) xo32[idx[j]] = (int)word;
+  }
+  qsum = __reduce_add_sync(kFullMask, qsum);
+  if (lane == 0 && qsum != 0) atomicAdd(sumx, qsum);
+  return s;
+}
+
+// Dynamic shared memory: the CTA's weight planes at 0 (plane kb holds rows
+// r0 .. r1-1 as R consecutive 16-byte chunks), xs[MT][K] int8 activations at
+// off_xs, red[MT][R] int32 row sums at off_red, (fused RMSNorm) gamma at off_gs.
+template <int MT, bool FUSED, int NJ>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ int sumx[MT];
   __shared__ float den[MT];
@@ -146,69 +305,58 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
   const int r0 = (int)(((int64_t)cl * mat.N) / mat.G);
   const int r1 = (int)(((int64_t)(cl + 1) * mat.N) / mat.G);
   const int R = r1 - r0;
-  const int KB = p.KB;
-  const size_t red_off = (size_t)MT * p.K;
-  const size_t hs_off = (red_off + (size_t)MT * p.rows_max * 4 + 15) & ~(size_t)15;
-  int8_t* xs = reinterpret_cast<int8_t*>(dsmem);
-  int* red = reinterpret_cast<int*>(dsmem + red_off);
-  float4* hs = reinterpret_cast<float4*>(dsmem + hs_off);      // fused: staged row
-  float4* us = hs + (p.K >> 2);                                 // fused: staged gating input
-  float4* gs = us + (p.mul ? (p.K >> 2) : 0);                   // fused: staged gamma
-  uint4* wsm = reinterpret_cast<uint4*>(dsmem + p.w_off);
+  const int KB = p.KB, K = p.K;
+  const uint4* wsm = reinterpret_cast<const uint4*>(dsmem);
+  int8_t* xs = reinterpret_cast<int8_t*>(dsmem + p.off_xs);
+  int* red = reinterpret_cast<int*>(dsmem + p.off_red);
+  float4* gs = reinterpret_cast<float4*>(dsmem + p.off_gs);
+  const bool norm = FUSED && p.gamma != nullptr;
 
-  // The weights: one bulk copy per k-block plane into shared memory, issued
-  // before the dependency wait (warp 0; the byte count is registered first).
+  // The weights (and gamma): bulk copies into shared memory, issued before the
+  // dependency wait by warp 0 (the byte count is registered first).
   if (t < 32) {
     if (t == 0) {
       bar_init(&wbar, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      expect_tx(&wbar, (uint32_t)R * (uint32_t)KB * 16u);
+      expect_tx(&wbar, (uint32_t)R * (uint32_t)KB * 16u + (norm ? (uint32_t)K * 4u : 0u));
     }
     __syncwarp();
     const uint4* src = reinterpret_cast<const uint4*>(mat.packed) + r0;
     for (int kb = lane; kb < KB; kb += 32)
-      bulk_copy(wsm + (size_t)kb * R, src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
+      bulk_copy((void*)(wsm + (size_t)kb * R), src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
+    if (norm && lane == 0) bulk_copy(gs, p.gamma, (uint32_t)K * 4u, &wbar);
   }
   // Let the next kernel on the stream start (and request its own weights) on
   // the SM resources this grid leaves free; it still waits for our results.
   pdl_release_dependents();
   if (t < MT) sumx[t] = 0;
-  for (int i = t; i < MT * p.rows_max; i += kDecThreads) red[i] = 0;
+  for (int i = t; i < MT * R; i += kDecThreads) red[i] = 0;
 
   pdl_wait_primary();
 
   if constexpr (FUSED) {
-    // One token row (MT == 1): quantised here exactly as the act_quant kernel
-    // does; the quantiser also leaves sum_k xq[k] in sumx[0].
-    stage_row(p.x + (int64_t)m0 * p.K, p.mul ? p.mul + (int64_t)m0 * p.K : nullptr, p.gamma, p.K, hs, us, gs);
-    const float s = quantize_row_staged(p.mul != nullptr, p.gamma != nullptr, p.eps, p.K, hs, us, gs, qsc, xs,
-                                        &sumx[0]);
+    const float s = quantize_row_regs<NJ>(p.x + (int64_t)m0 * K, p.mul ? p.mul + (int64_t)m0 * K : nullptr, norm,
+                                          gs, p.eps, K, &wbar, p.status, qsc, xs,
+                                          c == 0 ? p.xq_out + (p.xq_out ? (int64_t)m0 * K : 0) : nullptr,
+                                          &sumx[0]);
     if (t == 0) {
       den[0] = __fmul_rn(s, *mat.sw);
       if (c == 0 && p.sx_out) p.sx_out[m0] = s;
     }
+    __syncthreads();
   } else {
     // int8 rows -> shared memory in one round trip (cp.async bypasses the registers)
-    const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * p.K);
+    const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K);
     int4* dst = reinterpret_cast<int4*>(xs);
-    for (int i = t; i < mcount * (p.K >> 4); i += kDecThreads) cp_async16_row(dst + i, src + i);
+    for (int i = t; i < mcount * (K >> 4); i += kDecThreads) cp_async16_row(dst + i, src + i);
     if (t < MT) den[t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], *mat.sw) : 1.0f;
     asm volatile("cp.async.wait_all;" ::: "memory");
-  }
-  __syncthreads();
-  if (FUSED && c == 0 && p.xq_out) {
-    const int4* src4 = reinterpret_cast<const int4*>(xs);
-    int4* dst4 = reinterpret_cast<int4*>(p.xq_out + (int64_t)m0 * p.K);
-    for (int i = t; i < (p.K >> 4); i += kDecThreads) dst4[i] = src4[i];
-  }
-
-  // Row sums of the activations (the bias of the biased codes c = Wq + 1):
-  // every warp sums a slice of each row, the slices meet in shared memory
-  // (exact in any order); they are read after the barrier that ends the dots.
-  if constexpr (!FUSED) {
-    const int K16 = p.K >> 4;
+    __syncthreads();
+    // Row sums of the activations (the bias of the biased codes c = Wq + 1);
+    // read after the barrier that ends the dots.
+    const int K16 = K >> 4;
     for (int m = 0; m < mcount; ++m) {
-      const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.K);
+      const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * K);
       int s = 0;
       for (int i = t; i < K16; i += kDecThreads) {
         const int4 v = row[i];
@@ -225,48 +373,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
   // The weights have landed (bounded wait; on timeout the status word says so
   // and the outputs are not written).
   const bool have_w = bar_wait(&wbar, p.status);
-
-  // Thread t: row r = t % R, planes kb = j, j + J, ... (j = t / R, J = 512 / R).
-  const int J = kDecThreads / R;
-  const int r = t % R, j = t / R;
-  if (have_w && j < J) {
-    int a0[MT], a1[MT], a2[MT], a3[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
+  if (have_w) {
+    // chunk cc = kb * R + r, dealt out flat: thread t takes t, t + 512, ...
+    const int4* xs4 = reinterpret_cast<const int4*>(xs);
+    const int K16 = K >> 4;
+    const int C = R * KB;
+    const int dq = kDecThreads / R, dr = kDecThreads - dq * R;
+    int kb = t / R, r = t - kb * R;
 #pragma unroll 2
-    for (int kb = j; kb < KB; kb += J) {
-      const uint4 wv = wsm[(size_t)kb * R + r];
-      const uint32_t cw[4] = {wv.x, wv.y, wv.z, wv.w};
+    for (int cc = t; cc < C; cc += kDecThreads) {
+      const uint4 wv = wsm[cc];
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        const uint32_t q0 = cw[wi] & 0x03030303u, q1 = cw[wi] & 0x0C0C0C0Cu;
-        const uint32_t q2 = cw[wi] & 0x30303030u, q3 = cw[wi] & 0xC0C0C0C0u;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < mcount) {
-            const int4 xv = reinterpret_cast<const int4*>(xs + (size_t)m * p.K)[kb * 4 + wi];
-            a0[m] = dp4a_us(q0, xv.x, a0[m]);
-            a1[m] = dp4a_us(q1, xv.y, a1[m]);
-            a2[m] = dp4a_us(q2, xv.z, a2[m]);
-            a3[m] = dp4a_us(q3, xv.w, a3[m]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < mcount) {
-        // a_s is an exact multiple of 4^s: the shifts are exact
-        const int total = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6);
-        atomicAdd(&red[m * p.rows_max + r], total);
+      for (int m = 0; m < MT; ++m)
+        if (m < mcount) atomicAdd(&red[m * R + r], chunk_dot(wv, xs4 + m * K16 + kb * 4));
+      kb += dq;
+      r += dr;
+      if (r >= R) {
+        r -= R;
+        ++kb;
       }
     }
   }
   __syncthreads();
-  if (have_w && t < R) {
-    const int n = r0 + t;
-    for (int m = 0; m < mcount; ++m) {
-      const int total = red[m * p.rows_max + t] - sumx[m];
+  if (have_w) {
+    for (int i = t; i < mcount * R; i += kDecThreads) {
+      const int m = i / R, rr = i - m * R;
+      const int n = r0 + rr;
+      const int total = red[i] - sumx[m];
       mat.y[(int64_t)(m0 + m) * mat.N + n] = __fdiv_rn(__int2float_rn(total), den[m]);
       if (mat.acc) mat.acc[(int64_t)(m0 + m) * mat.N + n] = total;
     }
@@ -285,28 +418,29 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest(int* status, unsigne
   if (threadIdx.x == 0) bar_wait(&bar, status, limit_ns);
 }
 
-// Activations, partial sums and staging first; the weight planes after them.
-size_t decode_front_bytes(const DecodeParams& p, int mt) {
-  size_t smem = (size_t)mt * p.K + (size_t)mt * p.rows_max * sizeof(int);
-  if (p.fused) {
-    const int rows = 1 + (p.mul ? 1 : 0) + (p.gamma ? 1 : 0);  // staged x, mul, gamma
-    smem = ((smem + 15) & ~(size_t)15) + (size_t)rows * p.K * sizeof(float);
-  }
-  return (smem + 127) & ~(size_t)127;
+// Bytes of dynamic shared memory besides the weight planes.
+size_t decode_front_bytes(int64_t K, int mt, int rows_max, bool norm) {
+  size_t b = (size_t)mt * K;                               // xs
+  b = ((b + 15) & ~(size_t)15) + (size_t)mt * rows_max * 4;  // red
+  b = (b + 15) & ~(size_t)15;
+  if (norm) b += (size_t)K * 4;                            // gamma
+  return (b + 127) & ~(size_t)127;
 }
 
-template <int MT, bool FUSED>
-cudaError_t launch_mt(const DecodeParams& p, int grid_x, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  DecodeParams q = p;
-  q.w_off = (uint32_t)decode_front_bytes(p, MT);
-  const size_t smem = (size_t)q.w_off + (size_t)p.rows_max * p.KB * 16;
+template <int MT, bool FUSED, int NJ>
+cudaError_t launch_mt(DecodeParams p, int grid_x, bool norm, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  const size_t wbytes = ((size_t)p.rows_max * p.KB * 16 + 127) & ~(size_t)127;
+  p.off_xs = (uint32_t)wbytes;
+  p.off_red = (uint32_t)(((wbytes + (size_t)MT * p.K) + 15) & ~(size_t)15);
+  p.off_gs = (uint32_t)((p.off_red + (size_t)MT * p.rows_max * 4 + 15) & ~(size_t)15);
+  const size_t smem = wbytes + decode_front_bytes(p.K, MT, p.rows_max, norm);
   const size_t limit = dev.smem_optin - sizeof(RowQuantScratch) - 1024;
   if (smem > limit) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     static thread_local int configured_device = -1;
     if (configured_device != dev.device) {
       cudaError_t err =
-          cudaFuncSetAttribute(decode_kernel<MT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+          cudaFuncSetAttribute(decode_kernel<MT, FUSED, NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
       if (err != cudaSuccess) return err;
       configured_device = dev.device;
     }
@@ -321,25 +455,25 @@ cudaError_t launch_mt(const DecodeParams& p, int grid_x, bool pdl, const DeviceI
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED>, q);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NJ>, p);
 }
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
-// their bytes, with at most kMaxWeightBytes of weights and at most 512 rows a
+// their rows, with at most kMaxWeightBytes of weights and at most 512 rows a
 // CTA (more CTAs, in further waves, where a matrix needs it).  Returns the
 // total CTA count.
-int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, const DeviceInfo& dev) {
+int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm,
+                const DeviceInfo& dev) {
   p.K = (int)K;
   p.KB = (int)(K / 64);
   p.nmats = nmats;
   int64_t all_rows = 0;
   for (int i = 0; i < nmats; ++i) all_rows += mats[i].N;
   const int64_t row_bytes = (int64_t)p.KB * 16;
-  // Shared memory left for weights next to the activations, partial sums
-  // (sized for the 512-row maximum here) and staging.
-  p.rows_max = kDecThreads;
+  // Shared memory left for weights next to the activations, row sums (sized
+  // for the 512-row maximum here) and gamma.
   const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 -
-                       (int64_t)decode_front_bytes(p, mt);
+                       (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);
   int64_t rows_cap = (room < kMaxWeightBytes ? room : kMaxWeightBytes) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
   if (rows_cap > kDecThreads) rows_cap = kDecThreads;
@@ -373,24 +507,24 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   DecodeParams p = {};
   p.xq_in = xq;
   p.sx_in = sx;
-  p.fused = 0;
   p.status = dev.status;
   p.M = (int)M;
   // Token group: up to 8 tokens whose activations (MT * K bytes) fit in 64 KB.
   int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   while (mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
-  const int grid = plan_decode(p, mats, nmats, K, mt, dev);
+  const int grid = plan_decode(p, mats, nmats, K, mt, false, dev);
   switch (mt) {
-    case 1: return launch_mt<1, false>(p, grid, pdl, dev, stream);
-    case 2: return launch_mt<2, false>(p, grid, pdl, dev, stream);
-    case 4: return launch_mt<4, false>(p, grid, pdl, dev, stream);
-    default: return launch_mt<8, false>(p, grid, pdl, dev, stream);
+    case 1: return launch_mt<1, false, 1>(p, grid, false, pdl, dev, stream);
+    case 2: return launch_mt<2, false, 1>(p, grid, false, pdl, dev, stream);
+    case 4: return launch_mt<4, false, 1>(p, grid, false, pdl, dev, stream);
+    default: return launch_mt<8, false, 1>(p, grid, false, pdl, dev, stream);
   }
 }
 
 cudaError_t launch_decode_fused(const float* x, const float* mul, const float* gamma, double eps, int64_t K,
                                 const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out, bool pdl,
                                 const DeviceInfo& dev, cudaStream_t stream) {
+  if (K > (int64_t)kDecThreads * 4 * kMaxNJ) return cudaErrorInvalidValue;
   DecodeParams p = {};
   p.x = x;
   p.mul = mul;
@@ -398,11 +532,21 @@ cudaError_t launch_decode_fused(const float* x, const float* mul, const float* g
   p.eps = eps;
   p.xq_out = xq_out;
   p.sx_out = sx_out;
-  p.fused = 1;
   p.status = dev.status;
   p.M = 1;
-  const int grid = plan_decode(p, mats, nmats, K, 1, dev);
-  return launch_mt<1, true>(p, grid, pdl, dev, stream);
+  const bool norm = gamma != nullptr;
+  const int grid = plan_decode(p, mats, nmats, K, 1, norm, dev);
+  // float4 elements of the row a thread owns (the kernel keeps them in registers)
+  const int nj = (int)((K / 4 + kDecThreads - 1) / kDecThreads);
+  switch (nj) {
+    case 1: return launch_mt<1, true, 1>(p, grid, norm, pdl, dev, stream);
+    case 2: return launch_mt<1, true, 2>(p, grid, norm, pdl, dev, stream);
+    case 3: return launch_mt<1, true, 3>(p, grid, norm, pdl, dev, stream);
+    case 4: return launch_mt<1, true, 4>(p, grid, norm, pdl, dev, stream);
+    case 5: return launch_mt<1, true, 5>(p, grid, norm, pdl, dev, stream);
+    case 6: return launch_mt<1, true, 6>(p, grid, norm, pdl, dev, stream);
+    default: return launch_mt<1, true, kMaxNJ>(p, grid, norm, pdl, dev, stream);
+  }
 }
 
 cudaError_t launch_wait_selftest(int64_t limit_ns, const DeviceInfo& dev, cudaStream_t stream) {

@@ -21,124 +21,197 @@ namespace bitlinear {
 struct RowQuantScratch {
   unsigned long long buckets[kBuckets];
   unsigned long long digits[kSumDigits];
-  unsigned long long wlo[32], whi[32];  // per-warp 128-bit partial sums
+  unsigned long long win[3][2][32];  // per-warp window sums (low, high 64 bits)
   float red[32];
   int ired[32];
   float inv;
 };
 
-// Exact sum of squares of the K values in hs (shared memory), rounded once to
-// the nearest double (ties to even).  Every thread of the block calls it.
-// v^2 = m^2 * 2^(2e - 300) (m the 24-bit significand, e the biased exponent,
-// subnormals e = 1).  Fast path: with E the largest exponent of the row,
-// every square of exponent e >= E - 32 is added as the integer m^2 << 2(e - E
-// + 32) < 2^112 into a 128-bit fixed-point sum (at most 2^15 values: < 2^127),
-// which is rounded to double directly.  If any nonzero value lies below that
-// window (|v| < max|v| / 2^32), the whole sum is taken again with one integer
-// bucket per exponent (warp_bucket_add / warp_fold_buckets, exact for every
-// input).  Both give the exact sum rounded once.
-static __device__ double block_sq_sum_exact(const float4* hs, int K4, RowQuantScratch& sc) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (int)(blockDim.x >> 5);
-  int emax = 0;
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-    const float4 h = hs[i];
-    const uint32_t u[4] = {__float_as_uint(h.x), __float_as_uint(h.y), __float_as_uint(h.z), __float_as_uint(h.w)};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t a = u[c] & 0x7fffffffu;
-      const int e = a ? max((int)(a >> 23), 1) : 0;
-      emax = max(emax, e);
-    }
-  }
-  emax = __reduce_max_sync(kFullMask, emax);
-  if (lane == 0) sc.ired[warp] = emax;
+// ---------------------------------------------------------------------------
+// Exact sum of squares of a row, rounded once to the nearest double (ties to
+// even).  v^2 = m^2 * 2^(2e - 300) with m the 24-bit significand and e the
+// biased exponent (subnormals: e = 1, no hidden bit).  With E the largest
+// exponent of the row and d = E - e, the square goes into window w = d / 32
+// (w = 0, 1, 2) as the integer m^2 << 2 (31 - d % 32) (< 2^110; at most 2^15
+// terms: < 2^125), so that
+//     sum = (A0 * 2^128 + A1 * 2^64 + A2) * 2^(2E - 490)
+// exactly, which is rounded once.  A nonzero value more than 96 binades below
+// the row maximum (|v| < max|v| / 2^96) sends the row to the per-exponent
+// integer buckets instead (exact for every input, slower).
+// ---------------------------------------------------------------------------
+struct U128 {
+  uint64_t lo, hi;
+};
+__device__ __forceinline__ void add128(U128& a, uint64_t lo, uint64_t hi) {
+  a.lo += lo;
+  a.hi += hi + (a.lo < lo ? 1u : 0u);
+}
+__device__ __forceinline__ void shfl_add128(U128& a, int o) {
+  const uint64_t lo = __shfl_xor_sync(kFullMask, a.lo, o), hi = __shfl_xor_sync(kFullMask, a.hi, o);
+  add128(a, lo, hi);
+}
+__device__ __forceinline__ int fp32_exponent(uint32_t bits) {
+  const uint32_t a = bits & 0x7fffffffu;
+  return a ? max((int)(a >> 23), 1) : 0;
+}
+// Adds the square of the float with these bits to the windows of a row whose
+// largest exponent is emax; flags `slow` for a value below the three windows.
+__device__ __forceinline__ void sq_window_add(uint32_t bits, int emax, U128 (&A)[3], int& slow) {
+  const uint32_t a = bits & 0x7fffffffu;
+  if (!a) return;
+  const int e = max((int)(a >> 23), 1);
+  const uint64_t m = (a & 0x7fffffu) | ((a >> 23) ? 0x800000u : 0u);
+  const int d = emax - e;
+  const unsigned __int128 term = ((unsigned __int128)(m * m)) << (2 * (31 - (d & 31)));
+  const uint64_t tlo = (uint64_t)term, thi = (uint64_t)(term >> 64);
+  if (d < 32) add128(A[0], tlo, thi);
+  else if (d < 64) add128(A[1], tlo, thi);
+  else if (d < 96) add128(A[2], tlo, thi);
+  else slow = 1;
+}
+// Block-wide maximum of the exponents (every thread gets it).
+__device__ __forceinline__ int block_max_exponent(int e, RowQuantScratch& sc) {
+  e = __reduce_max_sync(kFullMask, e);
+  if ((threadIdx.x & 31) == 0) sc.ired[threadIdx.x >> 5] = e;
   __syncthreads();
-  emax = 0;
-  for (int w = 0; w < nwarps; ++w) emax = max(emax, sc.ired[w]);
-  if (emax == 0) return 0.0;  // every value is zero (the same on every thread)
-  const int eb = max(emax - 32, 1);
-  unsigned __int128 acc = 0;
-  int slow = 0;
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-    const float4 h = hs[i];
-    const uint32_t u[4] = {__float_as_uint(h.x), __float_as_uint(h.y), __float_as_uint(h.z), __float_as_uint(h.w)};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t a = u[c] & 0x7fffffffu;
-      if (!a) continue;
-      const int e = max((int)(a >> 23), 1);
-      const uint64_t m = (a & 0x7fffffu) | ((a >> 23) ? 0x800000u : 0u);
-      if (e < eb) slow = 1;
-      else acc += ((unsigned __int128)(m * m)) << (2 * (e - eb));
-    }
-  }
-  uint64_t lo = (uint64_t)acc, hi = (uint64_t)(acc >> 64);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t olo = __shfl_xor_sync(kFullMask, lo, o), ohi = __shfl_xor_sync(kFullMask, hi, o);
-    lo += olo;
-    hi += ohi + (lo < olo ? 1u : 0u);
-  }
-  if (lane == 0) {
-    sc.wlo[warp] = lo;
-    sc.whi[warp] = hi;
-  }
-  slow = __syncthreads_or(slow);
-  if (slow) {
-    // exact for every input: one integer bucket per exponent
-    for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
-    __syncthreads();
-    for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
-      const int i = base + lane;
-      const float4 h = i < K4 ? hs[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float f[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        int b;
-        uint32_t m;
-        fp32_bucket(f[c], &b, &m);
-        warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
-      }
-    }
-    __syncthreads();
-    double S = 0.0;
-    if (warp == 0) S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
-    if (threadIdx.x == 0) sc.digits[0] = (unsigned long long)__double_as_longlong(S);
-    __syncthreads();
-    const double r = __longlong_as_double((long long)sc.digits[0]);
-    __syncthreads();
-    return r;
-  }
-  // every thread folds the per-warp sums (the same result everywhere)
-  lo = 0;
-  hi = 0;
-  for (int w = 0; w < nwarps; ++w) {
-    const uint64_t a = sc.wlo[w];
-    lo += a;
-    hi += sc.whi[w] + (lo < a ? 1u : 0u);
-  }
-  __syncthreads();  // sc.wlo / whi / ired may be reused after this
-  // value = (hi:lo) * 2^(2 eb - 300), rounded to 53 bits, ties to even
-  const int P = hi ? 127 - __clzll((long long)hi) : 63 - __clzll((long long)lo);  // top bit (lo != 0 here)
-  const unsigned __int128 W = ((unsigned __int128)hi << 64) | lo;
-  uint64_t mant;
-  int E = P + 2 * eb - 300;
-  if (P <= 52) {
-    mant = (uint64_t)(W << (52 - P));
+  int m = 0;
+  const int nw = (int)(blockDim.x >> 5);
+  for (int w = 0; w < nw; ++w) m = max(m, sc.ired[w]);
+  return m;
+}
+// Rounds (A0 * 2^128 + A1 * 2^64 + A2) * 2^(2 emax - 490) to the nearest double.
+__device__ inline double windows_to_double(const U128 (&A)[3], int emax) {
+  const uint64_t t0 = A[2].lo;
+  uint64_t t1 = A[2].hi + A[1].lo;
+  const uint64_t c1 = t1 < A[1].lo ? 1u : 0u;
+  uint64_t t2 = A[1].hi + A[0].lo;
+  uint64_t c2 = t2 < A[0].lo ? 1u : 0u;
+  t2 += c1;
+  c2 += t2 < c1 ? 1u : 0u;
+  const uint64_t t3 = A[0].hi + c2;
+  int P;          // index of the top set bit of the 256-bit integer
+  uint64_t win;   // the 64 bits from the top bit down
+  bool sticky;    // any set bit below the window
+  if (t3 | t2 | t1) {
+    uint64_t hw, lw;
+    bool rest;
+    int basebit;
+    if (t3) { hw = t3; lw = t2; rest = (t1 | t0) != 0; basebit = 192; }
+    else if (t2) { hw = t2; lw = t1; rest = t0 != 0; basebit = 128; }
+    else { hw = t1; lw = t0; rest = false; basebit = 64; }
+    const int lz = __clzll((long long)hw);
+    P = basebit + 63 - lz;
+    win = lz ? (hw << lz) | (lw >> (64 - lz)) : hw;
+    sticky = rest || (lz ? (lw << lz) != 0 : lw != 0);
   } else {
-    const int sh = P - 52;
-    mant = (uint64_t)(W >> sh);
-    const unsigned __int128 rem = W & ((((unsigned __int128)1) << sh) - 1);
-    const unsigned __int128 half = ((unsigned __int128)1) << (sh - 1);
-    if (rem > half || (rem == half && (mant & 1ull))) {
-      mant += 1ull;
-      if (mant == (1ull << 53)) {
-        mant >>= 1;
-        E += 1;
-      }
+    if (!t0) return 0.0;
+    const int lz = __clzll((long long)t0);
+    P = 63 - lz;
+    win = t0 << lz;
+    sticky = false;
+  }
+  uint64_t mant = win >> 11;                 // 53 bits
+  const bool round_bit = (win >> 10) & 1u;
+  sticky = sticky || (win & 0x3ffull) != 0;
+  int E = P + 2 * emax - 490;
+  if (round_bit && (sticky || (mant & 1u))) {
+    mant += 1u;
+    if (mant == (1ull << 53)) {
+      mant >>= 1;
+      E += 1;
     }
   }
   return __longlong_as_double((long long)(((uint64_t)(E + 1023) << 52) | (mant & ((1ull << 52) - 1ull))));
+}
+// Block reduction of the per-thread windows.  Returns true (and the rounded
+// sum in *S, the same on every thread) unless some thread flagged `slow`.
+__device__ inline bool block_windows(U128 (&A)[3], int slow, int emax, RowQuantScratch& sc, double* S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    shfl_add128(A[0], o);
+    shfl_add128(A[1], o);
+    shfl_add128(A[2], o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      sc.win[k][0][warp] = A[k].lo;
+      sc.win[k][1][warp] = A[k].hi;
+    }
+  }
+  if (__syncthreads_or(slow)) return false;
+  // every warp folds the per-warp sums the same way
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    A[k].lo = lane < nw ? sc.win[k][0][lane] : 0ull;
+    A[k].hi = lane < nw ? sc.win[k][1][lane] : 0ull;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    shfl_add128(A[0], o);
+    shfl_add128(A[1], o);
+    shfl_add128(A[2], o);
+  }
+  *S = windows_to_double(A, emax);
+  return true;
+}
+// The bucket path: after zero_buckets and a barrier, every lane of every warp
+// calls bucket_sq_add the same number of times (value 0 for lanes without
+// data), then bucket_fold (it synchronises the block) returns the sum.
+__device__ __forceinline__ void zero_buckets(RowQuantScratch& sc) {
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) sc.buckets[i] = 0ull;
+}
+__device__ __forceinline__ void bucket_sq_add(float v, RowQuantScratch& sc) {
+  int b;
+  uint32_t m;
+  fp32_bucket(v, &b, &m);
+  warp_bucket_add(sc.buckets, b, (unsigned long long)m * (unsigned long long)m);
+}
+__device__ inline double bucket_fold(RowQuantScratch& sc) {
+  __syncthreads();
+  double S = 0.0;
+  if ((threadIdx.x >> 5) == 0) S = warp_fold_buckets(sc.buckets, 2, -298, sc.digits);
+  if (threadIdx.x == 0) sc.digits[0] = (unsigned long long)__double_as_longlong(S);
+  __syncthreads();
+  const double r = __longlong_as_double((long long)sc.digits[0]);
+  __syncthreads();
+  return r;
+}
+
+// Exact sum of squares of the K values in hs (shared memory); every thread of
+// the block calls it and gets the result.
+static __device__ double block_sq_sum_exact(const float4* hs, int K4, RowQuantScratch& sc) {
+  int e = 0;
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    const float4 h = hs[i];
+    e = max(max(fp32_exponent(__float_as_uint(h.x)), fp32_exponent(__float_as_uint(h.y))),
+            max(max(e, fp32_exponent(__float_as_uint(h.z))), fp32_exponent(__float_as_uint(h.w))));
+  }
+  const int emax = block_max_exponent(e, sc);
+  if (emax == 0) return 0.0;
+  U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
+  int slow = 0;
+  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+    const float4 h = hs[i];
+    sq_window_add(__float_as_uint(h.x), emax, A, slow);
+    sq_window_add(__float_as_uint(h.y), emax, A, slow);
+    sq_window_add(__float_as_uint(h.z), emax, A, slow);
+    sq_window_add(__float_as_uint(h.w), emax, A, slow);
+  }
+  double S;
+  if (block_windows(A, slow, emax, sc, &S)) return S;
+  zero_buckets(sc);
+  __syncthreads();
+  for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
+    const int i = base + (threadIdx.x & 31);
+    const float4 h = i < K4 ? hs[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    bucket_sq_add(h.x, sc);
+    bucket_sq_add(h.y, sc);
+    bucket_sq_add(h.z, sc);
+    bucket_sq_add(h.w, sc);
+  }
+  return bucket_fold(sc);
 }
 
 // h = x, or h = (r*r)*u with r = max(x, 0) when the gating input u is given.
@@ -237,95 +310,6 @@ __device__ __forceinline__ void cp_async16_row(void* dst_smem, const void* src) 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
                "l"(src)
                : "memory");
-}
-
-// quantize_row in two parts for the fused decode kernel: the row, the gating
-// input and gamma are first staged in shared memory with cp.async -- every
-// thread issues all of its copies before waiting, so the row costs one memory
-// round trip, and the kernel can queue its weight loads behind them -- and the
-// arithmetic then runs from shared memory, element by element the same
-// operations as quantize_row.  hs, us, gs: K floats of shared memory each (us
-// only with mul, gs only with gamma).  *sumx (shared, zero on entry) receives
-// sum_k xq[k].  Returns sx.
-// Part 1: issue this thread's copies of the row (and mul, gamma) into shared
-// memory.  Part 2 (quantize_row_staged) waits for them.
-static __device__ __forceinline__ void stage_row(const float* __restrict__ x, const float* __restrict__ mul,
-                                                 const float* __restrict__ gamma, int K, float4* hs, float4* us,
-                                                 float4* gs) {
-  const int K4 = K >> 2;
-  const float4* xr = reinterpret_cast<const float4*>(x);
-  const float4* ur = reinterpret_cast<const float4*>(mul);
-  const float4* gr = reinterpret_cast<const float4*>(gamma);
-  // Every CTA of a decode launch stages the same row: each starts at its own
-  // 128-byte line (rotated by CTA), so the CTAs' first requests spread over
-  // the L2 slices instead of all hitting the row's first lines at once.
-  const int rot = (int)((blockIdx.x * 296u) % (unsigned)K4) & ~7;
-  for (int j = threadIdx.x; j < K4; j += blockDim.x) {
-    int i = j + rot;
-    if (i >= K4) i -= K4;
-    cp_async16_row(hs + i, xr + i);
-    if (ur) cp_async16_row(us + i, ur + i);
-    if (gr) cp_async16_row(gs + i, gr + i);
-  }
-}
-static __device__ __forceinline__ float quantize_row_staged(bool gated, bool norm, double eps, int K, float4* hs,
-                                                  const float4* us, const float4* gs, RowQuantScratch& sc,
-                                                  int8_t* out, int* sumx) {
-  const int K4 = K >> 2;
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
-  const float4* hsc = hs;
-  const float4* usc = gated ? us : nullptr;
-  float amax = 0.0f;
-  if (norm) {
-    if (usc) {
-      for (int i = threadIdx.x; i < K4; i += blockDim.x) hs[i] = gated4(hsc, usc, i);
-      __syncthreads();
-    }
-    const double S = block_sq_sum_exact(hs, K4, sc);
-    if (threadIdx.x == 0) {
-      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-    }
-    __syncthreads();
-    const float inv = sc.inv;
-    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-      float4 h = hs[i];
-      const float4 gm = gs[i];
-      h.x = __fmul_rn(__fmul_rn(h.x, inv), gm.x);
-      h.y = __fmul_rn(__fmul_rn(h.y, inv), gm.y);
-      h.z = __fmul_rn(__fmul_rn(h.z, inv), gm.z);
-      h.w = __fmul_rn(__fmul_rn(h.w, inv), gm.w);
-      hs[i] = h;
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
-    }
-  } else {
-    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-      const float4 h = gated4(hsc, usc, i);
-      if (usc) hs[i] = h;
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w))));
-    }
-  }
-  amax = block_max(amax, sc.red);
-  const float s = __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
-  int* o = reinterpret_cast<int*>(out);
-  int qsum = 0;
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-    const float4 h = hs[i];
-    const float f[4] = {h.x, h.y, h.z, h.w};
-    uint32_t word = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      int q = __float2int_rn(__fmul_rn(f[c], s));
-      q = q < -128 ? -128 : (q > 127 ? 127 : q);
-      qsum += q;
-      word |= ((uint32_t)q & 0xffu) << (8 * c);
-    }
-    o[i] = (int)word;
-  }
-  qsum = __reduce_add_sync(kFullMask, qsum);
-  if ((threadIdx.x & 31) == 0 && qsum != 0) atomicAdd(sumx, qsum);
-  return s;
 }
 
 }  // namespace bitlinear

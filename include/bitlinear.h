@@ -87,6 +87,12 @@ size_t bitlinear_quantize_weights_workspace(int64_t N, int64_t K);
 
 /*
  * weight_quant + pack (absmean ternary quantiser; one fp32 scale per matrix).
+ * The weight_quant of the BitNet paper that the Candle PR ("Add Support for
+ * BitNet Architecture Inference", the answer listing the changes made) names
+ * for every BitLinear; the 2-bit codes give the 0.25 byte per weight of the
+ * per-layer weight table ("Transformer Block" page, section "Memory Layout")
+ * and of the model footprint ("Hesper.Models.BitNet" page, section "Memory
+ * Footprint (BitNet-3B with TQ2_0)").
  *   W          device, fp32 [N, K] row-major, read only.
  *   N, K       N > 0, K > 0, K % 64 == 0, N*K < 2^40.
  *   packed     device, bitlinear_packed_bytes(N, K) bytes, written.
@@ -104,6 +110,13 @@ bitlinear_status bitlinear_quantize_weights(const float* W, int64_t N, int64_t K
 
 /*
  * activation_quant with optional fused prologues, one kernel, one CTA per row.
+ * The activation_quant of the BitNet paper named in the Candle PR's list of
+ * changes (per-token absmax to int8), after the RMSNorm that sits before
+ * every BitLinear there.
+ * rms_eps is a double: the norm's mean square S/K + eps is formed in fp64
+ * from the exact sum of squares, and a double keeps the caller's epsilon
+ * exactly as given (1e-6 is not a float value; a float parameter would add
+ * its rounding to every call).
  *   x           device, fp32 [M, K] row-major.
  *   mul         device fp32 [M, K] or NULL.  When given, the row fed to the
  *               quantiser is h = (r*r)*mul with r = max(x, 0) (the ReLU^2
@@ -125,6 +138,13 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
 
 /*
  * Contraction + rescale: y = (xq . Wq^T) / (sx * sw).
+ * The BitLinear matmul that replaces every Linear of the attention and the
+ * MLP (Candle PR "Add Support for BitNet Architecture Inference", the answer
+ * listing the changes made): int8 activations times ternary weights with
+ * exact integer accumulation, then one rescale by both quantisation scales.
+ * At M = 1 it is the per-token work that dominates decoding ("Hesper.Models.
+ * BitNet" page, section "Performance (BitNet-3B on A100)": the 32 layers take
+ * 870 of 883 ms per token).
  *   xq, x_scale   device, from bitlinear_quant_act (int8 [M, K], fp32 [M]).
  *   packed, w_scale  device, from bitlinear_quantize_weights for [N, K].
  *   y             device, fp32 [M, N] row-major, written.
