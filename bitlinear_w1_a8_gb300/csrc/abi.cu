@@ -11,6 +11,11 @@ cudaError_t launch_argmax(const float* y, int64_t M, int64_t N, int32_t* index, 
 cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
                            bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+// prefill.cu: several matrices sharing xq (and K) in one launch of either kernel.
+cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                                int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_batched_mats(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                                int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 // wide.cu: activations widened once into `workspace`, 128 weight rows x up to
 // 192 tokens per tile.
 size_t wide_workspace_bytes(int64_t M, int64_t K);
@@ -307,32 +312,37 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
   }
   cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s);
   if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
-  // The matrices the decode kernel takes share one launch; the rest get one
-  // tensor-core launch each.
-  DecodeMatrix dec[kMaxDecodeMats];
-  int ndec = 0;
-  for (int i = 0; i < num_weights; ++i)
-    if (auto_algo(M, mats[i].N, K) == BITLINEAR_ALGO_DECODE) dec[ndec++] = mats[i];
+  // The matrices that take the same kernel share one launch of it (WIDE, with
+  // its per-matrix pre-pass bookkeeping, takes one launch each).
+  DecodeMatrix dec[kMaxDecodeMats], bat[kMaxDecodeMats], pre[kMaxDecodeMats];
+  int ndec = 0, nbat = 0, npre = 0;
+  bool widened = false;  // the workspace holds this call's xq once a WIDE launch has widened it
+  for (int i = 0; i < num_weights; ++i) {
+    const int algo = auto_algo(M, mats[i].N, K);
+    if (algo == BITLINEAR_ALGO_DECODE) {
+      dec[ndec++] = mats[i];
+    } else if (have_ws && wide_wins(M, mats[i].N, K)) {
+      err = launch_wide(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
+                        workspace, !widened, pdl, dev, s);
+      if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
+      widened = true;
+    } else if (algo == BITLINEAR_ALGO_BATCHED) {
+      bat[nbat++] = mats[i];
+    } else {
+      pre[npre++] = mats[i];
+    }
+  }
   if (ndec > 0) {
     if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
     err = launch_decode(xq, x_scale, M, dec, ndec, K, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
-  bool widened = false;  // the workspace holds this call's xq once a WIDE launch has widened it
-  for (int i = 0; i < num_weights; ++i) {
-    const int algo = auto_algo(M, mats[i].N, K);
-    if (algo == BITLINEAR_ALGO_DECODE) continue;
-    if (have_ws && wide_wins(M, mats[i].N, K)) {
-      err = launch_wide(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y, mats[i].acc,
-                        workspace, !widened, pdl, dev, s);
-      widened = true;
-    } else {
-      err = algo == BITLINEAR_ALGO_BATCHED
-                ? launch_batched(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
-                                 mats[i].acc, pdl, dev, s)
-                : launch_prefill(xq, x_scale, M, mats[i].packed, mats[i].w_scale, mats[i].N, K, mats[i].y,
-                                 mats[i].acc, pdl, dev, s);
-    }
+  if (nbat > 0) {
+    err = launch_batched_mats(xq, x_scale, M, bat, nbat, K, pdl, dev, s);
+    if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  }
+  if (npre > 0) {
+    err = launch_prefill_mats(xq, x_scale, M, pre, npre, K, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   return BITLINEAR_OK;

@@ -81,21 +81,31 @@ constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 colu
 static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget");
 static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
 
-struct PrefillParams {
-  CUtensorMap tmap_a;  // xq [M, K] int8: 64 x 128 boxes, 64-byte swizzle (the raw ring's layout)
-  const int8_t* xq;
-  const float* sx;
+// One weight matrix of a launch: the matrices share the activations, each has
+// its own codes, scale, output and row count; its column tiles are the global
+// column tiles tn0 .. tn0 + tiles_n - 1.
+struct PrefillMat {
   const uint4* packed;
   const float* sw;
   float* y;
   int32_t* acc;
+  int N;
+  int tn0;
+};
+
+struct PrefillParams {
+  CUtensorMap tmap_a;  // xq [M, K] int8: 64 x 128 boxes, 64-byte swizzle (the raw ring's layout)
+  const int8_t* xq;
+  const float* sx;
   int* status;
-  int M, N, K, KB;
+  int M, K, KB;
   int n_tile;      // multiple of 16, <= 256 (SWAP: 128 weight rows a tile)
   int mma_n;       // MMA N = the rows of the shared-memory operand: n_tile, or (SWAP) tokens rounded up to 16
-  int tiles_m, tiles_n;
-  int splits;      // SWAP: K is split into this many ranges of KB k-steps (1 otherwise)
+  int tiles_m, tiles_n;  // tiles_n: column tiles of all matrices together
+  int splits;      // K is split into this many ranges of KB k-steps (1 otherwise)
   int num_tiles;   // work units: tiles_m * tiles_n * splits
+  int nmats;
+  PrefillMat mats[kMaxDecodeMats];
 };
 
 struct SharedCtl {
@@ -122,14 +132,19 @@ __device__ __forceinline__ void store_weight_half(uint32_t row_addr, int r, int 
   }
 }
 
-// Work unit -> first token row, first weight row and first k-block.
-__device__ __forceinline__ void tile_coords(const PrefillParams& p, int unit, int& m0, int& n0, int& kb0) {
+// Work unit -> first token row, matrix, first weight row of that matrix and
+// first k-block.
+__device__ __forceinline__ void tile_coords(const PrefillParams& p, int unit, int& m0, int& mi, int& n0, int& kb0) {
   const int tile = unit / p.splits;
   kb0 = (unit - tile * p.splits) * p.KB;
   const int tm = tile % p.tiles_m;
   const int tn = tile / p.tiles_m;
+  mi = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxDecodeMats; ++i)
+    if (i < p.nmats && tn >= p.mats[i].tn0) mi = i;
   m0 = tm * kTileM;
-  n0 = tn * p.n_tile;
+  n0 = (tn - p.mats[mi].tn0) * p.n_tile;
 }
 
 // SWAP = false: A (TMEM) = 128 token rows, B (shared) = n_tile weight rows.
@@ -184,11 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // M read as zeros) and one bulk copy the packed codes of the tile's rows.
     if (warp == kLoadWarp0 && lane == 0) {
       int ks = 0, tile = blockIdx.x;
-      int m0 = 0, n0 = 0, kb0 = 0;
+      int m0 = 0, mi = 0, n0 = 0, kb0 = 0;
       uint32_t code_bytes = 0;
       auto start_tile = [&]() {
-        tile_coords(p, tile, m0, n0, kb0);
-        const int rows = p.N - n0 < p.n_tile ? p.N - n0 : p.n_tile;  // rows past N are not read
+        tile_coords(p, tile, m0, mi, n0, kb0);
+        const int Nm = p.mats[mi].N;
+        const int rows = Nm - n0 < p.n_tile ? Nm - n0 : p.n_tile;  // rows past N are not read
         code_bytes = (uint32_t)rows * 16u;
       };
       if (total > 0) start_tile();
@@ -205,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ::"r"(raw), "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kx), "r"(m0),
               "r"(smem_u32(&ctl.raw_full[slot]))
             : "memory");
-        bulk_copy_g2s(raw + kRawABytes, p.packed + ((int64_t)(kb0 + ks) * p.N + n0), code_bytes, &ctl.raw_full[slot]);
+        bulk_copy_g2s(raw + kRawABytes, p.mats[mi].packed + ((int64_t)(kb0 + ks) * p.mats[mi].N + n0), code_bytes,
+                      &ctl.raw_full[slot]);
         last = f;
         if (++ks == p.KB) {
           ks = 0;
@@ -232,7 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npieces = p.mma_n * 4;               // SWAP: 16-byte token pieces
     int cks = grp, ctile = blockIdx.x;             // k-step f as (tile, k-step in tile)
     while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
-    int n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
+    int cm0, cmi, n0, ckb0;
+    tile_coords(p, ctile, cm0, cmi, n0, ckb0);
+    int Nm = p.mats[cmi].N;
     // Every k-step this group owns ends with its arrival on the stage's named
     // barrier, after an abort too (without the work), and never before the
     // stage's previous MMAs were committed (a wait that ignores the abort flag;
@@ -254,8 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();  // the MMAs that read this stage are complete
       const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
       if constexpr (SWAP) {
-        // Weights: row u of the tile (its 64 codes of this k-block) -> TMEM lane u.
-        const uint4 wv = ld_shared_v4(raw + kRawABytes + (uint32_t)(u * 16));
+        // Weights: row u of the tile (its 64 codes of this k-block) -> TMEM lane u;
+        // rows past N (not copied) are zeros.
+        const uint4 wv = n0 + u < Nm ? ld_shared_v4(raw + kRawABytes + (uint32_t)(u * 16))
+                                     : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
         const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
                                 (uint32_t)grp * kTmemAStageCols;
         uint32_t cols[16];
@@ -308,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (h >= nh) continue;
           const int row = h >> 1, half = h & 1;
           const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
-          if (n0 + row < p.N) {
+          if (n0 + row < Nm) {
             store_weight_half(row_addr, row, half, ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)));
           } else {  // rows past N are zeros
 #pragma unroll
@@ -325,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       cks += kConvGroups;
       if (cks >= p.KB) {
         while (cks >= p.KB) { cks -= p.KB; ctile += gridDim.x; }
-        n0 = (ctile / p.splits / p.tiles_m) * p.n_tile;
+        tile_coords(p, ctile, cm0, cmi, n0, ckb0);
+        Nm = p.mats[cmi].N;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -380,11 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;  // TMEM lane = row of the tile
-    const float sw = *p.sw;
     int it = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-      int m0, n0, kb0;
-      tile_coords(p, tile, m0, n0, kb0);
+      int m0, mi, n0, kb0;
+      tile_coords(p, tile, m0, mi, n0, kb0);
+      const PrefillMat& mat = p.mats[mi];
+      const float sw = *mat.sw;
+      const int N = mat.N;
       const int slot = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl.abort_flag, p.status)) break;
@@ -393,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // TMEM lane = weight row n, column t = token t: y[t, n] for t < M
         // (a warp writes 32 consecutive n of one token).
         const int n = n0 + row;
-        const bool n_ok = n < p.N;
+        const bool n_ok = n < N;
         const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
         for (int c = 0; c < p.mma_n; c += 16) {
           uint32_t r[16];
@@ -407,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (p.splits > 1) {
                 // a partial sum over this unit's K range: integer-valued fp32
                 // additions below 2^24 are exact in any order
-                atomicAdd(&p.y[(int64_t)t * p.N + n], a);
+                atomicAdd(&mat.y[(int64_t)t * N + n], a);
               } else {
-                p.y[(int64_t)t * p.N + n] = __fdiv_rn(a, __fmul_rn(p.sx[t], sw));
-                if (p.acc) p.acc[(int64_t)t * p.N + n] = __float2int_rn(a);
+                mat.y[(int64_t)t * N + n] = __fdiv_rn(a, __fmul_rn(p.sx[t], sw));
+                if (mat.acc) mat.acc[(int64_t)t * N + n] = __float2int_rn(a);
               }
             }
           }
@@ -423,19 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = m0 + row;
       const bool row_ok = m < p.M;
       const float den = row_ok ? __fmul_rn(p.sx[m], sw) : 1.0f;
-      float* yrow = p.y + (int64_t)(row_ok ? m : 0) * p.N;
-      int32_t* arow = p.acc ? p.acc + (int64_t)(row_ok ? m : 0) * p.N : nullptr;
+      float* yrow = mat.y + (int64_t)(row_ok ? m : 0) * N;
+      int32_t* arow = mat.acc ? mat.acc + (int64_t)(row_ok ? m : 0) * N : nullptr;
       const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
       for (int c = 0; c < p.n_tile; c += 16) {
         uint32_t r[16];
         tmem_ld16(t_row + (uint32_t)c, r);
         const int n = n0 + c;
-        if (!row_ok || n >= p.N) continue;
+        if (!row_ok || n >= N) continue;
         if (p.splits > 1) {
           // a partial sum over this unit's K range (exact integer-valued fp32 adds)
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (n + j < p.N) atomicAdd(yrow + n + j, __uint_as_float(r[j]));
+            if (n + j < N) atomicAdd(yrow + n + j, __uint_as_float(r[j]));
           continue;
         }
         float yv[16];
@@ -446,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           yv[j] = __fdiv_rn(a, den);
           av[j] = __float2int_rn(a);
         }
-        if (n + 16 <= p.N && ((((uintptr_t)(yrow + n)) & 15u) == 0)) {
+        if (n + 16 <= N && ((((uintptr_t)(yrow + n)) & 15u) == 0)) {
           float4* dst = reinterpret_cast<float4*>(yrow + n);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_float4(yv[4 * j], yv[4 * j + 1], yv[4 * j + 2], yv[4 * j + 3]);
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (n + j < p.N) {
+            if (n + j < N) {
               yrow[n + j] = yv[j];
               if (arow) arow[n + j] = av[j];
             }
@@ -561,12 +585,19 @@ cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cuda
   p.KB = KB / best_s;
   p.num_tiles = (int)(tiles * best_s);
   if (best_s == 1) return launch_impl<SWAP>(p, pdl, dev, stream);
-  const int64_t M = p.M, N = p.N;
-  cudaError_t err = cudaMemsetAsync(p.y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
-  if (err != cudaSuccess) return err;
+  const int64_t M = p.M;
+  cudaError_t err;
+  for (int i = 0; i < p.nmats; ++i) {
+    err = cudaMemsetAsync(p.mats[i].y, 0, (size_t)M * (size_t)p.mats[i].N * sizeof(float), stream);
+    if (err != cudaSuccess) return err;
+  }
   err = launch_impl<SWAP>(p, false, dev, stream);
   if (err != cudaSuccess) return err;
-  return launch_rescale(p.y, p.acc, p.sx, p.sw, M, N, dev, stream);
+  for (int i = 0; i < p.nmats; ++i) {
+    err = launch_rescale(p.mats[i].y, p.mats[i].acc, p.sx, p.mats[i].sw, M, p.mats[i].N, dev, stream);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -585,8 +616,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed, const float* sw,
-                            int64_t N, int64_t K, float* y, int32_t* acc, const DeviceInfo& dev) {
+PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                            int64_t K, const DeviceInfo& dev) {
   PrefillParams p;
   p.KB = 0;
   {
@@ -602,16 +633,40 @@ PrefillParams common_params(const int8_t* xq, const float* sx, int64_t M, const 
   }
   p.xq = xq;
   p.sx = sx;
-  p.packed = reinterpret_cast<const uint4*>(packed);
-  p.sw = sw;
-  p.y = y;
-  p.acc = acc;
   p.status = dev.status;
   p.M = (int)M;
-  p.N = (int)N;
   p.K = (int)K;
+  p.nmats = nmats;
+  for (int i = 0; i < kMaxDecodeMats; ++i) {
+    PrefillMat& m = p.mats[i];
+    if (i < nmats) {
+      m.packed = reinterpret_cast<const uint4*>(mats[i].packed);
+      m.sw = mats[i].w_scale;
+      m.y = mats[i].y;
+      m.acc = mats[i].acc;
+      m.N = (int)mats[i].N;
+    } else {
+      m = PrefillMat{nullptr, nullptr, nullptr, nullptr, 0, 1 << 30};
+    }
+  }
   if (p.KB != -1) p.KB = (int)(K / kKStep);
   return p;
+}
+
+// Column tiles of n_tile rows: each matrix starts a new tile.
+int64_t column_tiles(const DecodeMatrix* mats, int nmats, int64_t n_tile) {
+  int64_t t = 0;
+  for (int i = 0; i < nmats; ++i) t += (mats[i].N + n_tile - 1) / n_tile;
+  return t;
+}
+
+void assign_tiles(PrefillParams& p, const DecodeMatrix* mats, int nmats) {
+  int tn = 0;
+  for (int i = 0; i < nmats; ++i) {
+    p.mats[i].tn0 = tn;
+    tn += (int)((mats[i].N + p.n_tile - 1) / p.n_tile);
+  }
+  p.tiles_n = tn;
 }
 
 }  // namespace
@@ -633,10 +688,11 @@ cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float*
   return cudaLaunchKernelEx(&cfg, batched_rescale, y, acc, sx, sw, M, N);
 }
 
-cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
-                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
-                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+// The matrices share xq and K; one launch covers all of their tiles.
+cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                                int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (nmats < 1 || nmats > kMaxDecodeMats) return cudaErrorInvalidValue;
+  PrefillParams p = common_params(xq, sx, M, mats, nmats, K, dev);
   if (p.KB < 0) return cudaErrorNotSupported;
   // Tile width and K split together: the fewest (k-steps of the busiest CTA)
   // x (tile width + 64), the +64 being the activation widening of a k-step.
@@ -646,7 +702,7 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
     p.n_tile = kMaxTileN;
     for (int nt = kMaxTileN; nt >= 64; nt -= 16) {
       int64_t ksteps = 0;
-      const int64_t tiles = tiles_m * ((N + nt - 1) / nt);
+      const int64_t tiles = tiles_m * column_tiles(mats, nmats, nt);
       const int sp = best_split(tiles, p.KB, dev.num_sms, &ksteps);
       const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 : 0);
       if (best < 0 || cost < best) {
@@ -657,23 +713,36 @@ cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const u
   }
   p.mma_n = p.n_tile;
   p.tiles_m = (int)((M + kTileM - 1) / kTileM);
-  p.tiles_n = (int)((N + p.n_tile - 1) / p.n_tile);
+  assign_tiles(p, mats, nmats);
   return launch_split<false>(p, pdl, dev, stream);
+}
+
+cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  const DecodeMatrix m = {packed, sw, N, y, acc};
+  return launch_prefill_mats(xq, sx, M, &m, 1, K, pdl, dev, stream);
 }
 
 // 1 <= M <= 128: 128-row weight tiles on the M side of the MMA, all tokens on
 // its N side (rounded up to 16; token rows past M are zeros).
-cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
-                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
-                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  if (M < 1 || M > kTileM) return cudaErrorInvalidValue;
-  PrefillParams p = common_params(xq, sx, M, packed, sw, N, K, y, acc, dev);
+cudaError_t launch_batched_mats(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
+                                int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M < 1 || M > kTileM || nmats < 1 || nmats > kMaxDecodeMats) return cudaErrorInvalidValue;
+  PrefillParams p = common_params(xq, sx, M, mats, nmats, K, dev);
   if (p.KB < 0) return cudaErrorNotSupported;
   p.n_tile = kTileM;
   p.mma_n = (int)((M + 15) / 16 * 16);
   p.tiles_m = 1;
-  p.tiles_n = (int)((N + kTileM - 1) / kTileM);
+  assign_tiles(p, mats, nmats);
   return launch_split<true>(p, pdl, dev, stream);
+}
+
+cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
+                           const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
+                           bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  const DecodeMatrix m = {packed, sw, N, y, acc};
+  return launch_batched_mats(xq, sx, M, &m, 1, K, pdl, dev, stream);
 }
 
 }  // namespace bitlinear

@@ -243,9 +243,11 @@ typedef struct bitlinear_weight {
  * share of the packed weights while it quantises the token itself (CTA 0
  * writes xq, x_scale), which keeps a separate act_quant kernel and its
  * latency off the decode critical path; the matrices' CTAs share one grid.
- * Otherwise it runs bitlinear_quant_act, then one decode launch for the
- * matrices that bitlinear_forward's AUTO rule gives to the decode kernel and
- * one tensor-core launch (as that rule picks) for each of the others.
+ * Otherwise it runs bitlinear_quant_act, then one launch per kernel that
+ * bitlinear_forward's AUTO rule picks for some matrix: the matrices given to
+ * the same kernel (decode, batched or 128-token-tile) share one grid, whose
+ * tiles span all of them.  (A split-K launch adds, per matrix, the clearing
+ * of y before it and the rescale pass after it.)
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream).
@@ -260,7 +262,7 @@ bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, i
  * bitlinear_linear; otherwise 16-byte aligned and at least
  * bitlinear_forward_workspace(M, K) bytes, else BITLINEAR_ERR_WORKSPACE).
  * Matrices that bitlinear_forward_ws's AUTO rule gives to the WIDE kernel use
- * it; the activations are widened into the workspace once per call, shared by
+ * it, one launch each; the activations are widened into the workspace once per call, shared by
  * those matrices.  Results are bit-identical to bitlinear_linear.
  */
 bitlinear_status bitlinear_linear_ws(const float* x, const float* mul, int64_t M, int64_t K,

@@ -376,6 +376,47 @@ def test_linear_matches_oracle(M, K, Ns, prolog, ws):
         assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
 
 
+# Matrices that the AUTO rule gives to the same tensor-core kernel share one
+# grid whose column tiles span all of them; each case names the kernel(s) its
+# shapes select (batched: M <= 128, N <= 4096, M >= 64 or K < 8192; the
+# 128-token-tile kernel otherwise).  Ragged N puts a matrix boundary inside a
+# wave and leaves partial tiles in the middle of the tile index space.
+@pytest.mark.parametrize("M,K,Ns", [
+    (32, 2560, (2560, 2560)),             # batched: two matrices (BitNet-3B q, k widths)
+    (32, 2048, (300, 1000, 64)),          # batched: three ragged matrices
+    (130, 1024, (257, 100, 1000)),        # 128-token tiles: three ragged matrices, ragged M
+    (130, 12288, (300, 200)),             # 128-token tiles, split-K with two matrices
+    (512, 512, (1000, 1500)),             # 128-token tiles: two matrices, four token tiles
+    (512, 640, (130, 2000, 40)),          # 128-token tiles: three matrices
+    (64, 12288, (300, 520, 96)),          # batched, split-K with three matrices
+    (32, 1024, (5000, 2000, 700)),        # one 128-token-tile launch + one batched launch of two
+], ids=lambda v: str(v))
+def test_linear_tensor_core_groups(M, K, Ns):
+    x = synth.activations(M, K, 80 + K, outlier_seed=81 + K)
+    xq_o, sx_o = oracle.act_quant(x.numpy())
+    mats, refs = [], []
+    for i, N in enumerate(Ns):
+        W = synth.weight(N, K, 90 + i + N)
+        Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+        refs.append(oracle.forward(xq_o, sx_o, oracle.pack(Wq_o), sw_o, N, K))
+        _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        y = torch.full((M, N), float("nan"), device="cuda")
+        acc = torch.full((M, N), -3, dtype=torch.int32, device="cuda")
+        mats.append((packed_d, sw_d, y, acc))
+    xq = torch.zeros(M, K, dtype=torch.int8, device="cuda")
+    sx = torch.zeros(M, dtype=torch.float32, device="cuda")
+    for flags in (0, bl.FLAG_PDL):
+        for (_, _, y, acc) in mats:
+            y.fill_(float("nan"))
+            acc.fill_(-3)
+        bl.bitlinear_linear(x.cuda(), mats, xq, sx, flags=flags)
+        assert bl.bitlinear_device_status() == 0
+        np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
+        for (packed_d, sw_d, y, acc), (acc_o, y_o) in zip(mats, refs):
+            np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
+            assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
+
+
 # --- greedy choice after the LM head -------------------------------------------
 def _gpu_argmax(y):
     """y: numpy fp32 [M, N] -> int32 [M] through bitlinear_argmax (canary-guarded)."""
