@@ -100,10 +100,9 @@ __device__ __forceinline__ bool bar_try(unsigned long long* bar, uint32_t parity
       : "memory");
   return ok != 0;
 }
-// Bounded wait for phase 0 of a single-use barrier.
-__device__ __noinline__ bool bar_wait(unsigned long long* bar, int* status,
-                                      unsigned long long limit_ns = kWaitNs) {
-  if (bar_try(bar, 0)) return true;
+// Bounded wait for phase 0 of a single-use barrier (the first test inline:
+// a call costs several times the test).
+__device__ __noinline__ bool bar_wait_slow(unsigned long long* bar, int* status, unsigned long long limit_ns) {
   const unsigned long long t0 = now_ns();
   for (uint32_t i = 1;; ++i) {
     if (bar_try(bar, 0)) return true;
@@ -112,6 +111,9 @@ __device__ __noinline__ bool bar_wait(unsigned long long* bar, int* status,
       return false;
     }
   }
+}
+__device__ __forceinline__ bool bar_wait(unsigned long long* bar, int* status, unsigned long long limit_ns = kWaitNs) {
+  return bar_try(bar, 0) || bar_wait_slow(bar, status, limit_ns);
 }
 // sum over 4 bytes of (unsigned a_i) * (signed b_i), plus c
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {

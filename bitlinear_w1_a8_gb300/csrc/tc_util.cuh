@@ -41,9 +41,10 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
 }
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // if the CTA is aborting (another role timed out) or this wait timed out.
-static __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, int* abort_flag,
-                                       int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The first test is inlined (mbar_wait below): a call costs several times
+// the test itself, and most waits in the pipelines find the phase complete.
+static __device__ __noinline__ bool mbar_wait_slow(unsigned long long* bar, uint32_t parity, int* abort_flag,
+                                                   int* status) {
   const unsigned long long t0 = global_timer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -56,6 +57,9 @@ static __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t 
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, int* abort_flag, int* status) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, status);
 }
 // Bounded wait that ignores the abort flag: used to drain this thread's own
 // in-flight MMAs before TMEM is freed.
@@ -72,9 +76,8 @@ static __device__ __noinline__ void mbar_drain(unsigned long long* bar, uint32_t
 // Bounded wait that ignores the abort flag, for the waits that keep two roles
 // in step after an abort (the partner keeps completing the phases).  On timeout
 // it records BITLINEAR_ERR_TIMEOUT, raises the abort flag and returns false.
-static __device__ __noinline__ bool mbar_wait_lockstep(unsigned long long* bar, uint32_t parity, int* abort_flag,
-                                                int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_lockstep_slow(unsigned long long* bar, uint32_t parity,
+                                                            int* abort_flag, int* status) {
   const unsigned long long t0 = global_timer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,6 +87,10 @@ static __device__ __noinline__ bool mbar_wait_lockstep(unsigned long long* bar, 
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_lockstep(unsigned long long* bar, uint32_t parity, int* abort_flag,
+                                                   int* status) {
+  return mbar_try_wait(bar, parity) || mbar_wait_lockstep_slow(bar, parity, abort_flag, status);
 }
 // Named barriers (bar.arrive does not block; bar.sync waits for `count` threads).
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
