@@ -20,16 +20,17 @@
 //               tiles of every fourth k-step to fp16 in stage g -- the
 //               activations into TMEM (one row per lane), the weights into
 //               shared memory in the 128-byte-swizzled K-major layout
-//   warps 20-23 loader: one thread of warp 20 fills an 8-deep shared-memory
-//               ring, per k-step one TMA tensor copy of the 128 x 64 int8
-//               activation tile (64-byte swizzle) and one bulk copy of the
-//               packed codes, completing on the slot's barrier; warps 21-23
-//               only reach the final barrier (16-byte cp.async from 128
-//               loader threads had bounded the 192-wide k-step: 130.7 ->
-//               121.3 us at M = 2048, K = 2560 -> N = 10240)
+//   warps 20-23 loaders of an 8-deep shared-memory ring: per k-step one
+//               thread of warp 20 issues the TMA tensor copy of the 128 x 64
+//               int8 activation tile (64-byte swizzle) and one thread of warp
+//               21 the bulk copy of the packed codes, both completing on the
+//               slot's barrier; warps 22-23 only reach the final barrier
+//               (16-byte cp.async from 128 loader threads had bounded the
+//               192-wide k-step: 130.7 -> 121.3 us at M = 2048, K = 2560 ->
+//               N = 10240)
 //   warp 24     allocates TMEM; one lane issues tcgen05.mma
 // Every hand-off between roles is one mbarrier arrival per warp (raw slot
-// full: the loader's arrive.expect_tx plus the copies' transaction bytes),
+// full: the two loaders' arrive.expect_tx plus the copies' transaction bytes),
 // except "stage full" (converters -> MMA warp), a named barrier per stage.
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
 // so the widened activations never pass through shared memory, whose
@@ -67,7 +68,7 @@ constexpr int kConvGroups = kStages;                // group g converts the k-st
 constexpr int kGroupWarps = 4;
 constexpr int kGroupThreads = kGroupWarps * 32;     // 128
 constexpr int kConvWarps = kConvGroups * kGroupWarps;  // 16
-constexpr int kLoadWarps = 4;                       // warp 20 loads; 21-23 keep the warp layout
+constexpr int kLoadWarps = 4;                       // warps 20, 21 load; 22-23 keep the warp layout
 constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 20
 constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 24
 constexpr int kThreads = (kMmaWarp + 1) * 32;       // 800
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&ctl.raw_full[s], 1);
+      mbar_init(&ctl.raw_full[s], 2);  // the activation and the code loader
       mbar_init(&ctl.raw_empty[s], kGroupWarps);
     }
     for (int s = 0; s < 2; ++s) {
@@ -192,12 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
-    // ------------------------------------------------------------------ loader
-    // One thread per k-step: arms the slot's barrier with the bytes of both
-    // copies, then one TMA tensor copy brings the 128 x 64 int8 activation
-    // tile (64-byte swizzle: piece q of row r at q ^ ((r / 2) % 4); rows past
-    // M read as zeros) and one bulk copy the packed codes of the tile's rows.
-    if (warp == kLoadWarp0 && lane == 0) {
+    // ------------------------------------------------------------------ loaders
+    // Per k-step one TMA tensor copy of the 128 x 64 int8 activation tile
+    // (64-byte swizzle: piece q of row r at q ^ ((r / 2) % 4); rows past M read
+    // as zeros), issued by warp 20, and one bulk copy of the packed codes of the
+    // tile's rows, issued by warp 21.  Each issuing thread arms the slot's
+    // barrier with its own bytes (two arrivals a phase): one thread issuing
+    // both copies took about 0.1 us a copy, which bounded the k-step.
+    if ((warp == kLoadWarp0 || warp == kLoadWarp0 + 1) && lane == 0) {
+      const bool codes = warp != kLoadWarp0;
       int ks = 0, tile = blockIdx.x;
       int m0 = 0, mi = 0, n0 = 0, kb0 = 0;
       uint32_t code_bytes = 0;
@@ -214,15 +218,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t use = (uint32_t)(f / kRawStages);
         if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl.abort_flag, p.status)) break;
         const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
-        mbar_arrive_expect_tx(&ctl.raw_full[slot], (uint32_t)kRawABytes + code_bytes);
-        const int kx = (kb0 + ks) * kKStep;  // a multiple of 64 bytes
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-            ::"r"(raw), "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kx), "r"(m0),
-              "r"(smem_u32(&ctl.raw_full[slot]))
-            : "memory");
-        bulk_copy_g2s(raw + kRawABytes, p.mats[mi].packed + ((int64_t)(kb0 + ks) * p.mats[mi].N + n0), code_bytes,
-                      &ctl.raw_full[slot]);
+        if (codes) {
+          mbar_arrive_expect_tx(&ctl.raw_full[slot], code_bytes);
+          bulk_copy_g2s(raw + kRawABytes, p.mats[mi].packed + ((int64_t)(kb0 + ks) * p.mats[mi].N + n0), code_bytes,
+                        &ctl.raw_full[slot]);
+        } else {
+          mbar_arrive_expect_tx(&ctl.raw_full[slot], (uint32_t)kRawABytes);
+          const int kx = (kb0 + ks) * kKStep;  // a multiple of 64 bytes
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+              ::"r"(raw), "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kx), "r"(m0),
+                "r"(smem_u32(&ctl.raw_full[slot]))
+              : "memory");
+        }
         last = f;
         if (++ks == p.KB) {
           ks = 0;

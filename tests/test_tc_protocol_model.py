@@ -16,7 +16,9 @@ sources, so the model follows the kernels' constants.  The two kernels differ
 in what frees a ring slot: in wide.cu the MMAs of the slot's previous k-step
 (one commit frees slot and stage); in prefill.cu the converter warps that
 widened the slot's previous k-step (the raw slot is free once they have read
-it).
+it).  And in who fills it: in wide.cu the loader warps take turns; in
+prefill.cu two loader threads each copy a part of every k-step (activations,
+codes) and the slot is full once both copies have landed.
 """
 import os
 import random
@@ -61,11 +63,13 @@ def prefill_constants():
     assert "named_bar_arrive(1 + grp, kGroupThreads + 32);" in text and "named_bar_sync(1 + stage" in text
     assert "mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u" in text and "mma_commit(&ctl.empty[stage]);" in text
     assert "mbar_wait(&ctl.raw_empty[slot]" in text
-    # one loader thread issues every k-step's copies
-    assert "if (warp == kLoadWarp0 && lane == 0) {" in text and "for (int f = 0; f < total; ++f) {" in text
+    # two loader threads (activation tile, codes) each issue every k-step's
+    # copy and arm the slot's barrier with it: a slot is full after both
+    assert "if ((warp == kLoadWarp0 || warp == kLoadWarp0 + 1) && lane == 0) {" in text
+    assert "for (int f = 0; f < total; ++f) {" in text and "mbar_init(&ctl.raw_full[s], 2);" in text
     # empty[g] serves the k-steps f with f % stages == g: a done ring of `stages` barriers
     return dict(ring=int(_const(text, "kRawStages")), done=stages, stages=stages, groups=stages,
-                gw=int(_const(text, "kGroupWarps")), loaders=1, gate="conv")
+                gw=int(_const(text, "kGroupWarps")), loaders=2, gate="conv", fill="all")
 
 
 class MBar:
@@ -105,8 +109,11 @@ def simulate(c, total, seed, abort_at=None, barrier_of=None):
     raw_empty = [MBar() for _ in range(ring)]  # prefill: converter warps of the slot's k-step arrived
     raw_arrivals = {}
 
+    fills = {}  # (slot, use) -> copies landed; "all": every loader fills every k-step
+
     def loader(li):
-        for f in range(li, total, loaders):
+        share = range(total) if c.get("fill") == "all" else range(li, total, loaders)
+        for f in share:
             if f >= ring:
                 prev = f - ring
                 if c["gate"] == "mma":
@@ -123,7 +130,10 @@ def simulate(c, total, seed, abort_at=None, barrier_of=None):
 
             def land(slot=slot, k=k):
                 assert ring_full[slot].completed == k
-                ring_full[slot].completed += 1
+                need = loaders if c.get("fill") == "all" else 1
+                fills[(slot, k)] = fills.get((slot, k), 0) + 1
+                if fills[(slot, k)] == need:
+                    ring_full[slot].completed += 1
             pending.append((st["t"] + rnd.randint(1, 40), land))
 
     def converter(g, w):
