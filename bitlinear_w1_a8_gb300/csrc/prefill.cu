@@ -313,21 +313,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // Activations: row u of the tile -> TMEM lane u, columns of stage grp.
+        // Activations: row u of the tile -> TMEM lane u, columns of stage grp;
+        // weight half-rows h = u + 128 j.  Every shared-memory read of the
+        // k-step is issued before the first conversion (the wrappers are
+        // volatile, so program order is issue order), so their latencies
+        // overlap instead of adding up.
         const uint32_t row_raw = raw + (uint32_t)(u * kKStep);
         const uint32_t sw = (uint32_t)((u >> 1) & 3);
         const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
                                 (uint32_t)grp * kTmemAStageCols;
+        uint4 av[4];
+#pragma unroll
+        for (int piece = 0; piece < 4; ++piece) av[piece] = ld_shared_v4(row_raw + (((uint32_t)piece ^ sw) << 4));
+        uint2 wv[kHalvesPerThread];
+#pragma unroll
+        for (int j = 0; j < kHalvesPerThread; ++j) {
+          const int h = u + j * kGroupThreads;
+          wv[j] = (h < nh && n0 + (h >> 1) < Nm) ? ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)) : make_uint2(0u, 0u);
+        }
 #pragma unroll
         for (int hpair = 0; hpair < 2; ++hpair) {  // pieces 2h, 2h+1 -> columns 16h .. 16h+15
           uint32_t cols[16];
 #pragma unroll
           for (int pi = 0; pi < 2; ++pi) {
-            const uint32_t piece = (uint32_t)(2 * hpair + pi);
-            const uint4 av = ld_shared_v4(row_raw + ((piece ^ sw) << 4));
-            const uint32_t wv[4] = {av.x, av.y, av.z, av.w};
+            const uint4 a = av[2 * hpair + pi];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) i8x4_to_f16x4(wv[j], cols[8 * pi + 2 * j], cols[8 * pi + 2 * j + 1]);
+            for (int j = 0; j < 4; ++j) i8x4_to_f16x4(aw[j], cols[8 * pi + 2 * j], cols[8 * pi + 2 * j + 1]);
           }
           tmem_st16(t_addr + (uint32_t)(16 * hpair), cols);
         }
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = h >> 1, half = h & 1;
           const uint32_t row_addr = b_tile + (uint32_t)row * 128u;
           if (n0 + row < Nm) {
-            store_weight_half(row_addr, row, half, ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)));
+            store_weight_half(row_addr, row, half, wv[j]);
           } else {  // rows past N are zeros
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) st_shared_v4(row_addr + (uint32_t)((4 * half + cc) << 4), 0u, 0u, 0u, 0u);
