@@ -26,6 +26,7 @@ __device__ __forceinline__ void better(float v, int64_t i, float& bv, int64_t& b
 
 __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const float* __restrict__ y, int64_t N,
                                                              int32_t* __restrict__ out) {
+  pdl_release_dependents();
   __shared__ float sv[kArgThreads / 32];
   __shared__ int64_t si[kArgThreads / 32];
   const float* row = y + (int64_t)blockIdx.x * N;

@@ -185,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
 
-  // Inputs are produced by the previous kernel on the stream.
-  pdl_wait_primary();
+  // Let the next kernel on the stream start as SM resources free up; it still
+  // waits for this grid's results.
+  pdl_release_dependents();
 
   const uint32_t raw_base = stage_base + (uint32_t)kStages * kStageBytes;
   const int my_tiles = (int)blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -200,6 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile's rows, issued by warp 21.  Each issuing thread arms the slot's
     // barrier with its own bytes (two arrivals a phase): one thread issuing
     // both copies took about 0.1 us a copy, which bounded the k-step.
+    // The packed codes do not come from the previous kernel on the stream:
+    // only the activation loader waits for it (the codes of the first ring
+    // slots are requested while that kernel finishes).
+    if (warp == kLoadWarp0) pdl_wait_primary();
     if ((warp == kLoadWarp0 || warp == kLoadWarp0 + 1) && lane == 0) {
       const bool codes = warp != kLoadWarp0;
       int ks = 0, tile = blockIdx.x;
@@ -421,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue
+    pdl_wait_primary();  // sx comes from the previous kernel, which may still read y
     const int row = warp * 32 + lane;  // TMEM lane = row of the tile
     int it = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
@@ -527,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, int32_t* __restrict__ acc,
                                                        const float* __restrict__ sx, const float* __restrict__ sw,
                                                        int64_t M, int64_t N) {
+  pdl_release_dependents();
   pdl_wait_primary();
   const float w = *sw;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M * N; i += (int64_t)gridDim.x * blockDim.x) {

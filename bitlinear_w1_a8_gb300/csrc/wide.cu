@@ -138,6 +138,7 @@ __device__ __forceinline__ void unit_coords(const WideParams& p, int unit, int& 
 // 16-byte chunk of k-block kb; rows M .. Mp-1 are written as zeros.
 __global__ void __launch_bounds__(256) widen_tokens(const int8_t* __restrict__ xq, int M, int Mp, int K,
                                                     uint4* __restrict__ xw) {
+  pdl_release_dependents();
   pdl_wait_primary();  // xq comes from the previous kernel on the stream
   const int kb = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // chunk within the k-block plane
@@ -182,6 +183,7 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
   const uint32_t tmem_base = ctl.tmem_base;
 
   // The workspace is written by the pre-pass just before on the stream.
+  pdl_release_dependents();
   pdl_wait_primary();
 
   const int my_units = (int)blockIdx.x < p.num_units ? (p.num_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;

@@ -181,8 +181,13 @@ enum {
   /* Launch with programmatic dependent launch: the kernel starts streaming
    * the packed weights while the previous kernel on the stream (normally the
    * bitlinear_quant_act that produced xq) is still running, and waits for it
-   * before touching xq / x_scale.  Only valid when `packed` and `w_scale` were
-   * NOT written by the kernel immediately before on the stream. */
+   * before touching xq / x_scale and before writing y / acc.  Every kernel of
+   * this library lets the next one start this way as soon as all of its CTAs
+   * are running, so in a chain of calls with this flag several launches can
+   * be copying weights at once.  Only valid when `packed` and `w_scale` were
+   * written before the chain began: not by the kernel immediately before on
+   * the stream, nor by any kernel between it and the last launch made
+   * without this flag. */
   BITLINEAR_FLAG_PDL = 1
 };
 
