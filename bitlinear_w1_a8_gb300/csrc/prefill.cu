@@ -57,6 +57,7 @@ constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in
 constexpr int kTileM = 128;
 constexpr int kMaxTileN = 192;                   // multiple of 16; TMEM holds 2 x 192 + 4 x 32 columns
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
+constexpr int kMaxSplits = 8;                    // K ranges of a tile: a portable cluster
 constexpr int kBBytes = kMaxTileN * 128;         // 26 KB of fp16 weights per stage
 constexpr int kStageBytes = kBBytes;             // (the fp16 activations of a stage live in TMEM)
 constexpr int kRawABytes = kTileM * kKStep;      // 8 KB of int8 activations
@@ -75,7 +76,9 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;       // 800
 constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert(kThreads * 80 <= 65536, "80 registers a thread for one CTA per SM");
-static_assert(kStages + 1 <= 16, "named barriers 1 .. kStages");
+constexpr int kEpiBar = 1 + kStages;  // the epilogue warps' named barrier
+static_assert(kEpiBar < 16, "named barriers 1 .. kStages, kEpiBar");
+static_assert(kStages * kStageBytes >= kMaxTileN * kTileM * 4, "split-K partial sums fit over the operand stages");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
 constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
@@ -116,6 +119,7 @@ struct SharedCtl {
   unsigned long long tmem_full[2];
   unsigned long long tmem_empty[2];
   unsigned long long mma_done;
+  unsigned long long parts_ready;  // split K: one arrival per other rank of the cluster
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -176,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.tmem_empty[s], kEpiWarps);
     }
     mbar_init(&ctl.mma_done, 1);
+    mbar_init(&ctl.parts_ready, p.splits > 1 ? (uint32_t)(p.splits - 1) : 1u);
     ctl.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -183,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Split K: the ranks' barriers are initialised before another rank arrives on them.
+  if (p.splits > 1) cluster_sync_all();
   const uint32_t tmem_base = ctl.tmem_base;
 
   // Let the next kernel on the stream start as SM resources free up; it still
@@ -439,12 +446,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = (uint32_t)(it >> 1);
       if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl.abort_flag, p.status)) break;
       tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
+      if (p.splits > 1) {
+        // Split K (one unit per CTA; the units of a tile are one cluster, rank
+        // = K range): this rank's exact partial sums go to its own shared
+        // memory, column-major by TMEM lane ([column][128]), over the operand
+        // stages, which no MMA reads any more.
+        const int ncols = SWAP ? p.mma_n : p.n_tile;
+        for (int c = 0; c < ncols; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(t_row + (uint32_t)c, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(stage_base + (uint32_t)(((c + j) * kTileM + row) * 4)),
+                         "r"(__float2int_rn(__uint_as_float(r[j])))
+                         : "memory");
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.tmem_empty[slot]);
+        break;
+      }
       if constexpr (SWAP) {
         // TMEM lane = weight row n, column t = token t: y[t, n] for t < M
         // (a warp writes 32 consecutive n of one token).
         const int n = n0 + row;
         const bool n_ok = n < N;
-        const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
         for (int c = 0; c < p.mma_n; c += 16) {
           uint32_t r[16];
           tmem_ld16(t_row + (uint32_t)c, r);
@@ -454,14 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = c + j;
             if (t < p.M) {
               const float a = __uint_as_float(r[j]);  // an exact integer
-              if (p.splits > 1) {
-                // a partial sum over this unit's K range: integer-valued fp32
-                // additions below 2^24 are exact in any order
-                atomicAdd(&mat.y[(int64_t)t * N + n], a);
-              } else {
-                mat.y[(int64_t)t * N + n] = __fdiv_rn(a, __fmul_rn(p.sx[t], sw));
-                if (mat.acc) mat.acc[(int64_t)t * N + n] = __float2int_rn(a);
-              }
+              mat.y[(int64_t)t * N + n] = __fdiv_rn(a, __fmul_rn(p.sx[t], sw));
+              if (mat.acc) mat.acc[(int64_t)t * N + n] = __float2int_rn(a);
             }
           }
         }
@@ -475,19 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float den = row_ok ? __fmul_rn(p.sx[m], sw) : 1.0f;
       float* yrow = mat.y + (int64_t)(row_ok ? m : 0) * N;
       int32_t* arow = mat.acc ? mat.acc + (int64_t)(row_ok ? m : 0) * N : nullptr;
-      const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
       for (int c = 0; c < p.n_tile; c += 16) {
         uint32_t r[16];
         tmem_ld16(t_row + (uint32_t)c, r);
         const int n = n0 + c;
         if (!row_ok || n >= N) continue;
-        if (p.splits > 1) {
-          // a partial sum over this unit's K range (exact integer-valued fp32 adds)
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (n + j < N) atomicAdd(yrow + n + j, __uint_as_float(r[j]));
-          continue;
-        }
         float yv[16];
         int av[16];
 #pragma unroll
@@ -519,6 +532,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.tmem_empty[slot]);  // one arrival per warp
     }
+    if (p.splits > 1 && (int)blockIdx.x < p.num_tiles) {
+      // Every rank adds one share of the tile's columns over all ranks'
+      // partial sums (distributed shared memory) and writes those outputs.
+      // Every rank takes part whatever happened before, so the others' waits
+      // end early.
+      named_bar_sync(kEpiBar, kEpiWarps * 32);  // this rank's partial sums are written
+      const uint32_t rank = cluster_rank();
+      if (warp == 0 && lane < p.splits && lane != (int)rank)
+        mbar_arrive_remote(map_shared(smem_u32(&ctl.parts_ready), (uint32_t)lane));
+      if (mbar_wait_cluster(&ctl.parts_ready, 0u, &ctl.abort_flag, p.status) &&
+          *reinterpret_cast<volatile int*>(&ctl.abort_flag) == 0) {
+        int m0, mi, n0, kb0;
+        tile_coords(p, blockIdx.x, m0, mi, n0, kb0);
+        const PrefillMat& mat = p.mats[mi];
+        const float sw = *mat.sw;
+        const int N = mat.N;
+        const int ncols = SWAP ? p.mma_n : p.n_tile;
+        const int c0 = (int)rank * ncols / p.splits, c1 = ((int)rank + 1) * ncols / p.splits;
+        // item: column c, TMEM lanes l4 .. l4 + 3
+        for (int it = c0 * (kTileM / 4) + warp * 32 + lane; it < c1 * (kTileM / 4); it += kEpiWarps * 32) {
+          const int c = it / (kTileM / 4), l4 = (it % (kTileM / 4)) * 4;
+          const uint32_t off = stage_base + (uint32_t)((c * kTileM + l4) * 4);
+          uint4 part[kMaxSplits];
+#pragma unroll
+          for (int k = 0; k < kMaxSplits; ++k)  // every load issued before the sum
+            part[k] = k < p.splits ? ld_cluster_v4(map_shared(off, (uint32_t)k)) : make_uint4(0u, 0u, 0u, 0u);
+          uint4 tot = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int k = 0; k < kMaxSplits; ++k) {
+            tot.x += part[k].x;
+            tot.y += part[k].y;
+            tot.z += part[k].z;
+            tot.w += part[k].w;
+          }
+          const int av[4] = {(int)tot.x, (int)tot.y, (int)tot.z, (int)tot.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // SWAP: lane = weight row, column = token; else lane = token, column = weight row
+            const int t = SWAP ? c : m0 + l4 + e;
+            const int n = SWAP ? n0 + l4 + e : n0 + c;
+            if (t < p.M && n < N) {
+              mat.y[(int64_t)t * N + n] = __fdiv_rn(__int2float_rn(av[e]), __fmul_rn(p.sx[t], sw));
+              if (mat.acc) mat.acc[(int64_t)t * N + n] = av[e];
+            }
+          }
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -527,6 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // Split K: every rank has read the others' shared memory before any exits.
+  if (p.splits > 1) cluster_sync_all();
 }
 
 // After a split-K batched launch y holds acc (exact integers): y = acc / (sx * sw).
@@ -549,46 +612,90 @@ __global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, in
 namespace {
 
 template <bool SWAP>
-cudaError_t launch_impl(const PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  const size_t smem = (size_t)kSmemBytes + 1024;
+cudaError_t configure(const DeviceInfo& dev) {
   static thread_local int configured = -1;
   if (configured != dev.device) {
-    cudaError_t err =
-        cudaFuncSetAttribute(prefill_kernel<SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err = cudaFuncSetAttribute(prefill_kernel<SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes + 1024);
     if (err != cudaSuccess) return err;
     configured = dev.device;
   }
-  const int grid = p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms;
+  return cudaSuccess;
+}
+
+template <bool SWAP>
+cudaLaunchConfig_t launch_config(int grid, int cluster, bool pdl, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = (size_t)kSmemBytes + 1024;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  int na = 0;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = (unsigned)na;
+  return cfg;
+}
+
+// Clusters of `size` CTAs of this kernel that fit on the GPU at once (0 on
+// error); cached per device and size.
+template <bool SWAP>
+int max_clusters(int size, const DeviceInfo& dev) {
+  static thread_local int cache_dev = -1;
+  static thread_local int cache[kMaxSplits + 1];
+  if (cache_dev != dev.device) {
+    for (int i = 0; i <= kMaxSplits; ++i) cache[i] = -1;
+    cache_dev = dev.device;
+  }
+  if (cache[size] < 0) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config<SWAP>(size, size, false, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<SWAP>, &cfg) != cudaSuccess) n = 0;
+    cache[size] = n;
+  }
+  return cache[size];
+}
+
+template <bool SWAP>
+cudaError_t launch_impl(const PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  cudaError_t err = configure<SWAP>(dev);
+  if (err != cudaSuccess) return err;
+  const int grid = p.splits > 1 ? p.num_tiles : (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config<SWAP>(grid, p.splits, pdl, stream, attr);
   return cudaLaunchKernelEx(&cfg, prefill_kernel<SWAP>, p);
 }
 
-// Split K (into a divisor of the k-block count, at most 16) when there are
-// too few tiles to fill the SMs: minimise the k-steps of the busiest CTA.
-// With a split, y is zeroed first, every unit adds its integer-valued partial
-// sums into y, and a rescale pass divides by sx * sw.
-int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out) {
+// Split K (into a divisor of the k-block count, at most kMaxSplits: a portable
+// cluster) when there are too few tiles to fill the SMs: minimise the k-steps
+// of the busiest CTA.  The units of a tile run as one thread-block cluster;
+// each rank adds a share of the tile's columns over all ranks' partial sums
+// (distributed shared memory), so every cluster must be resident at once (at
+// most `clusters[sp]` of them).
+int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out, const int* clusters = nullptr) {
   int best_s = 1;
   int64_t best_cost = -1;
-  // Only when at most half the SMs have a tile: the zeroing, the atomics and
-  // the rescale pass cost a pass over y each.
-  // A split must keep every unit in one wave and at least 8 k-steps long: each
-  // unit pays a pipeline fill and one atomic add per output of its tile.
-  for (int sp = 1; sp <= 16 && sp <= KB && (sp == 1 || 2 * tiles <= num_sms); ++sp) {
+  // A split keeps every unit in one wave and at least 8 k-steps long (each
+  // unit pays a pipeline fill and the reduction).
+  for (int sp = 1; sp <= kMaxSplits && sp <= KB && (sp == 1 || 2 * tiles <= num_sms); ++sp) {
     if (KB % sp) continue;
     if (sp > 1 && (tiles * sp > num_sms || KB / sp < 8)) continue;
+    if (sp > 1 && clusters && tiles > clusters[sp]) continue;
     const int64_t units = tiles * sp;
     const int64_t waves = (units + num_sms - 1) / num_sms;
-    const int64_t cost = waves * (KB / sp) + (sp > 1 ? 4 : 0);  // + the zeroing and rescale passes
+    const int64_t cost = waves * (KB / sp) + (sp > 1 ? 2 : 0);  // + the reduction
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_s = sp;
@@ -598,33 +705,20 @@ int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out) {
   return best_s;
 }
 
-}  // namespace
-cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float* sw, int64_t M, int64_t N,
-                           const DeviceInfo& dev, cudaStream_t stream);
-namespace {
-
 template <bool SWAP>
 cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  cudaError_t err = configure<SWAP>(dev);
+  if (err != cudaSuccess) return err;
   const int KB = p.KB;
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
-  const int best_s = best_split(tiles, KB, dev.num_sms, nullptr);
+  int clusters[kMaxSplits + 1] = {0};
+  if (2 * tiles <= dev.num_sms)
+    for (int sp = 2; sp <= kMaxSplits; ++sp) clusters[sp] = max_clusters<SWAP>(sp, dev);
+  const int best_s = best_split(tiles, KB, dev.num_sms, nullptr, clusters);
   p.splits = best_s;
   p.KB = KB / best_s;
   p.num_tiles = (int)(tiles * best_s);
-  if (best_s == 1) return launch_impl<SWAP>(p, pdl, dev, stream);
-  const int64_t M = p.M;
-  cudaError_t err;
-  for (int i = 0; i < p.nmats; ++i) {
-    err = cudaMemsetAsync(p.mats[i].y, 0, (size_t)M * (size_t)p.mats[i].N * sizeof(float), stream);
-    if (err != cudaSuccess) return err;
-  }
-  err = launch_impl<SWAP>(p, false, dev, stream);
-  if (err != cudaSuccess) return err;
-  for (int i = 0; i < p.nmats; ++i) {
-    err = launch_rescale(p.mats[i].y, p.mats[i].acc, p.sx, p.mats[i].sw, M, p.mats[i].N, dev, stream);
-    if (err != cudaSuccess) return err;
-  }
-  return cudaSuccess;
+  return launch_impl<SWAP>(p, pdl, dev, stream);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

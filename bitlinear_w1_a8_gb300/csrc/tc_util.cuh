@@ -1,7 +1,8 @@
 // tc_util.cuh -- PTX wrappers and operand widening shared by the tcgen05
 // kernels (sm_103a): mbarriers with bounded waits, named barriers, TMEM
 // allocation / loads / stores, tcgen05.mma with A in TMEM, shared-memory
-// descriptors, cp.async, and the exact int8 / 2-bit-code -> fp16 widening.
+// descriptors, cp.async, cluster barriers and distributed shared memory, and
+// the exact int8 / 2-bit-code -> fp16 widening.
 #pragma once
 
 #include "common.cuh"
@@ -91,6 +92,64 @@ static __device__ __noinline__ bool mbar_wait_lockstep_slow(unsigned long long* 
 __device__ __forceinline__ bool mbar_wait_lockstep(unsigned long long* bar, uint32_t parity, int* abort_flag,
                                                    int* status) {
   return mbar_try_wait(bar, parity) || mbar_wait_lockstep_slow(bar, parity, abort_flag, status);
+}
+// ---------------------------------------------------------------------------
+// Thread-block clusters: rank, the all-thread cluster barrier, distributed
+// shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; orders this CTA's earlier
+// shared-memory writes before the other CTAs' later reads.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's (and, through an earlier CTA barrier, its CTA's) prior writes.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+// Bounded wait whose completion also acquires what other CTAs of the cluster
+// released on this barrier (their remote arrivals).
+static __device__ __noinline__ bool mbar_wait_cluster(unsigned long long* bar, uint32_t parity, int* abort_flag,
+                                                      int* status) {
+  const unsigned long long t0 = global_timer();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 63u) == 63u) {
+      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+      if (global_timer() - t0 > kTimeoutNs) {
+        atomicExch(abort_flag, 1);
+        atomicExch(status, (int)BITLINEAR_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 // Named barriers (bar.arrive does not block; bar.sync waits for `count` threads).
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
