@@ -84,26 +84,33 @@ constexpr int64_t kPrefillMaxK = 131072;
 int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
-  if (M <= 16 && K <= 65536 && !(K >= 8192 && M > 8)) return BITLINEAR_ALGO_DECODE;
-  if (M <= 128 && N <= 4096 && (M >= 64 || K < 8192)) return BITLINEAR_ALGO_BATCHED;
+  // Measured on GB300 (BitNet-3B projections, back-to-back calls): the dp4a
+  // decode kernel wins up to 8 tokens on every shape and up to 16 for K < 8192;
+  // beyond, the batched tensor-core kernel (weight rows on the MMA's M side, K
+  // split inside a cluster) wins up to 64 column tiles, and the 128-token-tile
+  // kernel on wider outputs (M = 32: q||k||v 13.1 vs 20.8 us, o 8.5 vs 12.5,
+  // down 15.5 vs 22.4; gate||up 30.3 vs 23.4).
+  if (M <= 8 && K <= 65536) return BITLINEAR_ALGO_DECODE;
+  if (M <= 16 && K < 8192) return BITLINEAR_ALGO_DECODE;
+  if (M <= 128 && N <= 8192) return BITLINEAR_ALGO_BATCHED;
   return BITLINEAR_ALGO_PREFILL;
 }
 
 // With a workspace, AUTO takes the WIDE kernel for narrow outputs at medium
-// token counts, where it measured faster on GB300 (hot L2, pre-pass included;
-// WIDE vs the AUTO kernel, at M = 32 / 64 / 96 / 128 / 256 / 512 / 1024):
-//   N = 2560, K = 10240: 1.10 / 1.25 / 1.33 / 1.40 / 1.19 / 1.41 / 1.09x
-//   N = 2048, K = 8192:  1.21 / 1.23 / 1.26 / 1.39 / 1.38 / 1.38 / 1.06x
-//   N = K = 2560:        0.93 / 1.03 / 1.10 / 1.29 / 1.71 / 1.03 / 0.89x
-//   N = K = 2048:        0.85 / 0.96 / 1.26 (M <= 96 measured)
-// and for wide outputs (N = 8192, 10240) and at M = 2048: 0.67 - 1.00x.
-// In a whole BitNet-3B token step (cold weights, the pre-pass one more launch
-// on the chain) the down projections at M = 32 made the step 1.8 % slower
-// (at M = 64, 0.8 % faster): long K starts at M = 64.
+// token counts above the batched kernel's range, where it measured faster on
+// GB300 than the 128-token-tile kernel (hot L2, pre-pass included; at
+// M = 256 / 512 / 1024):
+//   N = 2560, K = 10240: 1.19 / 1.41 / 1.09x
+//   N = 2048, K = 8192:  1.38 / 1.38 / 1.06x
+//   N = K = 2560:        1.71 / 1.03 / 0.89x
+// and for wide outputs (N = 8192, 10240) and at M = 2048: 0.67 - 1.00x.  Up to
+// M = 128 the batched kernel (K split inside a cluster) is within a few per
+// cent of WIDE without the pre-pass launch (BitNet-3B o / down at M = 64:
+// 10.1 / 17.4 us against 10.7 / 17.9).
 bool wide_wins(int64_t M, int64_t N, int64_t K) {
-  if (N > 4096 || M > 1024) return false;
-  if (K >= 8192) return M >= 64;
-  return M >= 96 && M <= 512;
+  if (N > 4096 || M > 1024 || M <= 128) return false;
+  if (K >= 8192) return true;
+  return M <= 512;
 }
 
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values

@@ -152,13 +152,13 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *                 integer accumulators (for checking and debugging).
  * The kernel is chosen from M, N and K (BITLINEAR_ALGO_AUTO): the decode
  * kernel (packed weights bulk-copied into shared memory, dp4a on the 2-bit
- * codes; K <= 65536) for M <= 4, and for M <= 16 (M <= 8 when K >= 8192)
+ * codes; K <= 65536) for M <= 4, and for M <= 8 (M <= 16 when K < 8192)
  * when N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
- * MMA's M side, all tokens on its N side) for N <= 4096 and M <= 128 (from
- * M = 64 when K >= 8192); the tcgen05 kernel with 128-token tiles
- * (K <= 131072) otherwise.  Both tensor-core kernels split K over CTAs when
- * their tiles fill less than half of the SMs (y is then zeroed, accumulated
- * and rescaled in place: three passes on the stream).
+ * MMA's M side, all tokens on its N side) for N <= 8192 and M <= 128; the
+ * tcgen05 kernel with 128-token tiles (K <= 131072) otherwise.  Both
+ * tensor-core kernels split K over up to 8 CTAs when their tiles fill less
+ * than half of the SMs; the CTAs of a tile form one thread-block cluster and
+ * add their partial sums through distributed shared memory (one launch).
  */
 bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64_t M,
                                    const uint8_t* packed, const float* w_scale,
@@ -214,10 +214,11 @@ size_t bitlinear_forward_workspace(int64_t M, int64_t K);
  * 2-bit weight codes (into tensor memory) and bulk-copies the token tiles.
  * Results are bit-identical to every other algorithm.  BITLINEAR_ALGO_AUTO
  * follows bitlinear_forward's rule, except that it takes WIDE for narrow
- * outputs at medium token counts -- N <= 4096 and 64 <= M <= 1024 when
- * K >= 8192, 96 <= M <= 512 otherwise -- where it measured 1.03-1.71x faster
+ * outputs at medium token counts -- N <= 4096 and 128 < M <= 1024 when
+ * K >= 8192, 128 < M <= 512 otherwise -- where it measured 1.06-1.71x faster
  * on GB300 (BitNet-3B q/k/v/o and down, BitNet-1.3B down shapes); for wide
- * outputs and at M = 2048 the other kernels measured faster.  The other algorithms ignore the workspace.
+ * outputs, at M = 2048 and below 129 tokens the other kernels measured
+ * faster or within a few per cent.  The other algorithms ignore the workspace.
  * Errors: as bitlinear_forward_ex; BITLINEAR_ERR_WORKSPACE when
  * BITLINEAR_ALGO_WIDE is asked for without a large enough workspace;
  * BITLINEAR_ERR_ALIGN for a misaligned workspace.

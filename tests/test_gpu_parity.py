@@ -336,7 +336,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (130, 320, (257, 100), "norm"),         # tensor-core path per matrix
     (200, 1024, (300, 1000, 2000), None),   # WIDE region (with ws): three matrices, one pre-pass
     (256, 8192, (2048,), "gated+norm"),     # a 1.3B FFN down call in the WIDE region
-    (64, 8192, (2048, 300), "gated"),       # long K: WIDE from M = 64 (with ws)
+    (64, 8192, (2048, 300), "gated"),       # long K at M = 64: batched kernel, K split in a cluster
+    (136, 8192, (1000, 300), "gated"),      # long K above 128 tokens: WIDE (with ws)
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_matches_oracle(M, K, Ns, prolog, ws):
