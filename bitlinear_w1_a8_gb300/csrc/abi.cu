@@ -317,7 +317,7 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
     return from_cuda(launch_decode_fused(x, mul, rms_weight, rms_eps, K, mats, num_weights, xq, x_scale, pdl,
                                          dev, s));
   }
-  cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s);
+  cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s, pdl);
   if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   // The matrices that take the same kernel share one launch of it (WIDE, with
   // its per-matrix pre-pass bookkeeping, takes one launch each).

@@ -18,6 +18,9 @@ act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int
   __shared__ RowQuantScratch sc;
   // Let a dependent forward kernel start streaming its weights now.
   pdl_release_dependents();
+  // With programmatic launch, x (and mul) come from the previous kernel, which
+  // may also still be reading xq.
+  pdl_wait_primary();
   const int64_t row = blockIdx.x;
   const float s = quantize_row(x + row * (int64_t)K, mul ? mul + row * (int64_t)K : nullptr, gamma, eps, K,
                                hs, sc, xq + row * (int64_t)K);
@@ -28,7 +31,7 @@ act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int
 
 cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_t K,
                              const float* gamma, double eps, int8_t* xq, float* sx,
-                             const DeviceInfo& dev, cudaStream_t stream) {
+                             const DeviceInfo& dev, cudaStream_t stream, bool pdl) {
   const size_t smem = (size_t)K * sizeof(float);
   static thread_local int configured_device = -1;
   static thread_local size_t configured_smem = 0;
@@ -41,8 +44,17 @@ cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_
     configured_smem = dev.smem_optin - 4096;
   }
   const int threads = M < dev.num_sms ? kActThreadsFew : kActThreadsMany;
-  act_quant_kernel<<<(unsigned)M, threads, smem, stream>>>(x, mul, (int)K, gamma, eps, xq, sx);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, mul, (int)K, gamma, eps, xq, sx);
 }
 
 }  // namespace bitlinear

@@ -166,9 +166,11 @@ cudaError_t launch_weight_quant(const float* W, int64_t N, int64_t K, uint8_t* p
                                 float* w_scale, unsigned long long* buckets,
                                 const DeviceInfo& dev, cudaStream_t stream);
 
+// pdl: launched with programmatic dependent launch (waits for the previous
+// kernel on the stream before it reads x or writes xq).
 cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_t K,
                              const float* gamma, double eps, int8_t* xq, float* sx,
-                             const DeviceInfo& dev, cudaStream_t stream);
+                             const DeviceInfo& dev, cudaStream_t stream, bool pdl = false);
 
 cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
                            const float* sw, int64_t N, int64_t K, float* y, int32_t* acc,
