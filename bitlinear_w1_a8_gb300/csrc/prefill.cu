@@ -53,17 +53,14 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 4;                       // fp16 operand stages read by the MMA
-constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring
+constexpr int kRawStages = 8;                    // raw int8 / packed k-steps in the ring (192-wide tiles)
+constexpr int kRawStagesBig = 4;                 // the same for 320-wide tiles (the stages take the room)
 constexpr int kTileM = 128;
 constexpr int kMaxTileN = 192;                   // multiple of 16; TMEM holds 2 x 192 + 4 x 32 columns
+constexpr int kMaxTileNBig = 320;                // one accumulator: TMEM holds 320 + 4 x 32 columns
 constexpr int kKStep = 64;                       // K elements per stage (128 B of fp16)
 constexpr int kMaxSplits = 8;                    // K ranges of a tile: a portable cluster
-constexpr int kBBytes = kMaxTileN * 128;         // 26 KB of fp16 weights per stage
-constexpr int kStageBytes = kBBytes;             // (the fp16 activations of a stage live in TMEM)
 constexpr int kRawABytes = kTileM * kKStep;      // 8 KB of int8 activations
-constexpr int kRawBBytes = kMaxTileN * 16;       // 3.25 KB of packed codes
-constexpr int kRawStageBytes = kRawABytes + kRawBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + kRawStages * kRawStageBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kConvGroups = kStages;                // group g converts the k-steps f with f % kStages == g
 constexpr int kGroupWarps = 4;
@@ -73,17 +70,34 @@ constexpr int kLoadWarps = 4;                       // warps 20, 21 load; 22-23 
 constexpr int kLoadWarp0 = kEpiWarps + kConvWarps;  // 20
 constexpr int kMmaWarp = kLoadWarp0 + kLoadWarps;   // 24
 constexpr int kThreads = (kMmaWarp + 1) * 32;       // 800
-constexpr int kHalvesPerThread = (2 * kMaxTileN + kGroupThreads - 1) / kGroupThreads;  // weight half-rows
 static_assert(kGroupThreads == kTileM, "one activation row (TMEM lane) per converter thread");
 static_assert(kThreads * 80 <= 65536, "80 registers a thread for one CTA per SM");
 constexpr int kEpiBar = 1 + kStages;  // the epilogue warps' named barrier
 static_assert(kEpiBar < 16, "named barriers 1 .. kStages, kEpiBar");
-static_assert(kStages * kStageBytes >= kMaxTileN * kTileM * 4, "split-K partial sums fit over the operand stages");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemACol = 2 * kMaxTileN;      // activation stages follow the two accumulators
 constexpr uint32_t kTmemAStageCols = kKStep / 2;   // 64 fp16 of a row = 32 columns
-static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget");
-static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
+
+// Tile geometry.  Normal: output tiles up to 192 wide with two TMEM
+// accumulators, so the epilogue of one tile overlaps the MMAs of the next.
+// BIG: one tile up to 320 wide per CTA (two MMAs per K slice beyond 256
+// columns) with one accumulator: the activations of a k-step are widened once
+// for 320 weight rows instead of 192, which pays when the tiles fit in one
+// wave (the epilogue then overlaps nothing anyway).
+template <bool BIG>
+struct Shape {
+  static constexpr int kTileNMax = BIG ? kMaxTileNBig : kMaxTileN;
+  static constexpr int kAccBufs = BIG ? 1 : 2;
+  static constexpr int kRing = BIG ? kRawStagesBig : kRawStages;
+  static constexpr int kStageBytes = kTileNMax * 128;  // fp16 weights of a stage (activations live in TMEM)
+  static constexpr int kRawStageBytes = kRawABytes + kTileNMax * 16;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kRing * kRawStageBytes;
+  static constexpr uint32_t kTmemACol = (uint32_t)(kAccBufs * kTileNMax);  // activation stages follow
+  static constexpr int kHalvesPerThread = (2 * kTileNMax + kGroupThreads - 1) / kGroupThreads;
+  static_assert(kTmemACol + kStages * kTmemAStageCols <= kTmemCols, "TMEM budget");
+  static_assert(kStageBytes % 1024 == 0 && kRawStageBytes % 16 == 0, "stage alignment");
+  static_assert(kStages * kStageBytes >= kTileNMax * kTileM * 4, "split-K partial sums fit over the operand stages");
+  static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory");
+};
 
 // One weight matrix of a launch: the matrices share the activations, each has
 // its own codes, scale, output and row count; its column tiles are the global
@@ -103,8 +117,9 @@ struct PrefillParams {
   const float* sx;
   int* status;
   int M, K, KB;
-  int n_tile;      // multiple of 16, <= 256 (SWAP: 128 weight rows a tile)
+  int n_tile;      // multiple of 16, <= 192 (BIG: 320; SWAP: 128 weight rows a tile)
   int mma_n;       // MMA N = the rows of the shared-memory operand: n_tile, or (SWAP) tokens rounded up to 16
+  int mma_n1;      // BIG, n_tile > 256: the first MMA of a K slice covers rows 0 .. mma_n1 - 1, the second the rest
   int tiles_m, tiles_n;  // tiles_n: column tiles of all matrices together
   int splits;      // K is split into this many ranges of KB k-steps (1 otherwise)
   int num_tiles;   // work units: tiles_m * tiles_n * splits
@@ -156,9 +171,10 @@ __device__ __forceinline__ void tile_coords(const PrefillParams& p, int unit, in
 // SWAP = true (few tokens): A = 128 weight rows, B = every token (M <= 128),
 // so the weights pass through the tensor cores once.  The loader is the same
 // (token rows 0 .. 127 of the activations, weight rows n0 .. n0 + 127).
-template <bool SWAP>
+template <bool SWAP, bool BIG>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using S = Shape<BIG>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ SharedCtl ctl;
   const int warp = threadIdx.x >> 5;
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl.empty[s], 1);
     }
-    for (int s = 0; s < kRawStages; ++s) {
+    for (int s = 0; s < S::kRing; ++s) {
       mbar_init(&ctl.raw_full[s], 2);  // the activation and the code loader
       mbar_init(&ctl.raw_empty[s], kGroupWarps);
     }
@@ -196,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // waits for this grid's results.
   pdl_release_dependents();
 
-  const uint32_t raw_base = stage_base + (uint32_t)kStages * kStageBytes;
+  const uint32_t raw_base = stage_base + (uint32_t)kStages * S::kStageBytes;
   const int my_tiles = (int)blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int total = my_tiles * p.KB;  // flat k-steps of this CTA, tile-major
 
@@ -226,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (total > 0) start_tile();
       int last = -1;
       for (int f = 0; f < total; ++f) {
-        const int slot = f % kRawStages;
-        const uint32_t use = (uint32_t)(f / kRawStages);
+        const int slot = f % S::kRing;
+        const uint32_t use = (uint32_t)(f / S::kRing);
         if (!mbar_wait(&ctl.raw_empty[slot], (use & 1u) ^ 1u, &ctl.abort_flag, p.status)) break;
-        const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
+        const uint32_t raw = raw_base + (uint32_t)slot * S::kRawStageBytes;
         if (codes) {
           mbar_arrive_expect_tx(&ctl.raw_full[slot], code_bytes);
           bulk_copy_g2s(raw + kRawABytes, p.mats[mi].packed + ((int64_t)(kb0 + ks) * p.mats[mi].N + n0), code_bytes,
@@ -251,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // No copy may outlive the CTA: wait (bounded) for the last fills.
-      for (int f = last; f >= 0 && f > last - kRawStages; --f)
-        mbar_drain(&ctl.raw_full[f % kRawStages], (uint32_t)((f / kRawStages) & 1), p.status);
+      for (int f = last; f >= 0 && f > last - S::kRing; --f)
+        mbar_drain(&ctl.raw_full[f % S::kRing], (uint32_t)((f / S::kRing) & 1), p.status);
     }
     __syncwarp();
   } else if (warp >= kEpiWarps && warp < kLoadWarp0) {
@@ -280,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // k-step, and the MMA warp's syncs, which cannot time out, always complete.
     bool live = true;
     for (int f = grp; f < total; f += kConvGroups) {
-      const int slot = f % kRawStages;
-      const uint32_t use = (uint32_t)(f / kRawStages);
+      const int slot = f % S::kRing;
+      const uint32_t use = (uint32_t)(f / S::kRing);
       const uint32_t fill = (uint32_t)(f / kConvGroups);  // earlier fills of this stage
       const bool stage_free = mbar_wait_lockstep(&ctl.empty[grp], (fill & 1u) ^ 1u, &ctl.abort_flag, p.status);
       live = live && stage_free && mbar_wait(&ctl.raw_full[slot], use & 1u, &ctl.abort_flag, p.status);
@@ -289,15 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_arrive(1 + grp, kGroupThreads + 32);
         continue;
       }
-      const uint32_t raw = raw_base + (uint32_t)slot * kRawStageBytes;
+      const uint32_t raw = raw_base + (uint32_t)slot * S::kRawStageBytes;
       tc_fence_after();  // the MMAs that read this stage are complete
-      const uint32_t b_tile = stage_base + (uint32_t)grp * kStageBytes;
+      const uint32_t b_tile = stage_base + (uint32_t)grp * S::kStageBytes;
       if constexpr (SWAP) {
         // Weights: row u of the tile (its 64 codes of this k-block) -> TMEM lane u;
         // rows past N (not copied) are zeros.
         const uint4 wv = n0 + u < Nm ? ld_shared_v4(raw + kRawABytes + (uint32_t)(u * 16))
                                      : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
-        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
+        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + S::kTmemACol +
                                 (uint32_t)grp * kTmemAStageCols;
         uint32_t cols[16];
         codes_to_f16x8(wv.x, cols);
@@ -332,14 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // overlap instead of adding up.
         const uint32_t row_raw = raw + (uint32_t)(u * kKStep);
         const uint32_t sw = (uint32_t)((u >> 1) & 3);
-        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + kTmemACol +
+        const uint32_t t_addr = tmem_base + ((uint32_t)((u >> 5) * 32) << 16) + S::kTmemACol +
                                 (uint32_t)grp * kTmemAStageCols;
         uint4 av[4];
 #pragma unroll
         for (int piece = 0; piece < 4; ++piece) av[piece] = ld_shared_v4(row_raw + (((uint32_t)piece ^ sw) << 4));
-        uint2 wv[kHalvesPerThread];
+        uint2 wv[S::kHalvesPerThread];
 #pragma unroll
-        for (int j = 0; j < kHalvesPerThread; ++j) {
+        for (int j = 0; j < S::kHalvesPerThread; ++j) {
           const int h = u + j * kGroupThreads;
           wv[j] = (h < nh && n0 + (h >> 1) < Nm) ? ld_shared_v2(raw + kRawABytes + (uint32_t)(h * 8)) : make_uint2(0u, 0u);
         }
@@ -356,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(t_addr + (uint32_t)(16 * hpair), cols);
         }
 #pragma unroll
-        for (int j = 0; j < kHalvesPerThread; ++j) {
+        for (int j = 0; j < S::kHalvesPerThread; ++j) {
           const int h = u + j * kGroupThreads;
           if (h >= nh) continue;
           const int row = h >> 1, half = h & 1;
@@ -391,30 +407,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // still syncs and commits every k-step (issuing nothing), so the
     // converters, which wait for those commits, stay in step with it.
     {
-      const uint32_t idesc = make_idesc(kTileM, p.mma_n);
+      // BIG tiles wider than 256 take two MMAs a K slice (rows 0 .. mma_n1 - 1,
+      // then the rest: B 128 bytes a row further, D mma_n1 columns further).
+      const bool two = BIG && p.mma_n1 > 0;
+      const int n1 = two ? p.mma_n1 : p.mma_n;
+      const uint32_t idesc = make_idesc(kTileM, n1);
+      const uint32_t idesc2 = make_idesc(kTileM, two ? p.mma_n - n1 : 16);
       int stage = 0;
       bool aborted = false;
       int it = 0;
       for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
-        const int slot = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
+        const int slot = it % S::kAccBufs;
+        const uint32_t use = (uint32_t)(it / S::kAccBufs);
         // lane 0 decides for the warp
         bool ab = aborted || *reinterpret_cast<volatile int*>(&ctl.abort_flag) != 0;
         if (!ab && lane == 0) ab = !mbar_wait(&ctl.tmem_empty[slot], (use & 1u) ^ 1u, &ctl.abort_flag, p.status);
         aborted = __shfl_sync(0xffffffffu, ab ? 1 : 0, 0) != 0;
-        const uint32_t d_tmem = tmem_base + (uint32_t)(slot * kMaxTileN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(slot * S::kTileNMax);
         for (int ks = 0; ks < p.KB; ++ks) {
           named_bar_sync(1 + stage, kGroupThreads + 32);
           if (lane == 0) {
             if (!aborted) {
               tc_fence_after();
-              const uint32_t a_tmem = tmem_base + kTmemACol + (uint32_t)stage * kTmemAStageCols;
-              const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * kStageBytes);
+              const uint32_t a_tmem = tmem_base + S::kTmemACol + (uint32_t)stage * kTmemAStageCols;
+              const uint64_t b_desc = smem_desc_sw128(stage_base + (uint32_t)stage * S::kStageBytes);
 #pragma unroll
               for (int kk = 0; kk < kKStep / 16; ++kk) {
                 // 16 fp16 along K: 8 TMEM columns of A, 32 bytes inside B's swizzle atom
                 mma_f16_ta(d_tmem, a_tmem + (uint32_t)(kk * 8), b_desc + (uint64_t)(kk * 2), idesc,
                            (ks | kk) != 0 ? 1u : 0u);
+                if (two)  // rows n1 ..: 8-row swizzle atoms of 1024 bytes further (n1 is a multiple of 16)
+                  mma_f16_ta(d_tmem + (uint32_t)n1, a_tmem + (uint32_t)(kk * 8),
+                             b_desc + (uint64_t)(n1 * 8 + kk * 2), idesc2, (ks | kk) != 0 ? 1u : 0u);
               }
             }
             mma_commit(&ctl.empty[stage]);
@@ -442,11 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PrefillMat& mat = p.mats[mi];
       const float sw = *mat.sw;
       const int N = mat.N;
-      const int slot = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
+      const int slot = it % S::kAccBufs;
+      const uint32_t use = (uint32_t)(it / S::kAccBufs);
       if (!mbar_wait(&ctl.tmem_full[slot], use & 1u, &ctl.abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * kMaxTileN);
+      const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(slot * S::kTileNMax);
       if (p.splits > 1) {
         // Split K (one unit per CTA; the units of a tile are one cluster, rank
         // = K range): this rank's exact partial sums go to its own shared
@@ -611,24 +635,24 @@ __global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, in
 
 namespace {
 
-template <bool SWAP>
+template <bool SWAP, bool BIG>
 cudaError_t configure(const DeviceInfo& dev) {
   static thread_local int configured = -1;
   if (configured != dev.device) {
-    cudaError_t err = cudaFuncSetAttribute(prefill_kernel<SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes + 1024);
+    cudaError_t err = cudaFuncSetAttribute(prefill_kernel<SWAP, BIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Shape<BIG>::kSmemBytes + 1024);
     if (err != cudaSuccess) return err;
     configured = dev.device;
   }
   return cudaSuccess;
 }
 
-template <bool SWAP>
+template <bool BIG>
 cudaLaunchConfig_t launch_config(int grid, int cluster, bool pdl, cudaStream_t stream, cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)kSmemBytes + 1024;
+  cfg.dynamicSmemBytes = (size_t)Shape<BIG>::kSmemBytes + 1024;
   cfg.stream = stream;
   int na = 0;
   if (cluster > 1) {
@@ -650,7 +674,7 @@ cudaLaunchConfig_t launch_config(int grid, int cluster, bool pdl, cudaStream_t s
 
 // Clusters of `size` CTAs of this kernel that fit on the GPU at once (0 on
 // error); cached per device and size.
-template <bool SWAP>
+template <bool SWAP, bool BIG>
 int max_clusters(int size, const DeviceInfo& dev) {
   static thread_local int cache_dev = -1;
   static thread_local int cache[kMaxSplits + 1];
@@ -660,22 +684,22 @@ int max_clusters(int size, const DeviceInfo& dev) {
   }
   if (cache[size] < 0) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<SWAP>(size, size, false, nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<BIG>(size, size, false, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<SWAP>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<SWAP, BIG>, &cfg) != cudaSuccess) n = 0;
     cache[size] = n;
   }
   return cache[size];
 }
 
-template <bool SWAP>
+template <bool SWAP, bool BIG>
 cudaError_t launch_impl(const PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  cudaError_t err = configure<SWAP>(dev);
+  cudaError_t err = configure<SWAP, BIG>(dev);
   if (err != cudaSuccess) return err;
   const int grid = p.splits > 1 ? p.num_tiles : (p.num_tiles < dev.num_sms ? p.num_tiles : dev.num_sms);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_config<SWAP>(grid, p.splits, pdl, stream, attr);
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<SWAP>, p);
+  cudaLaunchConfig_t cfg = launch_config<BIG>(grid, p.splits, pdl, stream, attr);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<SWAP, BIG>, p);
 }
 
 // Split K (into a divisor of the k-block count, at most kMaxSplits: a portable
@@ -705,20 +729,20 @@ int best_split(int64_t tiles, int KB, int num_sms, int64_t* cost_out, const int*
   return best_s;
 }
 
-template <bool SWAP>
+template <bool SWAP, bool BIG>
 cudaError_t launch_split(PrefillParams& p, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  cudaError_t err = configure<SWAP>(dev);
+  cudaError_t err = configure<SWAP, BIG>(dev);
   if (err != cudaSuccess) return err;
   const int KB = p.KB;
   const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
   int clusters[kMaxSplits + 1] = {0};
   if (2 * tiles <= dev.num_sms)
-    for (int sp = 2; sp <= kMaxSplits; ++sp) clusters[sp] = max_clusters<SWAP>(sp, dev);
+    for (int sp = 2; sp <= kMaxSplits; ++sp) clusters[sp] = max_clusters<SWAP, BIG>(sp, dev);
   const int best_s = best_split(tiles, KB, dev.num_sms, nullptr, clusters);
   p.splits = best_s;
   p.KB = KB / best_s;
   p.num_tiles = (int)(tiles * best_s);
-  return launch_impl<SWAP>(p, pdl, dev, stream);
+  return launch_impl<SWAP, BIG>(p, pdl, dev, stream);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -817,25 +841,32 @@ cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, co
   if (p.KB < 0) return cudaErrorNotSupported;
   // Tile width and K split together: the fewest (k-steps of the busiest CTA)
   // x (tile width + 64), the +64 being the activation widening of a k-step.
-  {
-    const int64_t tiles_m = (M + kTileM - 1) / kTileM;
-    int64_t best = -1;
-    p.n_tile = kMaxTileN;
-    for (int nt = kMaxTileN; nt >= 64; nt -= 16) {
-      int64_t ksteps = 0;
-      const int64_t tiles = tiles_m * column_tiles(mats, nmats, nt);
-      const int sp = best_split(tiles, p.KB, dev.num_sms, &ksteps);
-      const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 : 0);
-      if (best < 0 || cost < best) {
-        best = cost;
-        p.n_tile = nt;
-      }
+  // 320-wide single-accumulator tiles only when every CTA has one tile: a
+  // CTA with more would run each tile's epilogue with no MMAs beside it (the
+  // up shape at M = 2048 took 144 us that way against 108).
+  const int64_t tiles_m = (M + kTileM - 1) / kTileM;
+  int64_t best = -1;
+  bool big = false;
+  p.n_tile = kMaxTileN;
+  for (int nt = kMaxTileNBig; nt >= 64; nt -= 16) {
+    int64_t ksteps = 0;
+    const int64_t tiles = tiles_m * column_tiles(mats, nmats, nt);
+    const bool is_big = nt > kMaxTileN;
+    if (is_big && tiles > dev.num_sms) continue;
+    const int sp = best_split(tiles, p.KB, dev.num_sms, &ksteps);
+    const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.n_tile = nt;
+      big = is_big;
     }
   }
   p.mma_n = p.n_tile;
-  p.tiles_m = (int)((M + kTileM - 1) / kTileM);
+  // two MMAs a K slice beyond 256 columns: halves rounded to 16 rows
+  p.mma_n1 = p.n_tile > 256 ? (p.n_tile / 2 + 15) / 16 * 16 : 0;
+  p.tiles_m = (int)tiles_m;
   assign_tiles(p, mats, nmats);
-  return launch_split<false>(p, pdl, dev, stream);
+  return big ? launch_split<false, true>(p, pdl, dev, stream) : launch_split<false, false>(p, pdl, dev, stream);
 }
 
 cudaError_t launch_prefill(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,
@@ -856,7 +887,8 @@ cudaError_t launch_batched_mats(const int8_t* xq, const float* sx, int64_t M, co
   p.mma_n = (int)((M + 15) / 16 * 16);
   p.tiles_m = 1;
   assign_tiles(p, mats, nmats);
-  return launch_split<true>(p, pdl, dev, stream);
+  p.mma_n1 = 0;
+  return launch_split<true, false>(p, pdl, dev, stream);
 }
 
 cudaError_t launch_batched(const int8_t* xq, const float* sx, int64_t M, const uint8_t* packed,

@@ -69,7 +69,8 @@ def prefill_constants():
     assert "for (int f = 0; f < total; ++f) {" in text and "mbar_init(&ctl.raw_full[s], 2);" in text
     # empty[g] serves the k-steps f with f % stages == g: a done ring of `stages` barriers
     return dict(ring=int(_const(text, "kRawStages")), done=stages, stages=stages, groups=stages,
-                gw=int(_const(text, "kGroupWarps")), loaders=2, gate="conv", fill="all")
+                gw=int(_const(text, "kGroupWarps")), loaders=2, gate="conv", fill="all",
+                ring_big=int(_const(text, "kRawStagesBig")))
 
 
 class MBar:
@@ -204,8 +205,12 @@ def consts():
 
 
 @pytest.mark.parametrize("total", list(range(1, 21)) + [48, 83])
-def test_prefill_protocol_completes_and_phases_match(total):
+@pytest.mark.parametrize("big", [False, True])
+def test_prefill_protocol_completes_and_phases_match(total, big):
+    """Both raw-ring depths: 192-wide tiles and the 320-wide single-accumulator tiles."""
     c = prefill_constants()
+    if big:
+        c = dict(c, ring=c["ring_big"])
     for seed in range(6):
         simulate(c, total, seed)
         simulate(c, total, 3000 + seed, abort_at=random.Random(seed).randint(1, 300))
