@@ -616,19 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.splits > 1) cluster_sync_all();
 }
 
-// After a split-K batched launch y holds acc (exact integers): y = acc / (sx * sw).
-__global__ void __launch_bounds__(256) batched_rescale(float* __restrict__ y, int32_t* __restrict__ acc,
-                                                       const float* __restrict__ sx, const float* __restrict__ sw,
-                                                       int64_t M, int64_t N) {
-  pdl_release_dependents();
-  pdl_wait_primary();
-  const float w = *sw;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M * N; i += (int64_t)gridDim.x * blockDim.x) {
-    const float a = y[i];
-    y[i] = __fdiv_rn(a, __fmul_rn(sx[i / N], w));
-    if (acc) acc[i] = __float2int_rn(a);
-  }
-}
 
 
 }  // namespace
@@ -816,22 +803,6 @@ void assign_tiles(PrefillParams& p, const DecodeMatrix* mats, int nmats) {
 
 }  // namespace
 
-// After a split-K launch y holds the exact integer sums: y = y / (sx * sw) in
-// place (and acc = y when acc is not NULL), launched as a dependent kernel.
-cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float* sw, int64_t M, int64_t N,
-                           const DeviceInfo& dev, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  const int64_t blocks = (M * N + 255) / 256;
-  cfg.gridDim = dim3((unsigned)(blocks < 4 * (int64_t)dev.num_sms ? blocks : 4 * (int64_t)dev.num_sms), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, batched_rescale, y, acc, sx, sw, M, N);
-}
 
 // The matrices share xq and K; one launch covers all of their tiles.
 cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,

@@ -94,7 +94,10 @@ static_assert(kSmemBytes + 1024 <= 232448, "shared memory per CTA");
 static_assert((kRing & (kRing - 1)) == 0 && kRing % kLoadWarps == 0, "ring indexing");
 static_assert((kDoneRing & (kDoneRing - 1)) == 0 && kDoneRing > kWStages && kDoneRing >= kRing,
               "a kstep_done barrier is reused only after its waiters are past");
-static_assert(kWStages + 1 <= 16, "named barriers 1 .. kWStages");
+constexpr int kEpiBar = 1 + kWStages;              // the epilogue warps' named barrier
+constexpr int kMaxSplits = 8;                      // K ranges of a tile: a portable cluster
+static_assert(kEpiBar < 16, "named barriers 1 .. kWStages, kEpiBar");
+static_assert(kSmemBytes >= kMaxTok * kRows * 4, "split-K partial sums fit over the ring");
 
 struct WideParams {
   const uint8_t* xw;      // widened tokens (layout above)
@@ -119,6 +122,7 @@ struct WideCtl {
   unsigned long long acc_full[kAccBufs];
   unsigned long long acc_empty[kAccBufs];
   unsigned long long mma_done;
+  unsigned long long parts_ready;           // split K: one arrival per other rank of the cluster
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -173,6 +177,7 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
       mbar_init(&ctl.acc_empty[s], kEpiWarps);
     }
     mbar_init(&ctl.mma_done, 1);
+    mbar_init(&ctl.parts_ready, p.splits > 1 ? (uint32_t)(p.splits - 1) : 1u);
     ctl.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -180,6 +185,8 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Split K: the ranks' barriers are initialised before another rank arrives on them.
+  if (p.splits > 1) cluster_sync_all();
   const uint32_t tmem_base = ctl.tmem_base;
 
   // The workspace is written by the pre-pass just before on the stream.
@@ -363,19 +370,30 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
       const int n = n0 + row;
       const bool n_ok = n < p.N;
       const uint32_t t_row = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(aslot * kMaxTok);
+      if (p.splits > 1) {
+        // Split K (one unit per CTA; the units of a tile are one cluster, rank
+        // = K range): this rank's exact partial sums go to its own shared
+        // memory, [token column][128 weight rows], over the ring, which no
+        // copy or MMA uses any more.
+        for (int c = 0; c < rows_t; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(t_row + (uint32_t)c, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(ring_base + (uint32_t)(((c + j) * kRows + row) * 4)),
+                         "r"(__float2int_rn(__uint_as_float(r[j])))
+                         : "memory");
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.acc_empty[aslot]);
+        break;
+      }
       for (int c = 0; c < rows_t; c += 16) {
         uint32_t r[16];
         tmem_ld16(t_row + (uint32_t)c, r);
         if (!n_ok) continue;
         float* yc = p.y + (int64_t)(m0 + c) * p.N + n;
-        if (p.splits > 1) {
-          // partial sums over this unit's K range: integer-valued fp32
-          // additions below 2^24 are exact in any order
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (m0 + c + j < p.M) atomicAdd(yc + (int64_t)j * p.N, __uint_as_float(r[j]));
-          continue;
-        }
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           if (m0 + c + j < p.M) yc[(int64_t)j * p.N] = __fdiv_rn(__uint_as_float(r[j]), dw[c + j]);  // r[j]: an exact integer
@@ -390,6 +408,51 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.acc_empty[aslot]);  // one arrival per warp
     }
+    if (p.splits > 1 && (int)blockIdx.x < p.num_units) {
+      // Every rank adds one share of the tile's token columns over all ranks'
+      // partial sums (distributed shared memory) and writes those outputs.
+      // Every rank takes part whatever happened before, so the others' waits
+      // end early.
+      named_bar_sync(kEpiBar, kEpiWarps * 32);  // this rank's partial sums are written
+      const uint32_t rank = cluster_rank();
+      if (warp == 0 && lane < p.splits && lane != (int)rank)
+        mbar_arrive_remote(map_shared(smem_u32(&ctl.parts_ready), (uint32_t)lane));
+      if (mbar_wait_cluster(&ctl.parts_ready, 0u, &ctl.abort_flag, p.status) &&
+          *reinterpret_cast<volatile int*>(&ctl.abort_flag) == 0) {
+        int n0, m0, kb0, rows_t;
+        unit_coords(p, blockIdx.x, n0, m0, kb0, rows_t);
+        const int c0 = (int)rank * rows_t / p.splits, c1 = ((int)rank + 1) * rows_t / p.splits;
+        // item: token column c, weight rows l4 .. l4 + 3
+        for (int it2 = c0 * (kRows / 4) + warp * 32 + lane; it2 < c1 * (kRows / 4); it2 += kEpiWarps * 32) {
+          const int c = it2 / (kRows / 4), l4 = (it2 % (kRows / 4)) * 4;
+          const uint32_t off = ring_base + (uint32_t)((c * kRows + l4) * 4);
+          uint4 part[kMaxSplits];
+#pragma unroll
+          for (int k = 0; k < kMaxSplits; ++k)  // every load issued before the sum
+            part[k] = k < p.splits ? ld_cluster_v4(map_shared(off, (uint32_t)k)) : make_uint4(0u, 0u, 0u, 0u);
+          uint4 tot = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int k = 0; k < kMaxSplits; ++k) {
+            tot.x += part[k].x;
+            tot.y += part[k].y;
+            tot.z += part[k].z;
+            tot.w += part[k].w;
+          }
+          const int t = m0 + c;
+          if (t >= p.M) continue;
+          const float den = __fmul_rn(p.sx[t], sw);
+          const int av[4] = {(int)tot.x, (int)tot.y, (int)tot.z, (int)tot.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = n0 + l4 + e;
+            if (n < p.N) {
+              p.y[(int64_t)t * p.N + n] = __fdiv_rn(__int2float_rn(av[e]), den);
+              if (p.acc) p.acc[(int64_t)t * p.N + n] = av[e];
+            }
+          }
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -398,21 +461,60 @@ __global__ void __maxnreg__(80) wide_kernel(const __grid_constant__ WideParams p
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // Split K: every rank has read the others' shared memory before any exits.
+  if (p.splits > 1) cluster_sync_all();
 }
 
-cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t stream,
-                       void** args) {
+cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, bool pdl, int cluster, cudaStream_t stream,
+                                 cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  int na = 0;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = (unsigned)na;
+  return cfg;
+}
+
+cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t stream,
+                       void** args, int cluster = 1) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(grid, block, smem, pdl, cluster, stream, attr);
   return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+// Clusters of `size` WIDE CTAs that fit on the GPU at once (0 on error);
+// cached per device and size.  Needs the kernel's shared-memory attribute set.
+int max_clusters(int size, const DeviceInfo& dev) {
+  static thread_local int cache_dev = -1;
+  static thread_local int cache[kMaxSplits + 1];
+  if (cache_dev != dev.device) {
+    for (int i = 0; i <= kMaxSplits; ++i) cache[i] = -1;
+    cache_dev = dev.device;
+  }
+  if (cache[size] < 0) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg =
+        launch_config(dim3((unsigned)size, 1, 1), dim3(kThreads, 1, 1), (size_t)kSmemBytes + 1024, false, size, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, wide_kernel, &cfg) != cudaSuccess) n = 0;
+    cache[size] = n;
+  }
+  return cache[size];
 }
 
 // Estimated time of one k-step of a 128 x tn tile, in ns: the MMAs take about
@@ -425,9 +527,6 @@ int64_t kstep_ns(int tn) {
 
 }  // namespace
 
-// Defined with the 128-token-tile kernel (prefill.cu).
-cudaError_t launch_rescale(float* y, int32_t* acc, const float* sx, const float* sw, int64_t M, int64_t N,
-                           const DeviceInfo& dev, cudaStream_t stream);
 
 size_t wide_workspace_bytes(int64_t M, int64_t K) {
   return (size_t)((M + 15) / 16 * 16) * (size_t)K * 2u;
@@ -453,20 +552,31 @@ cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint
   p.Mp = (int)Mp;
   p.N = (int)N;
   p.tiles_w = (int)((N + kRows - 1) / kRows);
+  {
+    const size_t smem = (size_t)kSmemBytes + 1024;
+    static thread_local int configured = -1;
+    if (configured != dev.device) {
+      cudaError_t err = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      configured = dev.device;
+    }
+  }
   // Token-tile width and K split: the least estimated time of the busiest
-  // CTA.  A split (only while the tiles fill at most half of the SMs: it costs
-  // a zeroing pass, one atomic add per output and unit, and a rescale pass)
-  // divides K into at most 16 ranges of at least 8 k-steps.
+  // CTA.  A split (only while the tiles fill at most half of the SMs) divides
+  // K into at most 8 ranges of at least 8 k-steps; the ranges of a tile run as
+  // one thread-block cluster that adds the partial sums through distributed
+  // shared memory (~1 us), so all of the launch's clusters must fit at once.
   {
     int64_t best = -1;
     for (int tn = 16; tn <= kMaxTok; tn += 16) {
       const int tn_eff = tn < Mp ? tn : (int)Mp;
       const int64_t tiles = (int64_t)p.tiles_w * ((Mp + tn_eff - 1) / tn_eff);
-      for (int sp = 1; sp <= 16 && sp <= KB; ++sp) {
+      for (int sp = 1; sp <= kMaxSplits && sp <= KB; ++sp) {
         if (KB % sp) continue;
         if (sp > 1 && (2 * tiles > dev.num_sms || tiles * sp > dev.num_sms || KB / sp < 8)) continue;
+        if (sp > 1 && tiles > max_clusters(sp, dev)) continue;
         const int64_t waves = (tiles * sp + dev.num_sms - 1) / dev.num_sms;
-        const int64_t cost = waves * (KB / sp) * kstep_ns(tn_eff) + (sp > 1 ? 3000 + M * N / 500 : 0);
+        const int64_t cost = waves * (KB / sp) * kstep_ns(tn_eff) + (sp > 1 ? 1000 : 0);
         if (best < 0 || cost < best) {
           best = cost;
           p.tn = tn_eff;
@@ -481,34 +591,18 @@ cudaError_t launch_wide(const int8_t* xq, const float* sx, int64_t M, const uint
   p.num_units = p.tiles_w * p.tiles_t * p.splits;
 
   cudaError_t err;
-  if (p.splits > 1) {
-    err = cudaMemsetAsync(y, 0, (size_t)M * (size_t)N * sizeof(float), stream);
-    if (err != cudaSuccess) return err;
-  }
   if (widen) {
     const int m32 = (int)M, mp32 = (int)Mp, k32 = (int)K;
     uint4* xw = static_cast<uint4*>(workspace);
     void* args[] = {(void*)&xq, (void*)&m32, (void*)&mp32, (void*)&k32, (void*)&xw};
     err = launch_pdl((const void*)widen_tokens, dim3((unsigned)((Mp * 8 + 255) / 256), (unsigned)KB, 1), dim3(256, 1, 1),
-                     0, pdl && p.splits == 1, stream, args);
+                     0, pdl, stream, args);
     if (err != cudaSuccess) return err;
   }
-  {
-    const size_t smem = (size_t)kSmemBytes + 1024;
-    static thread_local int configured = -1;
-    if (configured != dev.device) {
-      err = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (err != cudaSuccess) return err;
-      configured = dev.device;
-    }
-    const int grid = p.num_units < dev.num_sms ? p.num_units : dev.num_sms;
-    void* args[] = {(void*)&p};
-    err = launch_pdl((const void*)wide_kernel, dim3((unsigned)grid, 1, 1), dim3(kThreads, 1, 1), smem, true, stream,
-                     args);
-    if (err != cudaSuccess) return err;
-  }
-  if (p.splits > 1) return launch_rescale(y, acc, sx, sw, M, N, dev, stream);
-  return cudaSuccess;
+  const int grid = p.splits > 1 ? p.num_units : (p.num_units < dev.num_sms ? p.num_units : dev.num_sms);
+  void* args[] = {(void*)&p};
+  return launch_pdl((const void*)wide_kernel, dim3((unsigned)grid, 1, 1), dim3(kThreads, 1, 1),
+                    (size_t)kSmemBytes + 1024, true, stream, args, p.splits);
 }
 
 }  // namespace bitlinear

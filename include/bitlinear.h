@@ -252,8 +252,7 @@ typedef struct bitlinear_weight {
  * Otherwise it runs bitlinear_quant_act, then one launch per kernel that
  * bitlinear_forward's AUTO rule picks for some matrix: the matrices given to
  * the same kernel (decode, batched or 128-token-tile) share one grid, whose
- * tiles span all of them.  (A split-K launch adds, per matrix, the clearing
- * of y before it and the rescale pass after it.)
+ * tiles span all of them.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream).

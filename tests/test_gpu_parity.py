@@ -85,8 +85,9 @@ def test_forward_ws_auto_and_pdl(M, N, K):
     (bl.ALGO_WIDE, 130, 300, 2048), (bl.ALGO_WIDE, 200, 1000, 4096), (bl.ALGO_WIDE, 1, 1, 32768),
 ])
 def test_split_k(algo, M, N, K):
-    """Few tiles: K is split over CTAs, partial sums are added into y and
-    rescaled in place; acc and y must match the oracle as without a split."""
+    """Few tiles: K is split over the CTAs of a thread-block cluster, whose
+    partial sums are added through distributed shared memory; acc and y must
+    match the oracle as without a split."""
     W = synth.weight(N, K, 110 + K)
     x = synth.activations(M, K, 111 + M)
     full_parity(W, x, algo=algo)
