@@ -72,15 +72,15 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 constexpr int64_t kDecodeMaxK = 65536;
 // Tensor-core kernel: the fp32 accumulator is exact while 127 * K < 2^24.
 constexpr int64_t kPrefillMaxK = 131072;
-// AUTO, from timings on GB300 over the BitNet-3B shapes (hot L2):
+// AUTO, from timings on GB300 over the BitNet-3B shapes (back-to-back calls):
 //  * the decode kernel (dp4a; its work grows with every token) for a few
-//    tokens: M <= 4 always, M <= 16 unless K is long (K >= 8192: M <= 8) or the
-//    output very wide (N >= 32768, e.g. a 50000-row LM head);
+//    tokens: M <= 4 always, M <= 8, and M <= 16 when K < 8192, unless the
+//    output is very wide (N >= 32768, e.g. a 50000-row LM head);
 //  * the batched tensor-core kernel (weight rows on the MMA's M side, all
-//    tokens in one tile) for narrow outputs (N <= 4096) up to M = 128 -- from
-//    M = 64 when K >= 8192;
+//    tokens in one tile) for outputs up to 8192 rows up to M = 128;
 //  * the tensor-core kernel with 128-token tiles otherwise (both tensor-core
-//    kernels split K over CTAs when their tiles fill less than half the SMs).
+//    kernels split K over the CTAs of a cluster when their tiles fill less
+//    than half the SMs).
 int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;

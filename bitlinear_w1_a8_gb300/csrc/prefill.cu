@@ -20,7 +20,7 @@
 //               tiles of every fourth k-step to fp16 in stage g -- the
 //               activations into TMEM (one row per lane), the weights into
 //               shared memory in the 128-byte-swizzled K-major layout
-//   warps 20-23 loaders of an 8-deep shared-memory ring: per k-step one
+//   warps 20-23 loaders of the shared-memory ring: per k-step one
 //               thread of warp 20 issues the TMA tensor copy of the 128 x 64
 //               int8 activation tile (64-byte swizzle) and one thread of warp
 //               21 the bulk copy of the packed codes, both completing on the
@@ -35,13 +35,17 @@
 // The MMA takes A (activations) from TMEM and B (weights) from shared memory,
 // so the widened activations never pass through shared memory, whose
 // bandwidth the weight stores, the raw copies and the MMA's reads of B share.
-// Shared memory holds kStages fp16 weight stages (n_tile x 64) and kRawStages
+// Shared memory holds kStages fp16 weight stages (n_tile x 64) and a ring of
 // raw stages (A 128x64 int8, B n_tile x 16 B packed); TMEM holds two
 // 128 x n_tile fp32 accumulators, so the epilogue of one tile overlaps the
-// MMAs of the next, and kStages 128 x 64 fp16 activation stages.  Every mbarrier wait is bounded by the
-// global timer: on timeout the kernel records BITLINEAR_ERR_TIMEOUT in the
-// status word, every role leaves its loop, the MMA warp waits (bounded) for
-// its own MMAs, frees TMEM and the kernel returns.
+// MMAs of the next, and kStages 128 x 64 fp16 activation stages -- or, with
+// 320-wide tiles (one per CTA), one accumulator (Shape<true>).  When tiles are
+// few, K is split over the CTAs of a thread-block cluster that add their
+// partial sums through distributed shared memory.  Every mbarrier wait is
+// bounded by the global timer: on timeout the kernel records
+// BITLINEAR_ERR_TIMEOUT in the status word, every role leaves its loop, the
+// MMA warp waits (bounded) for its own MMAs, frees TMEM and the kernel
+// returns.
 #include <cuda.h>
 
 #include "common.cuh"

@@ -44,7 +44,9 @@
 //                tcgen05.commit per k-step, which frees both the ring slot and
 //                the TMEM weight stage
 // TMEM: two 128 x 192 fp32 accumulators (the epilogue of one tile overlaps
-// the MMAs of the next) and four 128 x 64 fp16 weight stages.  Every wait is
+// the MMAs of the next) and four 128 x 64 fp16 weight stages.  When tiles are
+// few, K is split over the CTAs of a thread-block cluster that add their
+// partial sums through distributed shared memory.  Every wait is
 // bounded by the global timer; on timeout the kernel records BITLINEAR_ERR_TIMEOUT, every role
 // leaves its loop, the loaders wait (bounded) for their own copies, the MMA
 // warp for its own MMAs, and TMEM is freed before the kernel returns.
