@@ -157,11 +157,12 @@ __device__ __forceinline__ int chunk_dot(const uint4 wv, const int4* xp) {
 // CTA-dependent rotation (by whole 128-byte lines) so that the CTAs' first
 // requests spread over the L2 slices.  Writes the int8 codes to xs (shared)
 // and, when out is not NULL, to out (global); adds sum_k xq[k] to *sumx.
-// Returns sx.  Every thread of the block calls it.
-template <int NJ>
-__device__ float quantize_row_regs(const float* __restrict__ x, const float* __restrict__ mul, bool norm,
-                                   const float4* gs, double eps, int K, unsigned long long* wbar, int* status,
-                                   RowQuantScratch& sc, int8_t* xs, int8_t* out, int* sumx) {
+// Returns sx; *have_g is false when gamma's copy (completing on gbar) did not
+// arrive in time.  Every thread of the block calls it.
+template <int NJ, bool NORM>
+__device__ float quantize_row_regs(const float* __restrict__ x, const float* __restrict__ mul,
+                                   const float4* gs, double eps, int K, unsigned long long* gbar, int* status,
+                                   RowQuantScratch& sc, int8_t* xs, int8_t* out, int* sumx, bool* have_g) {
   const int t = threadIdx.x, lane = t & 31;
   const int K4 = K >> 2;
   const int rot = (int)((blockIdx.x * 296u) % (unsigned)K4) & ~7;
@@ -178,6 +179,9 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
     idx[j] = ok[j] ? i : 0;
     h[j] = ok[j] ? ld_cg4(x4 + idx[j]) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // 1/K for the RMSNorm scale, by the thread that takes it, while the row's
+  // loads are in flight (parked in shared memory, not a register)
+  if (NORM && t == 0) sc.rcp_k = __drcp_rn((double)K);
   if (mul) {
     // h = (r*r)*u with r = max(g, 0): the ReLU^2 gating of the FFN
     const float4* u4 = reinterpret_cast<const float4*>(mul);
@@ -192,7 +196,7 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
       r = fmaxf(h[j].w, 0.0f); h[j].w = __fmul_rn(__fmul_rn(r, r), u.w);
     }
   }
-  if (norm) {
+  if constexpr (NORM) {
     // RMSNorm: inv = fp32(1 / sqrt(S/K + eps)) in fp64 from the exact sum S
     int e = 0;
 #pragma unroll
@@ -229,15 +233,12 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
     }
     // one thread takes the fp64 steps (fp64 is slow on this GPU), the block
     // picks the result up after a barrier
-    if (t == 0) {
-      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-    }
+    if (t == 0) sc.inv = rms_inv(S, K, sc.rcp_k, eps);
     __syncthreads();
     const float inv = sc.inv;
-    // gamma came with the weights (bounded wait; on timeout the status word
-    // says so and the outputs are not written)
-    bar_wait(wbar, status);
+    // gamma's own copy, issued ahead of the weights (bounded wait; on timeout
+    // the status word says so and the outputs are not written)
+    *have_g = bar_wait(gbar, status);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       if (!ok[j]) continue;
@@ -286,12 +287,13 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
 // Dynamic shared memory: the CTA's weight planes at 0 (plane kb holds rows
 // r0 .. r1-1 as R consecutive 16-byte chunks), xs[MT][K] int8 activations at
 // off_xs, red[MT][R] int32 row sums at off_red, (fused RMSNorm) gamma at off_gs.
-template <int MT, bool FUSED, int NJ>
+template <int MT, bool FUSED, bool NORM, int NJ>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ int sumx[MT];
   __shared__ float den[MT];
   __shared__ __align__(8) unsigned long long wbar;
+  __shared__ __align__(8) unsigned long long gbar;
   __shared__ RowQuantScratch qsc;
 
   const int t = threadIdx.x, lane = t & 31;
@@ -312,21 +314,25 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   int8_t* xs = reinterpret_cast<int8_t*>(dsmem + p.off_xs);
   int* red = reinterpret_cast<int*>(dsmem + p.off_red);
   float4* gs = reinterpret_cast<float4*>(dsmem + p.off_gs);
-  const bool norm = FUSED && p.gamma != nullptr;
+  constexpr bool norm = FUSED && NORM;  // the host launches NORM exactly when gamma is given
 
-  // The weights (and gamma): bulk copies into shared memory, issued before the
-  // dependency wait by warp 0 (the byte count is registered first).
+  // The weights and gamma: bulk copies into shared memory, issued before the
+  // dependency wait by warp 0 (the byte counts are registered first).  Gamma
+  // goes first and completes on its own barrier: the row's scaling needs it
+  // long before the last weight plane lands.
   if (t < 32) {
     if (t == 0) {
       bar_init(&wbar, 1);
+      if (norm) bar_init(&gbar, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      expect_tx(&wbar, (uint32_t)R * (uint32_t)KB * 16u + (norm ? (uint32_t)K * 4u : 0u));
+      if (norm) expect_tx(&gbar, (uint32_t)K * 4u);
+      expect_tx(&wbar, (uint32_t)R * (uint32_t)KB * 16u);
     }
     __syncwarp();
+    if (norm && lane == 0) bulk_copy(gs, p.gamma, (uint32_t)K * 4u, &gbar);
     const uint4* src = reinterpret_cast<const uint4*>(mat.packed) + r0;
     for (int kb = lane; kb < KB; kb += 32)
       bulk_copy((void*)(wsm + (size_t)kb * R), src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
-    if (norm && lane == 0) bulk_copy(gs, p.gamma, (uint32_t)K * 4u, &wbar);
   }
   // Let the next kernel on the stream start (and request its own weights) on
   // the SM resources this grid leaves free; it still waits for our results.
@@ -336,11 +342,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
 
   pdl_wait_primary();
 
+  bool have_g = true;
   if constexpr (FUSED) {
-    const float s = quantize_row_regs<NJ>(p.x + (int64_t)m0 * K, p.mul ? p.mul + (int64_t)m0 * K : nullptr, norm,
-                                          gs, p.eps, K, &wbar, p.status, qsc, xs,
+    const float s = quantize_row_regs<NJ, norm>(p.x + (int64_t)m0 * K, p.mul ? p.mul + (int64_t)m0 * K : nullptr,
+                                                gs, p.eps, K, &gbar, p.status, qsc, xs,
                                           c == 0 ? p.xq_out + (p.xq_out ? (int64_t)m0 * K : 0) : nullptr,
-                                          &sumx[0]);
+                                          &sumx[0], &have_g);
     if (t == 0) {
       den[0] = __fmul_rn(s, *mat.sw);
       if (c == 0 && p.sx_out) p.sx_out[m0] = s;
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
 
   // The weights have landed (bounded wait; on timeout the status word says so
   // and the outputs are not written).
-  const bool have_w = bar_wait(&wbar, p.status);
+  const bool have_w = bar_wait(&wbar, p.status) && have_g;
   if (have_w) {
     // chunk cc = kb * R + r, dealt out flat: thread t takes t, t + 512, ...
     const int4* xs4 = reinterpret_cast<const int4*>(xs);
@@ -429,20 +436,20 @@ size_t decode_front_bytes(int64_t K, int mt, int rows_max, bool norm) {
   return (b + 127) & ~(size_t)127;
 }
 
-template <int MT, bool FUSED, int NJ>
-cudaError_t launch_mt(DecodeParams p, int grid_x, bool norm, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+template <int MT, bool FUSED, bool NORM, int NJ>
+cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   const size_t wbytes = ((size_t)p.rows_max * p.KB * 16 + 127) & ~(size_t)127;
   p.off_xs = (uint32_t)wbytes;
   p.off_red = (uint32_t)(((wbytes + (size_t)MT * p.K) + 15) & ~(size_t)15);
   p.off_gs = (uint32_t)((p.off_red + (size_t)MT * p.rows_max * 4 + 15) & ~(size_t)15);
-  const size_t smem = wbytes + decode_front_bytes(p.K, MT, p.rows_max, norm);
+  const size_t smem = wbytes + decode_front_bytes(p.K, MT, p.rows_max, NORM);
   const size_t limit = dev.smem_optin - sizeof(RowQuantScratch) - 1024;
   if (smem > limit) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     static thread_local int configured_device = -1;
     if (configured_device != dev.device) {
       cudaError_t err =
-          cudaFuncSetAttribute(decode_kernel<MT, FUSED, NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+          cudaFuncSetAttribute(decode_kernel<MT, FUSED, NORM, NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
       if (err != cudaSuccess) return err;
       configured_device = dev.device;
     }
@@ -457,7 +464,7 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool norm, bool pdl, const Dev
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NJ>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NORM, NJ>, p);
 }
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
@@ -502,6 +509,23 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   return total;
 }
 
+// The fused launch for nj float4 elements of the row per thread; the RMSNorm
+// prologue is a template argument, so the kernel without it carries none of
+// its code.
+template <bool NORM>
+cudaError_t launch_fused(const DecodeParams& p, int grid, int nj, bool pdl, const DeviceInfo& dev,
+                         cudaStream_t stream) {
+  switch (nj) {
+    case 1: return launch_mt<1, true, NORM, 1>(p, grid, pdl, dev, stream);
+    case 2: return launch_mt<1, true, NORM, 2>(p, grid, pdl, dev, stream);
+    case 3: return launch_mt<1, true, NORM, 3>(p, grid, pdl, dev, stream);
+    case 4: return launch_mt<1, true, NORM, 4>(p, grid, pdl, dev, stream);
+    case 5: return launch_mt<1, true, NORM, 5>(p, grid, pdl, dev, stream);
+    case 6: return launch_mt<1, true, NORM, 6>(p, grid, pdl, dev, stream);
+    default: return launch_mt<1, true, NORM, kMaxNJ>(p, grid, pdl, dev, stream);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
@@ -516,10 +540,10 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   while (mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
   const int grid = plan_decode(p, mats, nmats, K, mt, false, dev);
   switch (mt) {
-    case 1: return launch_mt<1, false, 1>(p, grid, false, pdl, dev, stream);
-    case 2: return launch_mt<2, false, 1>(p, grid, false, pdl, dev, stream);
-    case 4: return launch_mt<4, false, 1>(p, grid, false, pdl, dev, stream);
-    default: return launch_mt<8, false, 1>(p, grid, false, pdl, dev, stream);
+    case 1: return launch_mt<1, false, false, 1>(p, grid, pdl, dev, stream);
+    case 2: return launch_mt<2, false, false, 1>(p, grid, pdl, dev, stream);
+    case 4: return launch_mt<4, false, false, 1>(p, grid, pdl, dev, stream);
+    default: return launch_mt<8, false, false, 1>(p, grid, pdl, dev, stream);
   }
 }
 
@@ -540,15 +564,7 @@ cudaError_t launch_decode_fused(const float* x, const float* mul, const float* g
   const int grid = plan_decode(p, mats, nmats, K, 1, norm, dev);
   // float4 elements of the row a thread owns (the kernel keeps them in registers)
   const int nj = (int)((K / 4 + kDecThreads - 1) / kDecThreads);
-  switch (nj) {
-    case 1: return launch_mt<1, true, 1>(p, grid, norm, pdl, dev, stream);
-    case 2: return launch_mt<1, true, 2>(p, grid, norm, pdl, dev, stream);
-    case 3: return launch_mt<1, true, 3>(p, grid, norm, pdl, dev, stream);
-    case 4: return launch_mt<1, true, 4>(p, grid, norm, pdl, dev, stream);
-    case 5: return launch_mt<1, true, 5>(p, grid, norm, pdl, dev, stream);
-    case 6: return launch_mt<1, true, 6>(p, grid, norm, pdl, dev, stream);
-    default: return launch_mt<1, true, kMaxNJ>(p, grid, norm, pdl, dev, stream);
-  }
+  return norm ? launch_fused<true>(p, grid, nj, pdl, dev, stream) : launch_fused<false>(p, grid, nj, pdl, dev, stream);
 }
 
 cudaError_t launch_wait_selftest(int64_t limit_ns, const DeviceInfo& dev, cudaStream_t stream) {

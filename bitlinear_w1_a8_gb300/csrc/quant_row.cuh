@@ -24,6 +24,7 @@ struct RowQuantScratch {
   unsigned long long win[3][2][32];  // per-warp window sums (low, high 64 bits)
   float red[32];
   int ired[32];
+  double rcp_k;  // RN(1/K), set early by thread 0 for the RMSNorm scale
   float inv;
 };
 
@@ -228,6 +229,30 @@ __device__ __forceinline__ float4 gated4(const float4* __restrict__ xr, const fl
   return h;
 }
 
+// The RMSNorm scale inv = fp32(1 / sqrt(S/K + eps)), exactly as the fp64 chain
+// RN32(RN64(1 / RN64(sqrt(RN64(RN64(S / K) + eps))))) gives it, for one
+// thread.  That chain (two fp64 divisions and a square root, long dependent
+// FMA chains on this GPU) takes ~1900 cycles; instead y = rsqrt(S * rcp_k +
+// eps) (rcp_k = RN(1/K); rsqrt of a double is within 1 ulp) is within ~7 fp64
+// ulps of the chain's fp64 result (each of the chain's four roundings and the
+// estimate's three steps moves the value by at most 2^-53 relative, halved
+// through the square root), so when y lies more than 32 fp64 ulps from every
+// fp32 rounding boundary (the midpoints between fp32 values, where the low 29
+// bits of its fraction are 2^28) both round to the same fp32 value.  Only in
+// the other case (about 1 in 10^7) and outside [1e-60, 1e60] the chain itself
+// runs.  ~875 cycles.
+__device__ __forceinline__ float rms_inv(double S, int K, double rcp_k, double eps) {
+  const double v = __dadd_rn(__dmul_rn(S, rcp_k), eps);
+  if (v > 1e-60 && v < 1e60) {
+    const double y = rsqrt(v);
+    const long long low = (long long)(__double_as_longlong(y) & ((1ll << 29) - 1));
+    const long long d = low - (1ll << 28);
+    if (d > 32 || d < -32) return __double2float_rn(y);
+  }
+  const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
+  return __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
+}
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
@@ -259,12 +284,12 @@ static __device__ __forceinline__ float quantize_row(const float* __restrict__ x
   float amax = 0.0f;
   if (norm) {
     for (int i = threadIdx.x; i < K4; i += blockDim.x) hs[i] = gated4(xr, ur, i);
+    // 1/K for the RMSNorm scale, by the thread that takes it (off the path of
+    // the row's loads and sums; parked in shared memory, not a register)
+    if (threadIdx.x == 0) sc.rcp_k = __drcp_rn((double)K);
     __syncthreads();
     const double S = block_sq_sum_exact(hs, K4, sc);
-    if (threadIdx.x == 0) {
-      const double ms = __dadd_rn(__ddiv_rn(S, (double)K), eps);
-      sc.inv = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(ms)));
-    }
+    if (threadIdx.x == 0) sc.inv = rms_inv(S, K, sc.rcp_k, eps);
     __syncthreads();
     const float inv = sc.inv;
     const float4* g4 = reinterpret_cast<const float4*>(gamma);

@@ -85,6 +85,33 @@ def max_rel_err(y_gpu, y_ref):
 Y_RTOL = 1e-5
 
 
+# Rows of one repeated value c (signs varied), K = 2560: the RMSNorm sum is
+# exactly K*c^2, so the scale's fp64 chain is 1/sqrt(c^2 + eps) rounded at
+# each step, and these c put that fp64 value within ~32 fp64 ulps of an fp32
+# rounding boundary (the midpoint between two fp32 values), where a faster
+# estimate of the scale would round the other way if it were trusted.  Each
+# entry: eps, the fp32 bit pattern of c, the signed distance of the chain's
+# low 29 fraction bits from 2^28 (in fp64 ulps).  With gamma drawn by
+# ``RMS_BOUNDARY_GAMMA`` a one-ulp change of the fp32 scale changes sx for
+# every entry.
+RMS_BOUNDARY_K = 2560
+RMS_BOUNDARY_ROWS = [
+    (0.0, 0x3DFC3237, 16), (0.0, 0x3DD0AC19, 20), (0.0, 0x3D869913, 30), (0.0, 0x3D87CC45, 30),
+    (1e-6, 0x3DD4EE44, 14), (1e-6, 0x3E814329, 1), (1e-6, 0x4138A38E, 4), (1e-6, 0x40978642, -37),
+]
+
+
+def rms_boundary_gamma():
+    return np.random.default_rng(91).uniform(0.5, 1.5, RMS_BOUNDARY_K).astype(np.float32)
+
+
+def rms_boundary_rows(eps):
+    """The rows of ``RMS_BOUNDARY_ROWS`` for one eps: (M, K) float32."""
+    cs = [np.array([b], dtype=np.uint32).view(np.float32)[0] for e, b, _ in RMS_BOUNDARY_ROWS if e == eps]
+    sign = np.where(np.random.default_rng(93).random((len(cs), RMS_BOUNDARY_K)) < 0.5, -1.0, 1.0)
+    return (np.array(cs, dtype=np.float32)[:, None] * sign).astype(np.float32)
+
+
 def full_parity(W, x, mul=None, gamma=None, eps=1e-6, algo=bl.ALGO_AUTO, flags=0, workspace=False):
     """Every stage of the library against the oracle on the same inputs."""
     N, K = W.shape

@@ -13,7 +13,7 @@ import bitlinear_w1_a8_gb300 as bl
 import oracle
 from bitlinear_w1_a8_gb300 import synth
 from harness import (Y_RTOL, check_canary, full_parity, gpu_act_quant, gpu_forward, gpu_quantize_weights,
-                     guarded, max_rel_err)
+                     guarded, max_rel_err, rms_boundary_gamma, rms_boundary_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -156,6 +156,32 @@ def test_rmsnorm_exact_sum_paths(kind, M):
         assert bl.bitlinear_device_status() == 0
         np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
         np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6])
+def test_rmsnorm_scale_at_fp32_boundary(eps):
+    """Rows whose RMSNorm scale lies within a few fp64 ulps of an fp32 rounding
+    boundary: the kernels' fast estimate of the scale must step aside there and
+    give the exact chain's value (act_quant kernel, the M = 1 fused launch and
+    the fused few-token launch)."""
+    x = torch.from_numpy(rms_boundary_rows(eps))
+    gamma = torch.from_numpy(rms_boundary_gamma())
+    M, K = x.shape
+    xq_o, sx_o = oracle.act_quant(x.numpy(), gamma=gamma.numpy(), eps=eps)
+    xq_g, sx_g, _ = gpu_act_quant(x, None, gamma, eps)
+    np.testing.assert_array_equal(sx_g, sx_o)
+    np.testing.assert_array_equal(xq_g, xq_o)
+    W = synth.weight(256, K, 94)
+    _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+    for rows in [slice(m, m + 1) for m in range(M)] + [slice(0, M)]:
+        n = rows.stop - rows.start
+        y = torch.empty(n, 256, device="cuda")
+        xq = torch.zeros(n, K, dtype=torch.int8, device="cuda")
+        sx = torch.zeros(n, dtype=torch.float32, device="cuda")
+        bl.bitlinear_linear(x[rows].cuda(), [(packed_d, sw_d, y)], xq, sx, rms_weight=gamma.cuda(), rms_eps=eps)
+        assert bl.bitlinear_device_status() == 0
+        np.testing.assert_array_equal(sx.cpu().numpy(), sx_o[rows])
+        np.testing.assert_array_equal(xq.cpu().numpy(), xq_o[rows])
 
 
 def test_edge_values():

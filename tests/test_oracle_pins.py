@@ -421,3 +421,32 @@ def test_argmax_rows_are_independent_one_hot():
     for m, h in enumerate(hot):
         y[m, h] = 1.0
     assert list(oracle.argmax(y)) == hot
+
+
+# --- RMSNorm scale next to an fp32 rounding boundary ----------------------------
+# The boundary rows (one repeated value c per row, K = 2560) must sit where
+# their table says: the fp64 chain 1/sqrt(c^2 + eps), each step rounded, lies
+# that many fp64 ulps from the midpoint between two fp32 values.  numpy's fp64
+# sqrt and division round correctly, so this recomputes the chain exactly.
+def test_rms_boundary_rows_sit_on_the_boundary():
+    from harness import RMS_BOUNDARY_ROWS
+    for eps, bits, dist in RMS_BOUNDARY_ROWS:
+        c = float(np.array([bits], dtype=np.uint32).view(np.float32)[0])
+        y = np.float64(1.0) / np.sqrt(np.float64(c) * np.float64(c) + np.float64(eps))
+        low = int(np.array([y]).view(np.uint64)[0]) & ((1 << 29) - 1)
+        assert low - (1 << 28) == dist, (eps, hex(bits))
+
+
+# With eps = 0 the chain collapses (sqrt(c^2) = |c| exactly), so the oracle's
+# normalised row is a closed form: inv = fp32(fp64(1/|c|)), h = fp32(fp32(x*inv)*gamma).
+def test_rms_boundary_rows_closed_form():
+    from harness import RMS_BOUNDARY_ROWS, rms_boundary_gamma, rms_boundary_rows
+    gamma = rms_boundary_gamma()
+    x = rms_boundary_rows(0.0)
+    _, sx, h = oracle.act_quant(x, gamma=gamma, eps=0.0, return_h=True)
+    for m in range(x.shape[0]):
+        c = abs(float(x[m, 0]))
+        inv = np.float32(np.float64(1.0) / np.float64(c))
+        want = ((x[m] * inv).astype(np.float32) * gamma).astype(np.float32)
+        np.testing.assert_array_equal(h[m], want)
+        assert sx[m] == np.float32(127.0) / np.abs(want).max()
