@@ -206,7 +206,21 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
                 max(fp32_exponent(__float_as_uint(h[j].z)), fp32_exponent(__float_as_uint(h[j].w))));
     const int emax = block_max_exponent(e, sc);
     double S = 0.0;
-    if (emax != 0) {
+    bool done = emax == 0;
+    if (!done) {
+      U128 W = {0, 0};
+      int far = 0;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (!ok[j]) continue;
+        sq_window0_add(__float_as_uint(h[j].x), emax, W, far);
+        sq_window0_add(__float_as_uint(h[j].y), emax, W, far);
+        sq_window0_add(__float_as_uint(h[j].z), emax, W, far);
+        sq_window0_add(__float_as_uint(h[j].w), emax, W, far);
+      }
+      done = block_window0(W, far, emax, sc, &S);
+    }
+    if (!done) {
       U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
       int slow = 0;
 #pragma unroll
@@ -339,6 +353,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   pdl_release_dependents();
   if (t < MT) sumx[t] = 0;
   for (int i = t; i < MT * R; i += kDecThreads) red[i] = 0;
+  // The weight scale, like the weights, does not come from the kernel before
+  // (the rule of FLAG_PDL): its load is off the path after the wait.
+  const float sw = t < MT ? *mat.sw : 0.0f;
 
   pdl_wait_primary();
 
@@ -349,7 +366,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
                                           c == 0 ? p.xq_out + (p.xq_out ? (int64_t)m0 * K : 0) : nullptr,
                                           &sumx[0], &have_g);
     if (t == 0) {
-      den[0] = __fmul_rn(s, *mat.sw);
+      den[0] = __fmul_rn(s, sw);
       if (c == 0 && p.sx_out) p.sx_out[m0] = s;
     }
     __syncthreads();
@@ -358,7 +375,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K);
     int4* dst = reinterpret_cast<int4*>(xs);
     for (int i = t; i < mcount * (K >> 4); i += kDecThreads) cp_async16_row(dst + i, src + i);
-    if (t < MT) den[t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], *mat.sw) : 1.0f;
+    if (t < MT) den[t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw) : 1.0f;
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // Row sums of the activations (the bias of the biased codes c = Wq + 1);

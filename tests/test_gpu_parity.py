@@ -122,12 +122,13 @@ def test_prologues(M, K):
         np.testing.assert_array_equal(xq_g, xq_o)
 
 
-@pytest.mark.parametrize("kind", ["wide", "tiny_only", "zeros_and_subnormals"])
+@pytest.mark.parametrize("kind", ["wide", "tiny_only", "zeros_and_subnormals", "window_edge", "just_below"])
 @pytest.mark.parametrize("M", [1, 3])
 def test_rmsnorm_exact_sum_paths(kind, M):
-    """The RMSNorm sum of squares takes a 128-bit fast path when every value is
-    within 2^32 of the row maximum and an exponent-bucket path otherwise; both
-    must give the oracle's codes (act_quant kernel and the fused M = 1 launch)."""
+    """The RMSNorm sum of squares takes one 128-bit window when every value is
+    within 2^31 of the row maximum's binade, three windows down to 2^96 below
+    it, and an exponent-bucket path otherwise; all must give the oracle's
+    codes (act_quant kernel and the fused M = 1 launch)."""
     K = 2048
     g = torch.Generator().manual_seed(90 + M)
     x = torch.randn(M, K, generator=g)
@@ -137,10 +138,17 @@ def test_rmsnorm_exact_sum_paths(kind, M):
         x[:, 9] = 1e3
     elif kind == "tiny_only":     # every value tiny, within the window of each other
         x = x * 1e-30
-    else:                         # exact zeros and fp32 subnormals next to normal values
+    elif kind == "zeros_and_subnormals":  # exact zeros and fp32 subnormals next to normal values
         x[:, ::7] = 0.0
         x[:, 3] = 1e-40
         x[:, 11] = -7e-42
+    elif kind == "window_edge":   # the row maximum in [2^10, 2^11), values in [2^-21, 2^-20): one window
+        x[:, 3] = 1536.0
+        x[:, 10] = float(np.float32(1.9999999) * np.float32(2.0 ** -21))
+        x[:, 11] = -float(np.float32(1.0000001) * np.float32(2.0 ** -21))
+    else:                         # one value a binade further down, [2^-22, 2^-21): three windows
+        x[:, 3] = 1536.0
+        x[:, 10] = 1.5 * 2.0 ** -22
     gamma = synth.uniform((K,), 0.5, 1.5, 91)
     xq_o, sx_o = oracle.act_quant(x.numpy(), gamma=gamma.numpy(), eps=1e-6)
     xq_g, sx_g, _ = gpu_act_quant(x, None, gamma, 1e-6)
