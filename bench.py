@@ -3,9 +3,9 @@
 
 Headline workload (BitNet-3B decode, M = 1 token): one step is the FFN's three
 BitLinear calls of one token, exactly as a decode step runs them:
-    act_quant(x_a [1, 2560])                   (shared by gate and up)
-    forward(gate 2560 -> 10240), forward(up 2560 -> 10240)
-    act_quant(x_b [1, 10240])
+    act_quant(x [1, 2560])                     (shared by gate and up)
+    g = forward(gate 2560 -> 10240), u = forward(up 2560 -> 10240)
+    act_quant(h = ReLU^2(g) * u [1, 10240])
     forward(down 10240 -> 2560)
 i.e. 19,660,800 packed weight bytes per step.  Inputs are seeded synthetic
 tensors (weights ~ N(0, 0.02), activations ~ N(0, 1) with 1% of channels x20).
@@ -13,7 +13,11 @@ Each step uses the next of R copies of the packed weights (R * 19.7 MB > 4x
 L2), so every weight byte comes from HBM.  Steps run as CUDA graphs with
 programmatic dependent launch between kernels.  By default a step is two
 bitlinear_linear calls (act_quant fused into the decode kernel; gate and up in
-one launch); --separate times the five separate act_quant / forward calls.
+one launch whose epilogue writes h); --separate times the five separate
+act_quant / forward calls.  The oracle arms (CPU baseline, --impl reference)
+quantise a synthetic [1, 10240] row pair with the same gating prologue for the
+down call: the oracle's work does not depend on the values, and a step split
+over host cores by output rows cannot chain the full h.
 
 Metric: packed-weight GB/s (1e9 B/s) over the whole job.  One JSON line on
 rank 0.  `--impl reference` times the CPU oracle on the same workload instead.
@@ -73,7 +77,8 @@ def workload_inputs():
     W_down_shape = synth.weight(D, F, s["W_down_shape"])   # down: 10240 -> 2560
     x_a = synth.activations(1, D, s["x"], outlier_seed=s["outliers"])
     x_b = synth.activations(1, F, s["x"], outlier_seed=s["outliers"])
-    return dict(D=D, F=F, W_up_shape=W_up_shape, W_down_shape=W_down_shape, x_a=x_a, x_b=x_b)
+    u_b = synth.activations(1, F, s["x"] + 1)   # the oracle arms' stand-in for the up output
+    return dict(D=D, F=F, W_up_shape=W_up_shape, W_down_shape=W_down_shape, x_a=x_a, x_b=x_b, u_b=u_b)
 
 
 def step_packed_bytes(D, F):
@@ -97,7 +102,7 @@ class OracleStep:
         self.nd = max(1, int(D * row_fraction))
         self.p_u = oracle.pack(Wq_u[: self.nu])
         self.p_d = oracle.pack(Wq_d[: self.nd])
-        self.x_a, self.x_b = inp["x_a"].numpy(), inp["x_b"].numpy()
+        self.x_a, self.x_b, self.u_b = inp["x_a"].numpy(), inp["x_b"].numpy(), inp["u_b"].numpy()
         self.D, self.F = D, F
         self.bytes = 2 * self.p_u.size + self.p_d.size
 
@@ -106,7 +111,7 @@ class OracleStep:
         xq, sx = o.act_quant(self.x_a)
         o.forward(xq, sx, self.p_u, self.sw_u, self.nu, self.D)   # gate
         o.forward(xq, sx, self.p_u, self.sw_u, self.nu, self.D)   # up
-        xq, sx = o.act_quant(self.x_b)
+        xq, sx = o.act_quant(self.x_b, mul=self.u_b)           # the gating prologue
         o.forward(xq, sx, self.p_d, self.sw_d, self.nd, self.F)   # down
 
 
@@ -128,13 +133,13 @@ def _oracle_worker(jobs, results):
         kind, payload = job
         t0 = time.perf_counter()
         if kind == "decode":
-            x_a, x_b, parts, steps = payload
+            x_a, x_b, u_b, parts, steps = payload
             for _ in range(steps):
                 xq, sx = oracle.act_quant(x_a)
                 for p_u, sw_u, nu, D in parts["up"]:
                     oracle.forward(xq, sx, p_u, sw_u, nu, D)   # gate
                     oracle.forward(xq, sx, p_u, sw_u, nu, D)   # up
-                xq, sx = oracle.act_quant(x_b)
+                xq, sx = oracle.act_quant(x_b, mul=u_b)
                 for p_d, sw_d, nd, F in parts["down"]:
                     oracle.forward(xq, sx, p_d, sw_d, nd, F)
         else:  # "prefill": a slice of output columns for a block of token rows
@@ -158,7 +163,7 @@ class OraclePool:
         nu = max(1, int(F * row_fraction))
         nd = max(1, int(D * row_fraction))
         self.bytes = 2 * oracle.packed_bytes(nu, D) + oracle.packed_bytes(nd, F)
-        self.x_a, self.x_b = inp["x_a"].numpy(), inp["x_b"].numpy()
+        self.x_a, self.x_b, self.u_b = inp["x_a"].numpy(), inp["x_b"].numpy(), inp["u_b"].numpy()
         self.parts = []
         for c in range(self.cores):
             u0, u1 = nu * c // self.cores, nu * (c + 1) // self.cores
@@ -195,7 +200,7 @@ class OraclePool:
         """Wall seconds for `steps` decode steps over all cores."""
         t0 = time.perf_counter()
         for c in range(self.cores):
-            self.jobs[c].put(("decode", (self.x_a, self.x_b, self.parts[c], steps)))
+            self.jobs[c].put(("decode", (self.x_a, self.x_b, self.u_b, self.parts[c], steps)))
         self._gather(self.cores)
         return time.perf_counter() - t0
 
@@ -649,8 +654,9 @@ def measure_weight_set(bl, dev, stream, dist, Ms=(1, 8, 32, 64), reps=10):
 def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
     """BitNet-1.3B FFN sub-block (dim 2048, ffn 8192): RMSNorm -> act_quant ->
     gate || up -> ReLU^2(gate) * up -> sub-norm -> act_quant -> down, as two
-    bitlinear_linear_ws calls (the prologues fused; with a workspace, so the
-    WIDE kernel takes the matrices its AUTO rule gives it), seeded as in the
+    bitlinear_linear_ws calls (the prologues fused, and at M <= 8 the gating in
+    the gate || up launch's epilogue; with a workspace, so the WIDE kernel
+    takes the matrices its AUTO rule gives it), seeded as in the
     parity test; one CUDA graph of `reps` sub-blocks over rotating weight
     copies (> 4x L2)."""
     import torch
@@ -681,12 +687,16 @@ def measure_ffn_1b3(bl, dev, stream, dist, Ms=(1, 512), reps=50):
         yd = torch.empty(M, D, dtype=torch.float32, device=dev)
         fws = torch.empty(bl.bitlinear_forward_workspace(M, F), dtype=torch.uint8, device=dev)
 
+        # At decode sizes the gate || up launch writes ReLU^2(gate) * up from its
+        # epilogue; above them the down call's prologue applies the gating.
+        gated = M <= 8
+
         def block(i, st):
             (g, sg), (u, su), (d, sd) = sets[i % copies]
             bl.bitlinear_linear_ws(x, [(g, sg, yg), (u, su, yu)], xq, sx, fws, rms_weight=gamma, rms_eps=1e-6,
-                                   flags=bl.FLAG_PDL, stream=st)
-            bl.bitlinear_linear_ws(yg, [(d, sd, yd)], hq, hsx, fws, mul=yu, rms_weight=gamma_sub, rms_eps=1e-6,
-                                   flags=bl.FLAG_PDL, stream=st)
+                                   flags=bl.FLAG_PDL | (bl.FLAG_GATED if gated else 0), stream=st)
+            bl.bitlinear_linear_ws(yg, [(d, sd, yd)], hq, hsx, fws, mul=None if gated else yu,
+                                   rms_weight=gamma_sub, rms_eps=1e-6, flags=bl.FLAG_PDL, stream=st)
 
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -747,7 +757,6 @@ def run_ours(args, rank, world, local_rank):
         slots.append((pu.clone(), pu.clone(), pd.clone()))
     sw_u, sw_d = sw[0:1], sw[1:2]
     x_a = inp["x_a"].to(dev)
-    x_b = inp["x_b"].to(dev)
     xq_a = torch.empty(1, D, dtype=torch.int8, device=dev)
     xq_b = torch.empty(1, F, dtype=torch.int8, device=dev)
     sx_a = torch.empty(1, dtype=torch.float32, device=dev)
@@ -757,20 +766,24 @@ def run_ours(args, rank, world, local_rank):
     y_d = torch.empty(1, D, dtype=torch.float32, device=dev)
     flags = 0 if args.no_pdl else bl.FLAG_PDL
 
+    # One step is the FFN of one decode token: down(ReLU^2(gate(x)) * up(x)).
     def step_separate(i, stream):
-        # act_quant and forward as separate calls (5 launches per step)
+        # act_quant and forward as separate calls (5 launches per step); the
+        # second act_quant applies the gating prologue to the gate and up outputs
         g, u, d = slots[i % R]
         bl.bitlinear_quant_act(x_a, xq_a, sx_a, stream=stream)
         bl.bitlinear_forward_ex(xq_a, sx_a, g, sw_u, F, y_g, flags=flags, stream=stream)
         bl.bitlinear_forward_ex(xq_a, sx_a, u, sw_u, F, y_u, flags=flags, stream=stream)
-        bl.bitlinear_quant_act(x_b, xq_b, sx_b, stream=stream)
+        bl.bitlinear_quant_act(y_g, xq_b, sx_b, mul=y_u, stream=stream)
         bl.bitlinear_forward_ex(xq_b, sx_b, d, sw_d, D, y_d, flags=flags, stream=stream)
 
     def step_linear(i, stream):
-        # bitlinear_linear: act_quant fused into the decode kernel, gate || up in one launch
+        # bitlinear_linear: act_quant fused into the decode kernel; gate || up in
+        # one launch whose epilogue writes h = ReLU^2(gate) * up; down on h
         g, u, d = slots[i % R]
-        bl.bitlinear_linear(x_a, [(g, sw_u, y_g), (u, sw_u, y_u)], xq_a, sx_a, flags=flags, stream=stream)
-        bl.bitlinear_linear(x_b, [(d, sw_d, y_d)], xq_b, sx_b, flags=flags, stream=stream)
+        bl.bitlinear_linear(x_a, [(g, sw_u, y_g), (u, sw_u, y_u)], xq_a, sx_a, flags=flags | bl.FLAG_GATED,
+                            stream=stream)
+        bl.bitlinear_linear(y_g, [(d, sw_d, y_d)], xq_b, sx_b, flags=flags, stream=stream)
 
     step = step_separate if args.separate else step_linear
     kernels_per_step = 5 if args.separate else 2
@@ -894,27 +907,30 @@ def run_ours(args, rank, world, local_rank):
 
     # End to end through the public API: pinned host inputs in, host outputs out
     # (one copy each way: the step's inputs and outputs sit in one buffer each).
+    # The step's input is the token row x, its result the down projection.
     e2e_steps = max(10, min(args.e2e_steps, args.steps))
-    h_in = torch.cat([inp["x_a"].reshape(-1), inp["x_b"].reshape(-1)]).pin_memory()
-    h_out = torch.empty(2 * F + D, dtype=torch.float32).pin_memory()
-    d_in = torch.empty(D + F, dtype=torch.float32, device=dev)
-    d_out = torch.empty(2 * F + D, dtype=torch.float32, device=dev)
-    e_xa, e_xb = d_in[:D].view(1, D), d_in[D:].view(1, F)
-    e_yg, e_yu, e_yd = d_out[:F].view(1, F), d_out[F:2 * F].view(1, F), d_out[2 * F:].view(1, D)
+    h_in = inp["x_a"].reshape(-1).clone().pin_memory()
+    h_out = torch.empty(D, dtype=torch.float32).pin_memory()
+    e_xa = torch.empty(1, D, dtype=torch.float32, device=dev)
+    e_yg = torch.empty(1, F, dtype=torch.float32, device=dev)
+    e_yu = torch.empty(1, F, dtype=torch.float32, device=dev)
+    e_yd = torch.empty(1, D, dtype=torch.float32, device=dev)
+    e2e_h2d, e2e_d2h = 4 * D, 4 * D
 
     def e2e_step(i):
         g, u, d = slots[i % R]
-        d_in.copy_(h_in, non_blocking=True)
+        e_xa.view(-1).copy_(h_in, non_blocking=True)
         if args.separate:
             bl.bitlinear_quant_act(e_xa, xq_a, sx_a, stream=stream)
             bl.bitlinear_forward(xq_a, sx_a, g, sw_u, F, e_yg, stream=stream)
             bl.bitlinear_forward(xq_a, sx_a, u, sw_u, F, e_yu, stream=stream)
-            bl.bitlinear_quant_act(e_xb, xq_b, sx_b, stream=stream)
+            bl.bitlinear_quant_act(e_yg, xq_b, sx_b, mul=e_yu, stream=stream)
             bl.bitlinear_forward(xq_b, sx_b, d, sw_d, D, e_yd, stream=stream)
         else:
-            bl.bitlinear_linear(e_xa, [(g, sw_u, e_yg), (u, sw_u, e_yu)], xq_a, sx_a, stream=stream)
-            bl.bitlinear_linear(e_xb, [(d, sw_d, e_yd)], xq_b, sx_b, stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
+            bl.bitlinear_linear(e_xa, [(g, sw_u, e_yg), (u, sw_u, e_yu)], xq_a, sx_a, flags=bl.FLAG_GATED,
+                                stream=stream)
+            bl.bitlinear_linear(e_yg, [(d, sw_d, e_yd)], xq_b, sx_b, stream=stream)
+        h_out.copy_(e_yd.view(-1), non_blocking=True)
 
     with torch.cuda.stream(stream):
         for i in range(20):
@@ -976,7 +992,8 @@ def run_ours(args, rank, world, local_rank):
                       f"{R * per_step / 1e6:.0f} MB > 4x {L2_BYTES / 1e6:.0f} MB",
                 "cuda_graph": True, "pdl": not args.no_pdl, "parallelism": f"replicas{world}",
                 "path": ("separate bitlinear_quant_act + bitlinear_forward_ex calls" if args.separate else
-                         "bitlinear_linear: gate||up in one launch, down in one launch, act_quant fused"),
+                         "bitlinear_linear: gate||up in one launch (its epilogue writes ReLU^2(gate)*up), "
+                         "down on that product in one launch, act_quant fused in both"),
             },
             "other_path": alt_line,
             "roofline": {
@@ -991,12 +1008,12 @@ def run_ours(args, rank, world, local_rank):
                 "timing": f"{fwd_launches} back-to-back launches in CUDA graphs (PDL), CUDA events",
             },
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
-                    "h2d_bytes_per_step": 4 * (D + F), "d2h_bytes_per_step": 4 * (2 * F + D),
+                    "h2d_bytes_per_step": e2e_h2d, "d2h_bytes_per_step": e2e_d2h,
                     "steps": e2e_steps,
                     "note": "eager calls through the Python binding of the C ABI; pinned host "
                             "inputs copied in and outputs copied out every step"},
             "e2e_graph": {"value": round(e2e_graph_value, 3), "unit": UNIT,
-                          "h2d_bytes_per_step": 4 * (D + F), "d2h_bytes_per_step": 4 * (2 * F + D),
+                          "h2d_bytes_per_step": e2e_h2d, "d2h_bytes_per_step": e2e_d2h,
                           "steps": R * e2e_reps,
                           "note": f"the same calls captured once into a CUDA graph of {R} steps and "
                                   "replayed: the host copies in and out still run every step"},

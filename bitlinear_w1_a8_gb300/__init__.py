@@ -30,6 +30,7 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libbitlinear.so")
 
 ALGO_AUTO, ALGO_DECODE, ALGO_PREFILL, ALGO_BATCHED, ALGO_WIDE = 0, 1, 2, 3, 4
 FLAG_PDL = 1
+FLAG_GATED = 2  # bitlinear_linear: gate, up pair; the first output receives (r * r) * up, r = max(gate, 0)
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_SHAPE", -3: "ERR_ALIGN", -4: "ERR_UNSUPPORTED",
           -5: "ERR_CUDA", -6: "ERR_TIMEOUT", -7: "ERR_WORKSPACE"}

@@ -243,7 +243,7 @@ bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M,
     return from_cuda(launch_batched(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
   if (use == BITLINEAR_ALGO_DECODE) {
     const DecodeMatrix mat = {packed, w_scale, N, y, acc};
-    return from_cuda(launch_decode(xq, x_scale, M, &mat, 1, K, pdl, dev, s));
+    return from_cuda(launch_decode(xq, x_scale, M, &mat, 1, K, false, pdl, dev, s));
   }
   return from_cuda(launch_prefill(xq, x_scale, M, packed, w_scale, N, K, y, acc, pdl, dev, s));
 }
@@ -283,7 +283,9 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
   if (num_weights < 1 || num_weights > kMaxDecodeMats) return BITLINEAR_ERR_SHAPE;
   if (M < 0 || M > kMaxDim || K <= 0 || K % 64 != 0 || K > 32768) return BITLINEAR_ERR_SHAPE;
   if (rms_weight && !(rms_eps >= 0.0)) return BITLINEAR_ERR_SHAPE;
-  if (flags & ~BITLINEAR_FLAG_PDL) return BITLINEAR_ERR_UNSUPPORTED;
+  if (flags & ~(BITLINEAR_FLAG_PDL | BITLINEAR_FLAG_GATED)) return BITLINEAR_ERR_UNSUPPORTED;
+  const bool gated = (flags & BITLINEAR_FLAG_GATED) != 0;
+  if (gated && (num_weights != 2 || weights[0].N != weights[1].N)) return BITLINEAR_ERR_SHAPE;
   for (int i = 0; i < num_weights; ++i) {
     const bitlinear_weight& w = weights[i];
     if (!w.packed || !w.w_scale) return BITLINEAR_ERR_NULL;
@@ -314,8 +316,8 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
     mats[i] = DecodeMatrix{weights[i].packed, weights[i].w_scale, weights[i].N, weights[i].y, weights[i].acc};
   if (M == 1 && K <= kFusedMaxK) {
     // one launch: every CTA quantises the token itself
-    return from_cuda(launch_decode_fused(x, mul, rms_weight, rms_eps, K, mats, num_weights, xq, x_scale, pdl,
-                                         dev, s));
+    return from_cuda(launch_decode_fused(x, mul, rms_weight, rms_eps, K, mats, num_weights, xq, x_scale, gated,
+                                         pdl, dev, s));
   }
   cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s, pdl);
   if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
@@ -339,9 +341,12 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
       pre[npre++] = mats[i];
     }
   }
+  // A gated pair that the decode kernel takes is gated in its epilogue; on
+  // any other kernel one elementwise launch follows.
+  const bool gate_in_decode = gated && ndec == 2;
   if (ndec > 0) {
     if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
-    err = launch_decode(xq, x_scale, M, dec, ndec, K, pdl, dev, s);
+    err = launch_decode(xq, x_scale, M, dec, ndec, K, gate_in_decode, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   if (nbat > 0) {
@@ -350,6 +355,10 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
   }
   if (npre > 0) {
     err = launch_prefill_mats(xq, x_scale, M, pre, npre, K, pdl, dev, s);
+    if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
+  }
+  if (gated && !gate_in_decode) {
+    err = launch_gate(mats[0].y, mats[1].y, M * mats[0].N, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }
   return BITLINEAR_OK;

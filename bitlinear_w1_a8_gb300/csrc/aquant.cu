@@ -27,6 +27,33 @@ act_quant_kernel(const float* __restrict__ x, const float* __restrict__ mul, int
   if (threadIdx.x == 0) sx[row] = s;
 }
 
+// The FFN gating of a gate / up pair: y0 = (r * r) * y1 with r = max(y0, 0),
+// the fp32 steps of the gating prologue.
+constexpr int kGateThreads = 256;
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(float* __restrict__ y0, const float* __restrict__ y1,
+                                                            int64_t n) {
+  pdl_release_dependents();
+  pdl_wait_primary();  // y0 and y1 come from the kernel before
+  const int64_t n4 = n >> 2;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  float4* g4 = reinterpret_cast<float4*>(y0);
+  const float4* u4 = reinterpret_cast<const float4*>(y1);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 g = g4[i];
+    const float4 u = u4[i];
+    float r;
+    r = fmaxf(g.x, 0.0f); g.x = __fmul_rn(__fmul_rn(r, r), u.x);
+    r = fmaxf(g.y, 0.0f); g.y = __fmul_rn(__fmul_rn(r, r), u.y);
+    r = fmaxf(g.z, 0.0f); g.z = __fmul_rn(__fmul_rn(r, r), u.z);
+    r = fmaxf(g.w, 0.0f); g.w = __fmul_rn(__fmul_rn(r, r), u.w);
+    g4[i] = g;
+  }
+  for (int64_t i = (n4 << 2) + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float r = fmaxf(y0[i], 0.0f);
+    y0[i] = __fmul_rn(__fmul_rn(r, r), y1[i]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_t K,
@@ -55,6 +82,23 @@ cudaError_t launch_act_quant(const float* x, const float* mul, int64_t M, int64_
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, mul, (int)K, gamma, eps, xq, sx);
+}
+
+cudaError_t launch_gate(float* y0, const float* y1, int64_t n, bool pdl, const DeviceInfo& dev,
+                        cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t want = ((n >> 2) + kGateThreads - 1) / kGateThreads;
+  const int64_t cap = (int64_t)dev.num_sms * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(want < 1 ? 1 : (want < cap ? want : cap)), 1, 1);
+  cfg.blockDim = dim3(kGateThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gate_kernel, y0, y1, n);
 }
 
 }  // namespace bitlinear

@@ -188,13 +188,21 @@ struct DecodeMatrix {
   int32_t* acc;
 };
 
+// gated: nmats == 2 with equal N (gate, up); every CTA takes the same rows of
+// both and mats[0].y receives (r * r) * u with r = max(gate, 0), mats[1].y u.
 cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
-                          int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+                          int64_t K, bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
 // M = 1 only: every CTA quantises x (with the optional gating / RMSNorm
 // prologue) itself; CTA 0 writes xq_out / sx_out when they are not NULL.
 cudaError_t launch_decode_fused(const float* x, const float* mul, const float* gamma, double eps, int64_t K,
-                                const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out, bool pdl,
-                                const DeviceInfo& dev, cudaStream_t stream);
+                                const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out,
+                                bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
+
+// y0[i] = (r * r) * y1[i] with r = max(y0[i], 0) for i < n (the FFN gating of
+// a gate / up pair computed by another kernel); waits for the previous kernel
+// on the stream when launched with programmatic dependent launch.
+cudaError_t launch_gate(float* y0, const float* y1, int64_t n, bool pdl, const DeviceInfo& dev,
+                        cudaStream_t stream);
 
 }  // namespace bitlinear

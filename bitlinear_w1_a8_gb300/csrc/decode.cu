@@ -75,6 +75,10 @@ struct DecodeParams {
   uint32_t off_red; //   int32 row sums,
   uint32_t off_gs;  //   gamma (fused RMSNorm); the weight planes start at 0
   int nmats;
+  // Gated pair (nmats == 2, equal N): every CTA takes rows r0 .. r1 - 1 of
+  // both matrices (gate, then up) and writes mats[0].y = (r * r) * u with
+  // r = max(gate, 0), mats[1].y = u.
+  int gated;
   DecodeMat mats[kMaxDecodeMats];
 };
 
@@ -305,17 +309,18 @@ template <int MT, bool FUSED, bool NORM, int NJ>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ int sumx[MT];
-  __shared__ float den[MT];
+  __shared__ float den[2][MT];  // sx * sw of each token, for mats[mi] and (gated) mats[1]
   __shared__ __align__(8) unsigned long long wbar;
   __shared__ __align__(8) unsigned long long gbar;
   __shared__ RowQuantScratch qsc;
 
   const int t = threadIdx.x, lane = t & 31;
   const int c = blockIdx.x;
+  const bool gated = p.gated != 0;
   int mi = 0;
 #pragma unroll
   for (int i = 1; i < kMaxDecodeMats; ++i)
-    if (i < p.nmats && c >= p.mats[i].g0) mi = i;
+    if (!gated && i < p.nmats && c >= p.mats[i].g0) mi = i;
   const DecodeMat& mat = p.mats[mi];
   const int cl = c - mat.g0;
   const int m0 = blockIdx.y * MT;
@@ -323,6 +328,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   const int r0 = (int)(((int64_t)cl * mat.N) / mat.G);
   const int r1 = (int)(((int64_t)(cl + 1) * mat.N) / mat.G);
   const int R = r1 - r0;
+  const int RR = gated ? 2 * R : R;  // rows held: R of mats[mi], then (gated) the same R of mats[1]
   const int KB = p.KB, K = p.K;
   const uint4* wsm = reinterpret_cast<const uint4*>(dsmem);
   int8_t* xs = reinterpret_cast<int8_t*>(dsmem + p.off_xs);
@@ -340,22 +346,28 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
       if (norm) bar_init(&gbar, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       if (norm) expect_tx(&gbar, (uint32_t)K * 4u);
-      expect_tx(&wbar, (uint32_t)R * (uint32_t)KB * 16u);
+      expect_tx(&wbar, (uint32_t)RR * (uint32_t)KB * 16u);
     }
     __syncwarp();
     if (norm && lane == 0) bulk_copy(gs, p.gamma, (uint32_t)K * 4u, &gbar);
     const uint4* src = reinterpret_cast<const uint4*>(mat.packed) + r0;
     for (int kb = lane; kb < KB; kb += 32)
-      bulk_copy((void*)(wsm + (size_t)kb * R), src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
+      bulk_copy((void*)(wsm + (size_t)kb * RR), src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
+    if (gated) {
+      const uint4* src1 = reinterpret_cast<const uint4*>(p.mats[1].packed) + r0;
+      for (int kb = lane; kb < KB; kb += 32)
+        bulk_copy((void*)(wsm + (size_t)kb * RR + R), src1 + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
+    }
   }
   // Let the next kernel on the stream start (and request its own weights) on
   // the SM resources this grid leaves free; it still waits for our results.
   pdl_release_dependents();
   if (t < MT) sumx[t] = 0;
-  for (int i = t; i < MT * R; i += kDecThreads) red[i] = 0;
-  // The weight scale, like the weights, does not come from the kernel before
-  // (the rule of FLAG_PDL): its load is off the path after the wait.
+  for (int i = t; i < MT * RR; i += kDecThreads) red[i] = 0;
+  // The weight scales, like the weights, do not come from the kernel before
+  // (the rule of FLAG_PDL): their loads are off the path after the wait.
   const float sw = t < MT ? *mat.sw : 0.0f;
+  const float sw1 = gated && t < MT ? *p.mats[1].sw : 0.0f;
 
   pdl_wait_primary();
 
@@ -366,7 +378,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
                                           c == 0 ? p.xq_out + (p.xq_out ? (int64_t)m0 * K : 0) : nullptr,
                                           &sumx[0], &have_g);
     if (t == 0) {
-      den[0] = __fmul_rn(s, sw);
+      den[0][0] = __fmul_rn(s, sw);
+      den[1][0] = __fmul_rn(s, sw1);
       if (c == 0 && p.sx_out) p.sx_out[m0] = s;
     }
     __syncthreads();
@@ -375,7 +388,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K);
     int4* dst = reinterpret_cast<int4*>(xs);
     for (int i = t; i < mcount * (K >> 4); i += kDecThreads) cp_async16_row(dst + i, src + i);
-    if (t < MT) den[t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw) : 1.0f;
+    if (t < MT) {
+      den[0][t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw) : 1.0f;
+      den[1][t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw1) : 1.0f;
+    }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // Row sums of the activations (the bias of the biased codes c = Wq + 1);
@@ -403,19 +419,19 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     // chunk cc = kb * R + r, dealt out flat: thread t takes t, t + 512, ...
     const int4* xs4 = reinterpret_cast<const int4*>(xs);
     const int K16 = K >> 4;
-    const int C = R * KB;
-    const int dq = kDecThreads / R, dr = kDecThreads - dq * R;
-    int kb = t / R, r = t - kb * R;
+    const int C = RR * KB;
+    const int dq = kDecThreads / RR, dr = kDecThreads - dq * RR;
+    int kb = t / RR, r = t - kb * RR;
 #pragma unroll 2
     for (int cc = t; cc < C; cc += kDecThreads) {
       const uint4 wv = wsm[cc];
 #pragma unroll
       for (int m = 0; m < MT; ++m)
-        if (m < mcount) atomicAdd(&red[m * R + r], chunk_dot(wv, xs4 + m * K16 + kb * 4));
+        if (m < mcount) atomicAdd(&red[m * RR + r], chunk_dot(wv, xs4 + m * K16 + kb * 4));
       kb += dq;
       r += dr;
-      if (r >= R) {
-        r -= R;
+      if (r >= RR) {
+        r -= RR;
         ++kb;
       }
     }
@@ -424,10 +440,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   if (have_w) {
     for (int i = t; i < mcount * R; i += kDecThreads) {
       const int m = i / R, rr = i - m * R;
-      const int n = r0 + rr;
-      const int total = red[i] - sumx[m];
-      mat.y[(int64_t)(m0 + m) * mat.N + n] = __fdiv_rn(__int2float_rn(total), den[m]);
-      if (mat.acc) mat.acc[(int64_t)(m0 + m) * mat.N + n] = total;
+      const int64_t o = (int64_t)(m0 + m) * mat.N + r0 + rr;
+      const int total = red[m * RR + rr] - sumx[m];
+      const float y0 = __fdiv_rn(__int2float_rn(total), den[0][m]);
+      if (mat.acc) mat.acc[o] = total;
+      if (gated) {
+        // the FFN gating, in the same fp32 steps as the activation prologue
+        const int total1 = red[m * RR + R + rr] - sumx[m];
+        const float u = __fdiv_rn(__int2float_rn(total1), den[1][m]);
+        const float rp = fmaxf(y0, 0.0f);
+        mat.y[o] = __fmul_rn(__fmul_rn(rp, rp), u);
+        p.mats[1].y[o] = u;
+        if (p.mats[1].acc) p.mats[1].acc[o] = total1;
+      } else {
+        mat.y[o] = y0;
+      }
     }
   }
 }
@@ -486,30 +513,38 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
 // their rows, with at most kMaxWeightBytes of weights and at most 512 rows a
-// CTA (more CTAs, in further waves, where a matrix needs it).  Returns the
-// total CTA count.
-int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm,
+// CTA (more CTAs, in further waves, where a matrix needs it).  A gated pair
+// (two matrices of equal N) splits as one matrix whose rows weigh double:
+// every CTA holds the same rows of both.  Returns the total CTA count.
+int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm, bool gated,
                 const DeviceInfo& dev) {
   p.K = (int)K;
   p.KB = (int)(K / 64);
   p.nmats = nmats;
+  p.gated = gated ? 1 : 0;
+  const int per = gated ? 2 : 1;  // weight rows a CTA holds per output row
   int64_t all_rows = 0;
-  for (int i = 0; i < nmats; ++i) all_rows += mats[i].N;
-  const int64_t row_bytes = (int64_t)p.KB * 16;
+  for (int i = 0; i < (gated ? 1 : nmats); ++i) all_rows += mats[i].N;
+  const int64_t row_bytes = (int64_t)p.KB * 16 * per;
   // Shared memory left for weights next to the activations, row sums (sized
   // for the 512-row maximum here) and gamma.
   const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 -
                        (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);
   int64_t rows_cap = (room < kMaxWeightBytes ? room : kMaxWeightBytes) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
-  if (rows_cap > kDecThreads) rows_cap = kDecThreads;
+  if (rows_cap * per > kDecThreads) rows_cap = kDecThreads / per;
   int total = 0, rows_max = 1;
   for (int i = 0; i < nmats; ++i) {
     const int64_t N = mats[i].N;
-    int64_t G = (dev.num_sms * N + all_rows / 2) / all_rows;  // this matrix's share of the SMs
-    if (G < 1) G = 1;
-    if ((N + G - 1) / G > rows_cap) G = (N + rows_cap - 1) / rows_cap;
-    if (G > N) G = N;
+    int64_t G;
+    if (gated && i == 1) {
+      G = p.mats[0].G;  // the pair shares one split
+    } else {
+      G = (dev.num_sms * N + all_rows / 2) / all_rows;  // this matrix's share of the SMs
+      if (G < 1) G = 1;
+      if ((N + G - 1) / G > rows_cap) G = (N + rows_cap - 1) / rows_cap;
+      if (G > N) G = N;
+    }
     DecodeMat& m = p.mats[i];
     m.packed = mats[i].packed;
     m.sw = mats[i].w_scale;
@@ -517,9 +552,9 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
     m.acc = mats[i].acc;
     m.N = (int)N;
     m.G = (int)G;
-    m.g0 = total;
-    total += (int)G;
-    const int rm = (int)((N + G - 1) / G);
+    m.g0 = gated ? 0 : total;
+    if (!(gated && i == 1)) total += (int)G;
+    const int rm = (int)((N + G - 1) / G) * per;
     if (rm > rows_max) rows_max = rm;
   }
   p.rows_max = rows_max;
@@ -546,7 +581,7 @@ cudaError_t launch_fused(const DecodeParams& p, int grid, int nj, bool pdl, cons
 }  // namespace
 
 cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
-                          int64_t K, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+                          int64_t K, bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   DecodeParams p = {};
   p.xq_in = xq;
   p.sx_in = sx;
@@ -555,7 +590,7 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   // Token group: up to 8 tokens whose activations (MT * K bytes) fit in 64 KB.
   int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   while (mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
-  const int grid = plan_decode(p, mats, nmats, K, mt, false, dev);
+  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev);
   switch (mt) {
     case 1: return launch_mt<1, false, false, 1>(p, grid, pdl, dev, stream);
     case 2: return launch_mt<2, false, false, 1>(p, grid, pdl, dev, stream);
@@ -565,8 +600,8 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
 }
 
 cudaError_t launch_decode_fused(const float* x, const float* mul, const float* gamma, double eps, int64_t K,
-                                const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out, bool pdl,
-                                const DeviceInfo& dev, cudaStream_t stream) {
+                                const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out,
+                                bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   if (K > (int64_t)kDecThreads * 4 * kMaxNJ) return cudaErrorInvalidValue;
   DecodeParams p = {};
   p.x = x;
@@ -578,7 +613,7 @@ cudaError_t launch_decode_fused(const float* x, const float* mul, const float* g
   p.status = dev.status;
   p.M = 1;
   const bool norm = gamma != nullptr;
-  const int grid = plan_decode(p, mats, nmats, K, 1, norm, dev);
+  const int grid = plan_decode(p, mats, nmats, K, 1, norm, gated, dev);
   // float4 elements of the row a thread owns (the kernel keeps them in registers)
   const int nj = (int)((K / 4 + kDecThreads - 1) / kDecThreads);
   return norm ? launch_fused<true>(p, grid, nj, pdl, dev, stream) : launch_fused<false>(p, grid, nj, pdl, dev, stream);

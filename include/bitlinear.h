@@ -188,7 +188,18 @@ enum {
    * written before the chain began: not by the kernel immediately before on
    * the stream, nor by any kernel between it and the last launch made
    * without this flag. */
-  BITLINEAR_FLAG_PDL = 1
+  BITLINEAR_FLAG_PDL = 1,
+  /* bitlinear_linear / bitlinear_linear_ws only: the two matrices are an FFN
+   * gate and up projection of equal N ("Hesper.Layers.TransformerBlock" page,
+   * section "Forward Pass", FFN sub-layer: hidden = ReLU^2(gate) x up, which
+   * the page's fused gate / up / ReLU kernel computes).  weights[0].y receives
+   * h = (r * r) * u with r = max(g, 0), g and u the gate and up outputs (the
+   * fp32 steps of the gating prologue, so a following call on h without mul
+   * gives bit for bit the results of one on g with mul = u); weights[1].y
+   * receives u.  The decode kernel computes h in its epilogue, every CTA
+   * holding the same rows of both matrices; the tensor-core kernels are
+   * followed by one elementwise launch. */
+  BITLINEAR_FLAG_GATED = 2
 };
 
 /* bitlinear_forward with an explicit algorithm and flags (see above). */
@@ -255,7 +266,9 @@ typedef struct bitlinear_weight {
  * tiles span all of them.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
- * scales must not come from the kernel immediately before on the stream).
+ * scales must not come from the kernel immediately before on the stream);
+ * BITLINEAR_FLAG_GATED (see above) needs num_weights == 2 and equal N, else
+ * BITLINEAR_ERR_SHAPE.  Other flag bits: BITLINEAR_ERR_UNSUPPORTED.
  */
 bitlinear_status bitlinear_linear(const float* x, const float* mul, int64_t M, int64_t K,
                                   const float* rms_weight, double rms_eps,

@@ -92,6 +92,22 @@ def test_linear_ws_argument_errors(lib):
     assert f(A, None, 200, 100, None, 1e-6, arr, 1, A, A, 0, A, ws, None) == -2        # K % 64
 
 
+def test_linear_gated_argument_errors(lib):
+    f = lib.bitlinear_linear
+    g = bl.BitLinearWeight(A, A, 64, A, None)
+    one = (bl.BitLinearWeight * 1)(g)
+    pair = (bl.BitLinearWeight * 2)(g, bl.BitLinearWeight(A, A, 128, A, None))
+    three = (bl.BitLinearWeight * 3)(g, g, g)
+    G = bl.FLAG_GATED
+    assert f(A, None, 1, 128, None, 1e-6, one, 1, A, A, G, None) == -2       # one matrix
+    assert f(A, None, 1, 128, None, 1e-6, three, 3, A, A, G, None) == -2     # three matrices
+    assert f(A, None, 1, 128, None, 1e-6, pair, 2, A, A, G, None) == -2      # N differ
+    assert f(A, None, 1, 128, None, 1e-6, one, 1, A, A, 4, None) == -4       # unknown flag bit
+    same = (bl.BitLinearWeight * 2)(g, bl.BitLinearWeight(A, A, 64, None, None))
+    assert f(A, None, 1, 128, None, 1e-6, same, 2, A, A, G, None) == -1      # the up output is required
+    assert f(A, None, 0, 128, None, 1e-6, same, 2, A, A, G, None) == 0       # empty batch
+
+
 def test_quant_act_argument_errors(lib):
     f = lib.bitlinear_quant_act
     assert f(None, None, 1, 64, None, 1e-6, A, A, None) == -1

@@ -412,6 +412,66 @@ def test_linear_matches_oracle(M, K, Ns, prolog, ws):
         assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
 
 
+def _f32_outputs(acc, sx, sw):
+    """The rescale of the BitLinear definition in fp32 steps: f32(acc) / f32(sx * sw)."""
+    den = (sx.astype(np.float32)[:, None] * np.float32(sw)).astype(np.float32)
+    return (acc.astype(np.float32) / den).astype(np.float32)
+
+
+@pytest.mark.parametrize("M,K,N,norm", [
+    (1, 2560, 10240, False),    # BitNet-3B gate || up at M = 1: fused decode, gated in its epilogue
+    (1, 2048, 5632, True),      # with the RMSNorm prologue
+    (1, 128, 100, False),       # more CTAs than rows: one row of each matrix a CTA
+    (3, 640, 500, False),       # act_quant, then the decode kernel (4-token groups)
+    (8, 2560, 2048, False),     # 8-token groups
+    (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
+    (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
+])
+@pytest.mark.parametrize("ws", [False, True])
+def test_linear_gated(M, K, N, norm, ws):
+    """BITLINEAR_FLAG_GATED: the first output is ReLU^2(gate) * up in the fp32 steps of
+    the gating prologue, the second the up output, bit for bit; a following call on that
+    output without mul quantises exactly as one on the gate output with mul = up."""
+    x = synth.activations(M, K, 100 + K, outlier_seed=101 + K)
+    gamma = synth.uniform((K,), 0.5, 1.5, 102 + K) if norm else None
+    xq_o, sx_o = oracle.act_quant(x.numpy(), gamma=None if gamma is None else gamma.numpy(), eps=1e-6)
+    mats, accs_o, outs_o = [], [], []
+    for i in range(2):
+        W = synth.weight(N, K, 103 + i + K)
+        Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+        acc_o, _ = oracle.forward(xq_o, sx_o, oracle.pack(Wq_o), sw_o, N, K)
+        accs_o.append(acc_o)
+        outs_o.append(_f32_outputs(acc_o, sx_o, sw_o))
+        _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        mats.append((packed_d, sw_d, torch.full((M, N), float("nan"), device="cuda"),
+                     torch.full((M, N), -3, dtype=torch.int32, device="cuda")))
+    g, u = outs_o
+    r = np.maximum(g, np.float32(0))
+    h = ((r * r).astype(np.float32) * u).astype(np.float32)
+    xq = torch.zeros(M, K, dtype=torch.int8, device="cuda")
+    sx = torch.zeros(M, dtype=torch.float32, device="cuda")
+    kw = dict(rms_weight=None if gamma is None else gamma.cuda(), rms_eps=1e-6,
+              flags=bl.FLAG_PDL | bl.FLAG_GATED)
+    if ws:
+        bl.bitlinear_linear_ws(x.cuda(), mats, xq, sx, torch.empty(bl.bitlinear_forward_workspace(M, K),
+                                                                   dtype=torch.uint8, device="cuda"), **kw)
+    else:
+        bl.bitlinear_linear(x.cuda(), mats, xq, sx, **kw)
+    assert bl.bitlinear_device_status() == 0
+    np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
+    np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
+    for (_, _, _, acc), acc_o in zip(mats, accs_o):
+        np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
+    np.testing.assert_array_equal(mats[1][2].cpu().numpy(), u)
+    np.testing.assert_array_equal(mats[0][2].cpu().numpy(), h)
+    if N % 64 == 0 and M <= 8:
+        # the down projection's input: h alone, against the oracle's gating prologue on g and u
+        xq2_o, sx2_o = oracle.act_quant(g, mul=u)
+        xq2, sx2, _ = gpu_act_quant(mats[0][2].cpu(), None, None)
+        np.testing.assert_array_equal(xq2, xq2_o)
+        np.testing.assert_array_equal(sx2, sx2_o)
+
+
 # Matrices that the AUTO rule gives to the same tensor-core kernel share one
 # grid whose column tiles span all of them; each case names the kernel(s) its
 # shapes select (batched: M <= 128, N <= 4096, M >= 64 or K < 8192; the
