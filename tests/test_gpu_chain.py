@@ -8,6 +8,9 @@ launch inside one CUDA graph, each call consuming the previous call's output:
     x -> [q || k || v] ; v -> o ; o -> RMSNorm -> [gate || up] ;
     ReLU^2(gate) * up -> sub-norm -> down ; down -> next layer's x
 
+(with `gated`, the gate || up call writes ReLU^2(gate) * up itself,
+BITLINEAR_FLAG_GATED, and the down call reads that product alone)
+
 (the FFN structure of the "Transformer Block" page, sections "Feed-Forward
 Network" and "Layer Structure"; attention itself is not part of this path, so
 o reads v directly).  After two replays every call's int8 activations and
@@ -47,8 +50,8 @@ def _quantize(N, K, seed):
 class Call:
     """One bitlinear_linear_ws call of the schedule with its own buffers."""
 
-    def __init__(self, M, K, mats, x, mul=None, gamma=None):
-        self.M, self.K, self.x, self.mul, self.gamma = M, K, x, mul, gamma
+    def __init__(self, M, K, mats, x, mul=None, gamma=None, gated=False):
+        self.M, self.K, self.x, self.mul, self.gamma, self.gated = M, K, x, mul, gamma, gated
         self.mats = mats  # list of (packed, sw, Wq)
         self.xq = torch.empty(M, K, dtype=torch.int8, device="cuda")
         self.sx = torch.empty(M, dtype=torch.float32, device="cuda")
@@ -58,7 +61,7 @@ class Call:
     def run(self, ws, stream):
         bl.bitlinear_linear_ws(self.x, [(p, s, y, a) for (p, s, _), y, a in zip(self.mats, self.ys, self.accs)],
                                self.xq, self.sx, ws, mul=self.mul, rms_weight=self.gamma, rms_eps=1e-6,
-                               flags=bl.FLAG_PDL, stream=stream)
+                               flags=bl.FLAG_PDL | (bl.FLAG_GATED if self.gated else 0), stream=stream)
 
     def check(self, rng):
         x = self.x.cpu().numpy()
@@ -67,14 +70,28 @@ class Call:
         xq_o, sx_o = oracle.act_quant(x, mul=mul, gamma=gamma, eps=1e-6)
         np.testing.assert_array_equal(self.xq.cpu().numpy(), xq_o)
         np.testing.assert_array_equal(self.sx.cpu().numpy(), sx_o)
+        N = self.mats[0][2].shape[0]
+        cols = np.sort(rng.choice(N, size=min(SAMPLE_COLS, N), replace=False))
+        cols[-1] = N - 1  # the last column (the ragged edge of any tile) always
+        f32 = []
         for (_, sw, Wq), y, acc in zip(self.mats, self.ys, self.accs):
-            N = Wq.shape[0]
-            cols = np.sort(rng.choice(N, size=min(SAMPLE_COLS, N), replace=False))
-            cols[-1] = N - 1  # the last column (the ragged edge of any tile) always
+            if Wq.shape[0] != N:
+                cols = np.sort(rng.choice(Wq.shape[0], size=min(SAMPLE_COLS, Wq.shape[0]), replace=False))
+                cols[-1] = Wq.shape[0] - 1
             acc_o, y_o = oracle.forward(xq_o, sx_o, oracle.pack(np.ascontiguousarray(Wq[cols])), sw.item(),
                                         len(cols), self.K)
             np.testing.assert_array_equal(acc.cpu().numpy()[:, cols], acc_o)
-            assert max_rel_err(y.cpu().numpy()[:, cols], y_o) <= Y_RTOL
+            if not self.gated:
+                assert max_rel_err(y.cpu().numpy()[:, cols], y_o) <= Y_RTOL
+            # the rescale's fp32 steps: f32(acc) / f32(sx * sw)
+            den = (sx_o.astype(np.float32)[:, None] * np.float32(sw.item())).astype(np.float32)
+            f32.append((acc_o.astype(np.float32) / den).astype(np.float32))
+        if self.gated:
+            g, u = f32
+            r = np.maximum(g, np.float32(0))
+            h = ((r * r).astype(np.float32) * u).astype(np.float32)
+            np.testing.assert_array_equal(self.ys[0].cpu().numpy()[:, cols], h)
+            np.testing.assert_array_equal(self.ys[1].cpu().numpy()[:, cols], u)
 
 
 @pytest.fixture(scope="module")
@@ -89,8 +106,9 @@ def weights():
     return layers, g_norm, g_sub
 
 
+@pytest.mark.parametrize("gated", [False, True])
 @pytest.mark.parametrize("M", [1, 8, 64])
-def test_two_layer_schedule_in_one_graph(weights, M):
+def test_two_layer_schedule_in_one_graph(weights, M, gated):
     layers, g_norm, g_sub = weights
     x0 = synth.activations(M, D, synth.SEEDS["weight_set"]["x"]).cuda()
     calls = []
@@ -99,8 +117,8 @@ def test_two_layer_schedule_in_one_graph(weights, M):
         q, k, v, o, gate, up, down = mats
         qkv = Call(M, D, [q, k, v], x)
         c_o = Call(M, D, [o], qkv.ys[2])
-        gu = Call(M, D, [gate, up], c_o.ys[0], gamma=g_norm)
-        dn = Call(M, F, [down], gu.ys[0], mul=gu.ys[1], gamma=g_sub)
+        gu = Call(M, D, [gate, up], c_o.ys[0], gamma=g_norm, gated=gated)
+        dn = Call(M, F, [down], gu.ys[0], mul=None if gated else gu.ys[1], gamma=g_sub)
         calls += [qkv, c_o, gu, dn]
         x = dn.ys[0]
     ws = torch.empty(bl.bitlinear_forward_workspace(M, F), dtype=torch.uint8, device="cuda")
@@ -121,6 +139,6 @@ def test_two_layer_schedule_in_one_graph(weights, M):
         g.replay()
     torch.cuda.synchronize()
     assert bl.bitlinear_device_status() == 0
-    rng = np.random.default_rng(1000 + M)
+    rng = np.random.default_rng(1000 + M + (7 if gated else 0))
     for c in calls:
         c.check(rng)
