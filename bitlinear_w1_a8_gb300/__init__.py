@@ -297,6 +297,12 @@ def bitlinear_selftest_wait_timeout(limit_ns: int, stream=None):
            "bitlinear_selftest_wait_timeout")
 
 
+def _packed_size(N: int, K: int) -> int:
+    """bitlinear_packed_bytes(N, K) without a call into the library (N * ceil(K/64) * 16,
+    the layout the header documents); a CPU test holds the two equal."""
+    return N * ((K + 63) // 64) * 16
+
+
 def _weight_array(weights, M, K):
     import torch
     arr = (BitLinearWeight * len(weights))()
@@ -304,7 +310,7 @@ def _weight_array(weights, M, K):
         packed, w_scale, y = w[0], w[1], w[2]
         acc = w[3] if len(w) > 3 else None
         N = y.shape[1]
-        _need(packed, torch.uint8, "packed", (bitlinear_packed_bytes(N, K),))
+        _need(packed, torch.uint8, "packed", (_packed_size(N, K),))
         _need(w_scale, torch.float32, "w_scale")
         _need(y, torch.float32, "y", (M, N))
         if acc is not None:

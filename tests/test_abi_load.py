@@ -40,6 +40,8 @@ def test_host_only_calls(lib):
     assert bl.bitlinear_packed_bytes(3, 65) == 96
     assert bl.bitlinear_packed_bytes(0, 64) == 0
     assert bl.bitlinear_quantize_weights_workspace(10240, 2560) >= 256 * 8
+    for N, K in ((1, 64), (3, 65), (10240, 2560), (2560, 10240), (50000, 2560), (7, 32768), (0, 64)):
+        assert bl._packed_size(N, K) == bl.bitlinear_packed_bytes(N, K)
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert bl.bitlinear_status_string(code).startswith("BITLINEAR_")
 
