@@ -319,6 +319,21 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
     return from_cuda(launch_decode_fused(x, mul, rms_weight, rms_eps, K, mats, num_weights, xq, x_scale, gated,
                                          pdl, dev, s));
   }
+  if (!mul && !rms_weight && decode_rows_fit(M, K)) {
+    // 2..8 tokens without a prologue, every matrix on the decode kernel: one
+    // launch again, every CTA quantising the token rows itself -- when each
+    // CTA's weight rows (about all rows / SMs) outnumber 4 M, i.e. its dots
+    // outweigh loading the M fp32 rows (measured on the BitNet-3B shapes: the
+    // 2560-row o projection gains at M <= 4 and loses 0.9 us at M = 8)
+    bool all_decode = true;
+    int64_t rows = 0;
+    for (int i = 0; i < num_weights; ++i) {
+      all_decode = all_decode && auto_algo(M, mats[i].N, K) == BITLINEAR_ALGO_DECODE;
+      rows += mats[i].N;
+    }
+    if (all_decode && rows >= 4 * M * dev.num_sms)
+      return from_cuda(launch_decode_rows(x, M, K, mats, num_weights, xq, x_scale, gated, pdl, dev, s));
+  }
   cudaError_t err = launch_act_quant(x, mul, M, K, rms_weight, rms_eps, xq, x_scale, dev, s, pdl);
   if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   // The matrices that take the same kernel share one launch of it (WIDE, with

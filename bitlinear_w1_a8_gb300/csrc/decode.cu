@@ -302,6 +302,84 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
   return s;
 }
 
+// Fused-mode quantisation of a group's mcount (<= MT <= 8) token rows held in
+// registers, without prologues: thread t owns the float4 elements
+// f = t + 512 j (j < NJ) of the rows laid end to end (row f / K4), so every
+// load is issued before the first use.  Per element group a warp reduces
+// first and adds to its row in shared memory (amx: the row's absmax as
+// integer bits, which order like the non-negative floats; sumx: the row's sum
+// of codes); thread m < mcount leaves row m's sx in sxs[m].  Writes the int8
+// codes to xs (shared) and, when out is not NULL, to out (global).  amx must
+// be zero and sumx zero before the call; every thread of the block calls it.
+template <int MT, int NJ>
+__device__ __forceinline__ void quantize_rows_regs(const float* __restrict__ x, int K, int mcount, int* amx,
+                                                   float* sxs, int8_t* xs, int8_t* out, int* sumx) {
+  static_assert(MT <= 8 && NJ <= 10, "row indices are packed 3 bits each into one word");
+  const int t = threadIdx.x, lane = t & 31;
+  const int K4 = K >> 2;
+  const int total = mcount * K4;
+  const int nvalid = total > t ? (total - t + kDecThreads - 1) / kDecThreads : 0;  // elements f < total
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  float4 h[NJ];
+  uint32_t rows = 0;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int f = t + j * kDecThreads;
+    const bool ok = j < nvalid;
+    h[j] = ok ? ld_cg4(x4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    rows |= (uint32_t)(ok ? f / K4 : 0) << (3 * j);
+  }
+  __syncthreads();  // amx and sumx were zeroed before the call
+  // A warp whose valid lanes share one row reduces first; otherwise each lane adds.
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const bool ok = j < nvalid;
+    const int rj = (int)((rows >> (3 * j)) & 7u);
+    float a = ok ? fmaxf(fmaxf(fabsf(h[j].x), fabsf(h[j].y)), fmaxf(fabsf(h[j].z), fabsf(h[j].w))) : 0.0f;
+    const int r0 = __shfl_sync(kFullMask, rj, 0);
+    if (__all_sync(kFullMask, !ok || rj == r0)) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFullMask, a, o));
+      if (lane == 0 && a > 0.0f) atomicMax(&amx[r0], __float_as_int(a));
+    } else if (ok && a > 0.0f) {
+      atomicMax(&amx[rj], __float_as_int(a));
+    }
+  }
+  __syncthreads();
+  if (t < mcount) sxs[t] = __fdiv_rn(127.0f, fmaxf(__int_as_float(amx[t]), 1e-5f));
+  __syncthreads();
+  int* xs32 = reinterpret_cast<int*>(xs);
+  int* xo32 = reinterpret_cast<int*>(out);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const bool ok = j < nvalid;
+    const int rj = (int)((rows >> (3 * j)) & 7u);
+    int q4 = 0;
+    if (ok) {
+      const float sj = sxs[rj];
+      const float f4[4] = {h[j].x, h[j].y, h[j].z, h[j].w};
+      uint32_t word = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        int v = __float2int_rn(__fmul_rn(f4[q], sj));
+        v = v < -128 ? -128 : (v > 127 ? 127 : v);
+        q4 += v;
+        word |= ((uint32_t)v & 0xffu) << (8 * q);
+      }
+      const int f = t + j * kDecThreads;
+      xs32[f] = (int)word;
+      if (out) xo32[f] = (int)word;
+    }
+    const int r0 = __shfl_sync(kFullMask, rj, 0);
+    if (__all_sync(kFullMask, !ok || rj == r0)) {
+      const int q = __reduce_add_sync(kFullMask, q4);
+      if (lane == 0 && q != 0) atomicAdd(&sumx[r0], q);
+    } else if (ok && q4 != 0) {
+      atomicAdd(&sumx[rj], q4);
+    }
+  }
+}
+
 // Dynamic shared memory: the CTA's weight planes at 0 (plane kb holds rows
 // r0 .. r1-1 as R consecutive 16-byte chunks), xs[MT][K] int8 activations at
 // off_xs, red[MT][R] int32 row sums at off_red, (fused RMSNorm) gamma at off_gs.
@@ -372,7 +450,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   pdl_wait_primary();
 
   bool have_g = true;
-  if constexpr (FUSED) {
+  if constexpr (FUSED && MT > 1) {
+    static_assert(!NORM, "the RMSNorm prologue is fused for one token only");
+    // a few token rows, no prologue: every CTA quantises the group itself
+    __shared__ int amx[MT];
+    __shared__ float sxs[MT];
+    if (t < MT) amx[t] = 0;
+    quantize_rows_regs<MT, NJ>(p.x + (int64_t)m0 * K, K, mcount, amx, sxs, xs,
+                               c == 0 && p.xq_out ? p.xq_out + (int64_t)m0 * K : nullptr, &sumx[0]);
+    if (t < MT) {
+      den[0][t] = t < mcount ? __fmul_rn(sxs[t], sw) : 1.0f;
+      den[1][t] = t < mcount ? __fmul_rn(sxs[t], sw1) : 1.0f;
+      if (c == 0 && p.sx_out && t < mcount) p.sx_out[m0 + t] = sxs[t];
+    }
+    __syncthreads();
+  } else if constexpr (FUSED) {
     const float s = quantize_row_regs<NJ, norm>(p.x + (int64_t)m0 * K, p.mul ? p.mul + (int64_t)m0 * K : nullptr,
                                                 gs, p.eps, K, &gbar, p.status, qsc, xs,
                                           c == 0 ? p.xq_out + (p.xq_out ? (int64_t)m0 * K : 0) : nullptr,
@@ -533,6 +625,31 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   int64_t rows_cap = (room < kMaxWeightBytes ? room : kMaxWeightBytes) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
   if (rows_cap * per > kDecThreads) rows_cap = kDecThreads / per;
+  // Each matrix's share of the SMs in proportion to its rows, rounded down and
+  // the SMs left over given to the largest remainders, so that the shares add
+  // up to the SM count: one CTA more than there are SMs waits for a free slot
+  // behind the co-resident previous launch and delays the whole grid.
+  // (Every matrix has one CTA first; the rest of the SMs are shared out.)
+  const int nshare = gated ? 1 : nmats;
+  const int64_t pool = dev.num_sms > nshare ? dev.num_sms - nshare : 0;
+  int64_t share[kMaxDecodeMats];
+  int64_t left = pool;
+  for (int i = 0; i < nshare; ++i) {
+    share[i] = pool * mats[i].N / all_rows;
+    left -= share[i];
+  }
+  for (; left > 0; --left) {
+    int best = 0;
+    int64_t best_rem = -1;
+    for (int i = 0; i < nshare; ++i) {
+      const int64_t rem = pool * mats[i].N - share[i] * all_rows;
+      if (rem > best_rem) {
+        best_rem = rem;
+        best = i;
+      }
+    }
+    ++share[best];
+  }
   int total = 0, rows_max = 1;
   for (int i = 0; i < nmats; ++i) {
     const int64_t N = mats[i].N;
@@ -540,8 +657,7 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
     if (gated && i == 1) {
       G = p.mats[0].G;  // the pair shares one split
     } else {
-      G = (dev.num_sms * N + all_rows / 2) / all_rows;  // this matrix's share of the SMs
-      if (G < 1) G = 1;
+      G = 1 + share[i];
       if ((N + G - 1) / G > rows_cap) G = (N + rows_cap - 1) / rows_cap;
       if (G > N) G = N;
     }
@@ -596,6 +712,32 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
     case 2: return launch_mt<2, false, false, 1>(p, grid, pdl, dev, stream);
     case 4: return launch_mt<4, false, false, 1>(p, grid, pdl, dev, stream);
     default: return launch_mt<8, false, false, 1>(p, grid, pdl, dev, stream);
+  }
+}
+
+bool decode_rows_fit(int64_t M, int64_t K) {
+  if (M < 2 || M > 8 || K <= 0) return false;
+  const int64_t mt = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
+  const int64_t nj = mt == 2 ? 3 : (mt == 4 ? 5 : 10);  // float4 a thread holds (the instances below)
+  return M * (K / 4) <= nj * kDecThreads;
+}
+
+cudaError_t launch_decode_rows(const float* x, int64_t M, int64_t K, const DecodeMatrix* mats, int nmats,
+                               int8_t* xq_out, float* sx_out, bool gated, bool pdl, const DeviceInfo& dev,
+                               cudaStream_t stream) {
+  if (!decode_rows_fit(M, K)) return cudaErrorInvalidValue;
+  DecodeParams p = {};
+  p.x = x;
+  p.xq_out = xq_out;
+  p.sx_out = sx_out;
+  p.status = dev.status;
+  p.M = (int)M;
+  const int mt = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
+  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev);
+  switch (mt) {
+    case 2: return launch_mt<2, true, false, 3>(p, grid, pdl, dev, stream);
+    case 4: return launch_mt<4, true, false, 5>(p, grid, pdl, dev, stream);
+    default: return launch_mt<8, true, false, 10>(p, grid, pdl, dev, stream);
   }
 }
 

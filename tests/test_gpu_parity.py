@@ -412,6 +412,45 @@ def test_linear_matches_oracle(M, K, Ns, prolog, ws):
         assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
 
 
+@pytest.mark.parametrize("M,K,Ns", [
+    (2, 3072, (1300,)),            # 2 tokens at the register limit (3 float4 a thread)
+    (3, 192, (1500, 401)),         # rows of 48 float4: warps straddle token rows
+    (4, 2560, (2560, 2560, 640)),  # q || k || v widths at the 4-token limit
+    (5, 704, (3100,)),             # 8-token instance with 5 rows, ragged N
+    (7, 2048, (4000, 400)),
+    (8, 2560, (10240, 10240)),     # gate || up widths at the 8-token limit (10 float4 a thread)
+])
+def test_linear_few_tokens_fused_quant(M, K, Ns):
+    """2..8 tokens without a prologue and at least 4 M rows a CTA: one decode launch in
+    which every CTA quantises the token rows itself; codes, scales, accumulators and
+    outputs against the oracle, with an all-zero row and an outlier row among the tokens."""
+    x = synth.activations(M, K, 110 + K, outlier_seed=111 + K)
+    x[M // 2] = 0.0
+    x[M - 1, K // 3] = 3.0e4
+    xq_o, sx_o = oracle.act_quant(x.numpy())
+    mats, refs = [], []
+    for i, N in enumerate(Ns):
+        W = synth.weight(N, K, 112 + i + N)
+        Wq_o, sw_o, _ = oracle.weight_quant(W.numpy())
+        refs.append(oracle.forward(xq_o, sx_o, oracle.pack(Wq_o), sw_o, N, K))
+        _, _, _, (packed_d, sw_d) = gpu_quantize_weights(W)
+        mats.append((packed_d, sw_d, torch.full((M, N), float("nan"), device="cuda"),
+                     torch.full((M, N), -3, dtype=torch.int32, device="cuda")))
+    xq_full = guarded(M * K, torch.int8, 77)
+    sx_full = guarded(M, torch.float32, -3.0)
+    xq, sx = xq_full[0].view(M, K), sx_full[0]
+    for flags in (0, bl.FLAG_PDL):
+        bl.bitlinear_linear(x.cuda(), mats, xq, sx, flags=flags)
+        assert bl.bitlinear_device_status() == 0
+        check_canary(xq_full[1], 77)
+        check_canary(sx_full[1], -3.0)
+        np.testing.assert_array_equal(xq.cpu().numpy(), xq_o)
+        np.testing.assert_array_equal(sx.cpu().numpy(), sx_o)
+        for (_, _, y, acc), (acc_o, y_o) in zip(mats, refs):
+            np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
+            assert max_rel_err(y.cpu().numpy(), y_o) <= Y_RTOL
+
+
 def _f32_outputs(acc, sx, sw):
     """The rescale of the BitLinear definition in fp32 steps: f32(acc) / f32(sx * sw)."""
     den = (sx.astype(np.float32)[:, None] * np.float32(sw)).astype(np.float32)
