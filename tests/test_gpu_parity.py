@@ -463,6 +463,8 @@ def _f32_outputs(acc, sx, sw):
     (1, 128, 100, False),       # more CTAs than rows: one row of each matrix a CTA
     (3, 640, 500, False),       # act_quant, then the decode kernel (4-token groups)
     (8, 2560, 2048, False),     # 8-token groups
+    (4, 2560, 5120, False),     # few tokens quantised in every CTA (no act_quant launch), gated pairs
+    (8, 2560, 10240, False),    # the same at 8 tokens, BitNet-3B gate || up widths
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
     (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
 ])
