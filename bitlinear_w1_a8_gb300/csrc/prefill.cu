@@ -815,7 +815,13 @@ cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, co
   PrefillParams p = common_params(xq, sx, M, mats, nmats, K, dev);
   if (p.KB < 0) return cudaErrorNotSupported;
   // Tile width and K split together: the fewest (k-steps of the busiest CTA)
-  // x (tile width + 64), the +64 being the activation widening of a k-step.
+  // x (tile width + 64), the +64 being the activation widening of a k-step;
+  // a split also pays its fill and its partial-sum exchange, which grows with
+  // the tile width (128 x width fp32 per rank): 1024 + 16 x width.  (With a
+  // flat 1024 the planner split 320-wide tiles four ways where plain 80-wide
+  // tiles run twice as fast: 10240 x 2560 at M = 32 took 39.6 us against
+  // 20.1, 256 x 2560 x 2560 21.8 against 17.5, 1024 x 2048 x 8192 68.2 against
+  // 48.2, on GB300.)
   // 320-wide single-accumulator tiles only when every CTA has one tile: a
   // CTA with more would run each tile's epilogue with no MMAs beside it (the
   // up shape at M = 2048 took 144 us that way against 108).
@@ -829,7 +835,7 @@ cudaError_t launch_prefill_mats(const int8_t* xq, const float* sx, int64_t M, co
     const bool is_big = nt > kMaxTileN;
     if (is_big && tiles > dev.num_sms) continue;
     const int sp = best_split(tiles, p.KB, dev.num_sms, &ksteps);
-    const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 : 0);
+    const int64_t cost = ksteps * (nt + 64) + (sp > 1 ? 4 * 256 + 16 * nt : 0);
     if (best < 0 || cost < best) {
       best = cost;
       p.n_tile = nt;
