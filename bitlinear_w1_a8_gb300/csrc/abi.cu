@@ -98,19 +98,20 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
 
 // With a workspace, AUTO takes the WIDE kernel for narrow outputs at medium
 // token counts above the batched kernel's range, where it measured faster on
-// GB300 than the 128-token-tile kernel (hot L2, pre-pass included; at
-// M = 256 / 512 / 1024):
-//   N = 2560, K = 10240: 1.19 / 1.41 / 1.09x
-//   N = 2048, K = 8192:  1.38 / 1.38 / 1.06x
-//   N = K = 2560:        1.71 / 1.03 / 0.89x
-// and for wide outputs (N = 8192, 10240) and at M = 2048: 0.67 - 1.00x.  Up to
+// GB300 than the 128-token-tile kernel (pre-pass included, back to back; us
+// per call, 128-token tiles / WIDE):
+//   N = 2048, K = 8192:   M = 256 37.2 / 20.1, M = 512 38.1 / 33.2, M = 1024 48.3 / 52.7
+//   N = 2560, K = 10240:  M = 256 32.9 / 34.5, M = 512 49.3 / 41.4, M = 1024 61.2 / 65.0
+//   N = K = 2560:         M = 256 17.6 / 17.5, M = 512 19.2 / 23.3
+//   N = 1000, K = 4096, M = 200: 14.4 / 12.7;  N = K = 4096, M = 384: 28.8 / 29.4
+// so up to 512 tokens at K >= 8192 and up to 256 below; for wide outputs
+// (N = 8192, 10240) and at M = 2048 the other kernels measured faster.  Up to
 // M = 128 the batched kernel (K split inside a cluster) is within a few per
 // cent of WIDE without the pre-pass launch (BitNet-3B o / down at M = 64:
 // 10.1 / 17.4 us against 10.7 / 17.9).
 bool wide_wins(int64_t M, int64_t N, int64_t K) {
-  if (N > 4096 || M > 1024 || M <= 128) return false;
-  if (K >= 8192) return true;
-  return M <= 512;
+  if (N > 4096 || M <= 128) return false;
+  return K >= 8192 ? M <= 512 : M <= 256;
 }
 
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
