@@ -321,11 +321,10 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
                                          pdl, dev, s));
   }
   if (!mul && !rms_weight && decode_rows_fit(M, K)) {
-    // 2..8 tokens without a prologue, every matrix on the decode kernel: one
+    // Two tokens without a prologue, every matrix on the decode kernel: one
     // launch again, every CTA quantising the token rows itself -- when each
     // CTA's weight rows (about all rows / SMs) outnumber 4 M, i.e. its dots
-    // outweigh loading the M fp32 rows (measured on the BitNet-3B shapes: the
-    // 2560-row o projection gains at M <= 4 and loses 0.9 us at M = 8)
+    // outweigh loading the fp32 rows
     bool all_decode = true;
     int64_t rows = 0;
     for (int i = 0; i < num_weights; ++i) {

@@ -199,9 +199,9 @@ cudaError_t launch_decode_fused(const float* x, const float* mul, const float* g
                                 const DecodeMatrix* mats, int nmats, int8_t* xq_out, float* sx_out,
                                 bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream);
 
-// 2 <= M <= 8 token rows without prologues: every CTA quantises the rows
-// itself from registers (decode_rows_fit: M * K / 4 float4 within the
-// kernel's per-thread budget); CTA 0 writes xq_out / sx_out when not NULL.
+// M = 2 token rows without prologues: every CTA quantises the rows itself
+// from registers (decode_rows_fit: K <= 3072); CTA 0 writes xq_out / sx_out
+// when they are not NULL.
 bool decode_rows_fit(int64_t M, int64_t K);
 cudaError_t launch_decode_rows(const float* x, int64_t M, int64_t K, const DecodeMatrix* mats, int nmats,
                                int8_t* xq_out, float* sx_out, bool gated, bool pdl, const DeviceInfo& dev,

@@ -715,11 +715,13 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   }
 }
 
+// Two tokens only: the 4- and 8-token instances (58 and 64 registers a
+// thread) were faster on each projection alone but slower inside a block's
+// chain of calls (BitNet-3B, eight layers: 42.0 -> 43.9 us a layer at M = 4,
+// 63.9 -> 71.5 at M = 8, against 29.8 -> 28.6 at M = 2): beside them the next
+// launch's CTAs no longer fit on the SM early.
 bool decode_rows_fit(int64_t M, int64_t K) {
-  if (M < 2 || M > 8 || K <= 0) return false;
-  const int64_t mt = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
-  const int64_t nj = mt == 2 ? 3 : (mt == 4 ? 5 : 10);  // float4 a thread holds (the instances below)
-  return M * (K / 4) <= nj * kDecThreads;
+  return M == 2 && K > 0 && M * (K / 4) <= 3 * kDecThreads;  // 3 float4 a thread
 }
 
 cudaError_t launch_decode_rows(const float* x, int64_t M, int64_t K, const DecodeMatrix* mats, int nmats,
@@ -732,13 +734,8 @@ cudaError_t launch_decode_rows(const float* x, int64_t M, int64_t K, const Decod
   p.sx_out = sx_out;
   p.status = dev.status;
   p.M = (int)M;
-  const int mt = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
-  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev);
-  switch (mt) {
-    case 2: return launch_mt<2, true, false, 3>(p, grid, pdl, dev, stream);
-    case 4: return launch_mt<4, true, false, 5>(p, grid, pdl, dev, stream);
-    default: return launch_mt<8, true, false, 10>(p, grid, pdl, dev, stream);
-  }
+  const int grid = plan_decode(p, mats, nmats, K, 2, false, gated, dev);
+  return launch_mt<2, true, false, 3>(p, grid, pdl, dev, stream);
 }
 
 cudaError_t launch_decode_fused(const float* x, const float* mul, const float* gamma, double eps, int64_t K,

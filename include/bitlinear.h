@@ -260,12 +260,10 @@ typedef struct bitlinear_weight {
  * share of the packed weights while it quantises the token itself (CTA 0
  * writes xq, x_scale), which keeps a separate act_quant kernel and its
  * latency off the decode critical path; the matrices' CTAs share one grid.
- * So is a call of 2 <= M <= 8 tokens without mul and rms_weight whose
- * matrices all take the decode kernel, when M * K fits the kernel's
- * registers (M * K <= 6144 for M = 2, 10240 for M <= 4, 20480 for M <= 8:
- * e.g. up to 8 tokens at K = 2560) and the matrices have at least
- * 4 * M * (SM count) rows together (each CTA's dots outweigh its loading
- * the M rows).
+ * So is a call of M = 2 tokens without mul and rms_weight whose matrices
+ * all take the decode kernel, when K <= 3072 (the rows fit the kernel's
+ * registers) and the matrices have at least 8 * (SM count) rows together
+ * (each CTA's dots outweigh its loading the two rows).
  * Otherwise it runs bitlinear_quant_act, then one launch per kernel that
  * bitlinear_forward's AUTO rule picks for some matrix: the matrices given to
  * the same kernel (decode, batched or 128-token-tile) share one grid, whose

@@ -413,17 +413,18 @@ def test_linear_matches_oracle(M, K, Ns, prolog, ws):
 
 
 @pytest.mark.parametrize("M,K,Ns", [
-    (2, 3072, (1300,)),            # 2 tokens at the register limit (3 float4 a thread)
-    (3, 192, (1500, 401)),         # rows of 48 float4: warps straddle token rows
-    (4, 2560, (2560, 2560, 640)),  # q || k || v widths at the 4-token limit
-    (5, 704, (3100,)),             # 8-token instance with 5 rows, ragged N
-    (7, 2048, (4000, 400)),
-    (8, 2560, (10240, 10240)),     # gate || up widths at the 8-token limit (10 float4 a thread)
+    (2, 3072, (1300,)),            # at the register limit (3 float4 a thread)
+    (2, 192, (1500, 401)),         # rows of 48 float4: warps straddle the two token rows
+    (2, 2560, (2560, 2560, 640)),  # q || k || v widths
+    (2, 704, (3100,)),             # ragged N
+    (2, 2560, (10240, 10240)),     # gate || up widths
+    (3, 2560, (10240, 10240)),     # 3 and 8 tokens take act_quant and the decode kernel
+    (8, 2560, (10240, 10240)),
 ])
 def test_linear_few_tokens_fused_quant(M, K, Ns):
-    """2..8 tokens without a prologue and at least 4 M rows a CTA: one decode launch in
-    which every CTA quantises the token rows itself; codes, scales, accumulators and
-    outputs against the oracle, with an all-zero row and an outlier row among the tokens."""
+    """Two tokens without a prologue and at least 8 rows a CTA: one decode launch in which
+    every CTA quantises the token rows itself; codes, scales, accumulators and outputs
+    against the oracle, with an all-zero row and an outlier row among the tokens."""
     x = synth.activations(M, K, 110 + K, outlier_seed=111 + K)
     x[M // 2] = 0.0
     x[M - 1, K // 3] = 3.0e4
@@ -463,8 +464,8 @@ def _f32_outputs(acc, sx, sw):
     (1, 128, 100, False),       # more CTAs than rows: one row of each matrix a CTA
     (3, 640, 500, False),       # act_quant, then the decode kernel (4-token groups)
     (8, 2560, 2048, False),     # 8-token groups
-    (4, 2560, 5120, False),     # few tokens quantised in every CTA (no act_quant launch), gated pairs
-    (8, 2560, 10240, False),    # the same at 8 tokens, BitNet-3B gate || up widths
+    (2, 2560, 5120, False),     # two tokens quantised in every CTA (no act_quant launch), gated pairs
+    (2, 2560, 10240, False),    # the same at BitNet-3B gate || up widths
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
     (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
 ])
