@@ -121,17 +121,18 @@ def _check(status: int, what: str):
         raise BitLinearError(status, what)
 
 
+# Addresses go to ctypes as plain ints (the argtypes are c_void_p; None is NULL).
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
         import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def _need(t, dtype, name, shape=None):
