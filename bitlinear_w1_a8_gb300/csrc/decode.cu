@@ -9,20 +9,22 @@
 // calls run back to back, each waiting for the previous one's output.  Design:
 //  * grid: about one CTA per SM per launch (CTA c of a matrix owns rows
 //    [c*N/G, (c+1)*N/G); the matrices of one launch -- q, k, v or gate, up,
-//    which share one input -- split the SMs in proportion to their rows), and
+//    which share one input -- split the SMs in proportion to their rows, or,
+//    for a gated gate / up pair, every CTA holds the same rows of both), and
 //    each CTA uses at most half of an SM (512 threads of <= 64 registers,
 //    <= ~110 KB of shared memory), so under programmatic dependent launch the
 //    next launch's CTAs are resident while this one runs;
-//  * first thing, before griddepcontrol.wait, warp 0 bulk-copies all of the
-//    CTA's weights (one copy per k-block plane: its rows are contiguous
-//    there), and the RMSNorm gamma when there is one, into shared memory --
-//    they never come from the previous kernel, so they stream from HBM while
-//    the previous kernel finishes;
-//  * after the wait (fused mode, M = 1) every thread loads its share of the
-//    fp32 row straight into registers -- one memory round trip -- applies
-//    the optional gating and RMSNorm there, and the row is quantised with two
-//    block barriers (the absmax, then the codes in shared memory); with int8
-//    input (M tokens) the token rows are staged with cp.async;
+//  * first thing, before griddepcontrol.wait, warp 0 bulk-copies the RMSNorm
+//    gamma when there is one (on its own mbarrier) and all of the CTA's
+//    weights (one copy per k-block plane: its rows are contiguous there) into
+//    shared memory, and the weight scales are loaded -- they never come from
+//    the previous kernel, so they stream from HBM while it finishes;
+//  * after the wait (fused mode: M = 1, or two tokens without prologues)
+//    every thread loads its share of the fp32 rows straight into registers
+//    -- one memory round trip -- applies the optional gating and RMSNorm
+//    there, and the rows are quantised with block barriers (the absmax, then
+//    the codes in shared memory); with int8 input (M tokens) the token rows
+//    are staged with cp.async;
 //  * dots: the CTA's (k-block, row) chunks are dealt out to the 512 threads
 //    flat, in the order of the weight planes (chunk c = kb * R + r), so every
 //    thread gets the same number of chunks and a warp reads 32 consecutive
@@ -34,7 +36,8 @@
 //    sum Wq*x (the ternary add/sub) exactly.  On GB300 the dp4a pipe accepts
 //    about 32 per clock per SM, which bounds this phase;
 //  * each chunk's sum meets its row's others in shared memory (an int32
-//    atomic, exact in any order), then one thread per row rescales.
+//    atomic, exact in any order), then one thread per row rescales (and, for
+//    a gated pair, writes ReLU^2(gate) * up).
 #include "quant_row.cuh"
 
 namespace bitlinear {
