@@ -43,14 +43,16 @@ bitlinear_status current_device(DeviceInfo* out) {
   if (!g_dev_ready[d]) {
     DeviceInfo info = {};
     info.device = d;
-    int smem = 0;
+    int smem = 0, smem_sm = 0;
     if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
         cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
         cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess) {
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d) != cudaSuccess) {
       return BITLINEAR_ERR_CUDA;
     }
     info.smem_optin = (size_t)smem;
+    info.smem_per_sm = (size_t)smem_sm;
     // The kernels are built for sm_103a only.
     if (info.cc_major != 10 || info.cc_minor != 3) return BITLINEAR_ERR_UNSUPPORTED;
     void* addr = nullptr;

@@ -159,6 +159,7 @@ struct DeviceInfo {
   int num_sms;
   int cc_major, cc_minor;
   size_t smem_optin;
+  size_t smem_per_sm;  // shared memory of one SM (all its resident CTAs together)
   int* status;  // device address of the per-device status word
 };
 

@@ -46,7 +46,10 @@ namespace {
 constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr int kMaxWeightBytes = 96 * 1024;  // weight planes a CTA holds in shared memory
+// Static shared memory of a decode CTA (the row-quantisation scratch, the
+// barriers and the per-token scalars: 4 KB by ptxas for every instance), for
+// the two-CTAs-per-SM budget below.
+constexpr int kDecStaticSmem = 4352;
 constexpr int kMaxNJ = 8;                   // fused mode: K <= kDecThreads * 4 * kMaxNJ
 
 struct DecodeMat {
@@ -607,8 +610,9 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
 }
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
-// their rows, with at most kMaxWeightBytes of weights and at most 512 rows a
-// CTA (more CTAs, in further waves, where a matrix needs it).  A gated pair
+// their rows, with at most 512 rows a CTA and no more weights than leave room
+// for two CTAs on an SM -- this launch's and the next one's, or two of a tall
+// matrix's (more CTAs, in further waves, where a matrix needs it).  A gated pair
 // (two matrices of equal N) splits as one matrix whose rows weigh double:
 // every CTA holds the same rows of both.  Returns the total CTA count.
 int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm, bool gated,
@@ -625,7 +629,9 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   // for the 512-row maximum here) and gamma.
   const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 -
                        (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);
-  int64_t rows_cap = (room < kMaxWeightBytes ? room : kMaxWeightBytes) / row_bytes;
+  const int64_t pair = (int64_t)dev.smem_per_sm / 2 - 1024 - kDecStaticSmem -
+                       (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);  // two CTAs an SM
+  int64_t rows_cap = (room < pair ? room : pair) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
   if (rows_cap * per > kDecThreads) rows_cap = kDecThreads / per;
   // Each matrix's share of the SMs in proportion to its rows, rounded down and
