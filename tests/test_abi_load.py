@@ -110,6 +110,15 @@ def test_linear_gated_argument_errors(lib):
     assert f(A, None, 0, 128, None, 1e-6, same, 2, A, A, G, None) == 0       # empty batch
 
 
+def test_linear_matrix_count_errors(lib):
+    f = lib.bitlinear_linear
+    w = bl.BitLinearWeight(A, A, 64, A, None)
+    five = (bl.BitLinearWeight * 5)(w, w, w, w, w)
+    assert f(A, None, 1, 128, None, 1e-6, five, 5, A, A, 0, None) == -2      # more than four matrices
+    assert f(A, None, 1, 128, None, 1e-6, five, 0, A, A, 0, None) == -2      # none
+    assert f(A, None, 1, 128, None, 1e-6, None, 1, A, A, 0, None) == -1      # NULL array
+
+
 def test_quant_act_argument_errors(lib):
     f = lib.bitlinear_quant_act
     assert f(None, None, 1, 64, None, 1e-6, A, A, None) == -1

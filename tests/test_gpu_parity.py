@@ -373,6 +373,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (256, 8192, (2048,), "gated+norm"),     # a 1.3B FFN down call in the WIDE region
     (64, 8192, (2048, 300), "gated"),       # long K at M = 64: batched kernel, K split in a cluster
     (136, 8192, (1000, 300), "gated"),      # long K above 128 tokens: WIDE (with ws)
+    (1, 2048, (300, 1000, 64, 7), "norm"),  # four matrices (the most one call takes), fused M = 1
+    (40, 1024, (257, 100, 1000, 33), None), # four matrices on the batched kernel
+    (5, 640, (500, 77, 1300, 16), "gated"), # four matrices on the decode kernel after act_quant
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_matches_oracle(M, K, Ns, prolog, ws):
