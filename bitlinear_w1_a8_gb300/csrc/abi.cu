@@ -76,8 +76,9 @@ constexpr int64_t kDecodeMaxK = 65536;
 constexpr int64_t kPrefillMaxK = 131072;
 // AUTO, from timings on GB300 over the BitNet-3B shapes (back-to-back calls):
 //  * the decode kernel (dp4a; its work grows with every token) for a few
-//    tokens: M <= 4 always, M <= 8, and M <= 16 when K < 8192, unless the
-//    output is very wide (N >= 32768, e.g. a 50000-row LM head);
+//    tokens: M <= 4 always, M <= 8 (very wide outputs, N >= 32768 such as a
+//    50000-row LM head, only for K <= 4096), and M <= 16 when K < 8192 and the
+//    output is narrower;
 //  * the batched tensor-core kernel (weight rows on the MMA's M side, all
 //    tokens in one tile) for outputs up to 8192 rows up to M = 128;
 //  * the tensor-core kernel with 128-token tiles otherwise (both tensor-core
@@ -85,6 +86,10 @@ constexpr int64_t kPrefillMaxK = 131072;
 //    than half the SMs).
 int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
+  // A very wide output at up to 8 tokens too, where its CTAs fit two an SM
+  // (the 50000-row LM head at K = 2560: 23.8 / 33.2 us against 46.9 / 40.7 on
+  // 128-token tiles at M = 5 / 8)
+  if (M <= 8 && K <= 4096) return BITLINEAR_ALGO_DECODE;
   if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
   // Measured on GB300 (BitNet-3B projections, back-to-back calls): the dp4a
   // decode kernel wins up to 8 tokens on every shape and up to 16 for K < 8192;

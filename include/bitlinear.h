@@ -152,8 +152,8 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *                 integer accumulators (for checking and debugging).
  * The kernel is chosen from M, N and K (BITLINEAR_ALGO_AUTO): the decode
  * kernel (packed weights bulk-copied into shared memory, dp4a on the 2-bit
- * codes; K <= 65536) for M <= 4, and for M <= 8 (M <= 16 when K < 8192)
- * when N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
+ * codes; K <= 65536) for M <= 4, for M <= 8 when K <= 4096 or N < 32768, and
+ * for M <= 16 when K < 8192 and N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
  * MMA's M side, all tokens on its N side) for N <= 8192 and M <= 128; the
  * tcgen05 kernel with 128-token tiles (K <= 131072) otherwise.  Both
  * tensor-core kernels split K over up to 8 CTAs when their tiles fill less
