@@ -363,6 +363,21 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
       pre[npre++] = mats[i];
     }
   }
+  // Above 12 tokens the decode kernel's dots outweigh its gains once a launch
+  // holds many rows: such a group goes to the tensor-core kernels (BitNet-3B
+  // layers of calls at M = 16, gate || up's 20480 rows: 77.3 -> 69.4 us a
+  // layer; at M = 12 no change).
+  if (M > 12 && ndec > 0) {
+    int64_t drows = 0;
+    for (int i = 0; i < ndec; ++i) drows += dec[i].N;
+    if (drows >= 16384) {
+      for (int i = 0; i < ndec; ++i) {
+        if (dec[i].N <= 8192) bat[nbat++] = dec[i];
+        else pre[npre++] = dec[i];
+      }
+      ndec = 0;
+    }
+  }
   // A gated pair that the decode kernel takes is gated in its epilogue; on
   // any other kernel one elementwise launch follows.
   const bool gate_in_decode = gated && ndec == 2;

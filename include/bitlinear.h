@@ -267,7 +267,8 @@ typedef struct bitlinear_weight {
  * Otherwise it runs bitlinear_quant_act, then one launch per kernel that
  * bitlinear_forward's AUTO rule picks for some matrix: the matrices given to
  * the same kernel (decode, batched or 128-token-tile) share one grid, whose
- * tiles span all of them.
+ * tiles span all of them -- except that above 12 tokens matrices of 16384
+ * rows or more together leave the decode kernel for the tensor-core ones.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream);

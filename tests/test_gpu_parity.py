@@ -376,6 +376,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 2048, (300, 1000, 64, 7), "norm"),  # four matrices (the most one call takes), fused M = 1
     (40, 1024, (257, 100, 1000, 33), None), # four matrices on the batched kernel
     (5, 640, (500, 77, 1300, 16), "gated"), # four matrices on the decode kernel after act_quant
+    (16, 2560, (10240, 10240), None),       # 16 tokens, 20480 rows: the tensor-core kernels, not decode
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_matches_oracle(M, K, Ns, prolog, ws):
@@ -471,6 +472,7 @@ def _f32_outputs(acc, sx, sw):
     (2, 2560, 10240, False),    # the same at BitNet-3B gate || up widths
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
     (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
+    (16, 2560, 10240, False),   # 16 tokens, 20480 rows: 128-token tiles, then the elementwise gating
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_gated(M, K, N, norm, ws):
