@@ -86,19 +86,21 @@ constexpr int64_t kPrefillMaxK = 131072;
 //    than half the SMs).
 int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
-  // A very wide output at up to 8 tokens too, where its CTAs fit two an SM
-  // (the 50000-row LM head at K = 2560: 23.8 / 33.2 us against 46.9 / 40.7 on
-  // 128-token tiles at M = 5 / 8)
-  if (M <= 8 && K <= 4096) return BITLINEAR_ALGO_DECODE;
-  if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
-  // Measured on GB300 (BitNet-3B projections, back-to-back calls): the dp4a
-  // decode kernel wins up to 8 tokens on every shape and up to 16 for K < 8192;
-  // beyond, the batched tensor-core kernel (weight rows on the MMA's M side, K
-  // split inside a cluster) wins up to 64 column tiles, and the 128-token-tile
-  // kernel on wider outputs (M = 32: q||k||v 13.1 vs 20.8 us, o 8.5 vs 12.5,
-  // down 15.5 vs 22.4; gate||up 30.3 vs 23.4).
-  if (M <= 8 && K <= 65536) return BITLINEAR_ALGO_DECODE;
+  // Measured on GB300 (BitNet-3B projections, back-to-back calls, us a call,
+  // decode / batched / 128-token tiles): from 5 tokens the decode kernel runs
+  // its dots on the warp-level MMA in 8- or 16-token groups and wins up to 16
+  // tokens wherever those groups fit (K < 8192), the very wide LM head
+  // included (10240 x 2560 at M = 16: 9.4 / 18.1 / 20.5; 50000 x 2560 at
+  // M = 12 / 16: 33.6 / 35.4 against 40.9 / 40.4 on 128-token tiles); at
+  // long K (10240: 4-token dp4a groups) up to 8 tokens (2560 x 10240 at
+  // M = 8: 12.4 / 14.4 / 22.1).  Beyond, the batched tensor-core kernel
+  // (weight rows on the MMA's M side, K split inside a cluster) wins up to 64
+  // column tiles, and the 128-token-tile kernel on wider outputs (M = 32:
+  // q||k||v 13.0 vs 18.8, o 8.4 vs 12.3, down 15.3 vs 22.3; 10240 x 2560
+  // 19.6 vs 20.5 batched, 14.8 decode -- slower inside a layer's chain).
   if (M <= 16 && K < 8192) return BITLINEAR_ALGO_DECODE;
+  if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
+  if (M <= 8 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   if (M <= 128 && N <= 8192) return BITLINEAR_ALGO_BATCHED;
   return BITLINEAR_ALGO_PREFILL;
 }
@@ -124,6 +126,13 @@ bool wide_wins(int64_t M, int64_t N, int64_t K) {
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values
 // in shared memory next to the weights.
 constexpr int64_t kFusedMaxK = 16384;
+
+// The decode grid's height (token groups) stays within the launch limit.
+bool decode_grid_ok(int64_t M, int64_t K) {
+  bool mma = false;
+  const int64_t group = decode_token_group(M, K, &mma);
+  return (M + group - 1) / group <= 65535;
+}
 
 bitlinear_status check_nk(int64_t N, int64_t K) {
   if (N <= 0 || K <= 0 || N > kMaxDim || K > kMaxDim) return BITLINEAR_ERR_SHAPE;
@@ -235,7 +244,7 @@ bitlinear_status forward_impl(const int8_t* xq, const float* x_scale, int64_t M,
     use = auto_algo(M, N, K);
     if (use != BITLINEAR_ALGO_DECODE && have_ws && K <= kPrefillMaxK && wide_wins(M, N, K)) use = BITLINEAR_ALGO_WIDE;
   }
-  if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || (M + 7) / 8 > 65535))
+  if (use == BITLINEAR_ALGO_DECODE && (K > kDecodeMaxK || !decode_grid_ok(M, K)))
     return BITLINEAR_ERR_UNSUPPORTED;
   if ((use == BITLINEAR_ALGO_PREFILL || use == BITLINEAR_ALGO_WIDE) && K > kPrefillMaxK)
     return BITLINEAR_ERR_UNSUPPORTED;
@@ -363,26 +372,11 @@ bitlinear_status linear_impl(const float* x, const float* mul, int64_t M, int64_
       pre[npre++] = mats[i];
     }
   }
-  // Above 12 tokens the decode kernel's dots outweigh its gains once a launch
-  // holds many rows: such a group goes to the tensor-core kernels (BitNet-3B
-  // layers of calls at M = 16, gate || up's 20480 rows: 77.3 -> 69.4 us a
-  // layer; at M = 12 no change).
-  if (M > 12 && ndec > 0) {
-    int64_t drows = 0;
-    for (int i = 0; i < ndec; ++i) drows += dec[i].N;
-    if (drows >= 16384) {
-      for (int i = 0; i < ndec; ++i) {
-        if (dec[i].N <= 8192) bat[nbat++] = dec[i];
-        else pre[npre++] = dec[i];
-      }
-      ndec = 0;
-    }
-  }
   // A gated pair that the decode kernel takes is gated in its epilogue; on
   // any other kernel one elementwise launch follows.
   const bool gate_in_decode = gated && ndec == 2;
   if (ndec > 0) {
-    if ((M + 7) / 8 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
+    if (!decode_grid_ok(M, K)) return BITLINEAR_ERR_UNSUPPORTED;
     err = launch_decode(xq, x_scale, M, dec, ndec, K, gate_in_decode, pdl, dev, s);
     if (err != cudaSuccess) return BITLINEAR_ERR_CUDA;
   }

@@ -35,9 +35,16 @@
 //    combined with exact shifts and subtracting the row sum of x gives
 //    sum Wq*x (the ternary add/sub) exactly.  On GB300 the dp4a pipe accepts
 //    about 32 per clock per SM, which bounds this phase;
-//  * each chunk's sum meets its row's others in shared memory (an int32
-//    atomic, exact in any order), then one thread per row rescales (and, for
-//    a gated pair, writes ReLU^2(gate) * up).
+//  * dots for 8 or 16 tokens (int8 input): the warp-level fp16 MMA
+//    (m16n8k16, fp32 sums; ~950 multiply-adds per clock per SM on GB300
+//    against dp4a's ~128, while its int8 form runs at a quarter of that).
+//    The masked code words are the A fragments as they are (fp16 subnormals
+//    c * 2^-24, exact), each warp works through a contiguous piece of the
+//    CTA's (16-row tile group, k-block) space, and every 8 tokens are one
+//    column tile; see the dot phase for the k matching and the exactness;
+//  * each chunk's or piece's sum meets its row's others in shared memory (an
+//    int32 atomic, exact in any order), then one thread per row rescales
+//    (and, for a gated pair, writes ReLU^2(gate) * up).
 #include "quant_row.cuh"
 
 namespace bitlinear {
@@ -76,6 +83,7 @@ struct DecodeParams {
   float* sx_out;
   int* status;
   int M, K, KB;
+  int XS;           // bytes from one token row of xs to the next (K, or K + 64 for the MMA dots)
   int rows_max;     // max rows of a CTA over all matrices
   uint32_t off_xs;  // byte offsets in dynamic shared memory: int8 activations,
   uint32_t off_red; //   int32 row sums,
@@ -160,6 +168,26 @@ __device__ __forceinline__ int chunk_dot(const uint4 wv, const int4* xp) {
   }
   // a_s is an exact multiple of 4^s: the shifts are exact
   return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+}
+
+// D += A * B for one 16 x 8 x 16 fp16 tile with fp32 accumulation (the warp-level MMA)
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four int8 activations (bytes 0..3 of X) as two fp16 pairs (bytes 0, 2) and
+// (bytes 1, 3), exactly: with u = X ^ 0x80 per byte (the value + 128), the half
+// with bits 0x64uu is 1024 + u, and subtracting 1152 leaves the value.
+__device__ __forceinline__ void int8x4_to_f16x2x2(uint32_t X, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = X ^ 0x80808080u;
+  const uint32_t e = __byte_perm(u, 0x64646464u, 0x4240);
+  const uint32_t o = __byte_perm(u, 0x64646464u, 0x4341);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(e), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(o), "r"(0x64806480u));
 }
 
 // Fused-mode quantisation of one token row held in registers: thread t owns
@@ -387,10 +415,12 @@ __device__ __forceinline__ void quantize_rows_regs(const float* __restrict__ x, 
 }
 
 // Dynamic shared memory: the CTA's weight planes at 0 (plane kb holds rows
-// r0 .. r1-1 as R consecutive 16-byte chunks), xs[MT][K] int8 activations at
+// r0 .. r1-1 as R consecutive 16-byte chunks), xs[MT][XS] int8 activations at
 // off_xs, red[MT][R] int32 row sums at off_red, (fused RMSNorm) gamma at off_gs.
-template <int MT, bool FUSED, bool NORM, int NJ>
+// MMA: the dots run on the warp-level fp16 MMA instead of dp4a (int8 input).
+template <int MT, bool FUSED, bool NORM, int NJ, bool MMA = false>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+  static_assert(!(MMA && FUSED), "the MMA dots take int8 token rows");
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ int sumx[MT];
   __shared__ float den[2][MT];  // sx * sw of each token, for mats[mi] and (gated) mats[1]
@@ -484,8 +514,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   } else {
     // int8 rows -> shared memory in one round trip (cp.async bypasses the registers)
     const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K);
+    const int K16 = K >> 4, XS16 = p.XS >> 4;
     int4* dst = reinterpret_cast<int4*>(xs);
-    for (int i = t; i < mcount * (K >> 4); i += kDecThreads) cp_async16_row(dst + i, src + i);
+    int m = t / K16, j = t - m * K16;  // element t + 512 i of the rows laid end to end
+    for (int i = t; i < mcount * K16; i += kDecThreads) {
+      cp_async16_row(dst + (m * XS16 + j), src + i);
+      j += kDecThreads;
+      while (j >= K16) {
+        j -= K16;
+        ++m;
+      }
+    }
     if (t < MT) {
       den[0][t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw) : 1.0f;
       den[1][t] = t < mcount ? __fmul_rn(p.sx_in[m0 + t], sw1) : 1.0f;
@@ -494,9 +533,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     __syncthreads();
     // Row sums of the activations (the bias of the biased codes c = Wq + 1);
     // read after the barrier that ends the dots.
-    const int K16 = K >> 4;
     for (int m = 0; m < mcount; ++m) {
-      const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * K);
+      const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.XS);
       int s = 0;
       for (int i = t; i < K16; i += kDecThreads) {
         const int4 v = row[i];
@@ -513,10 +551,92 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   // The weights have landed (bounded wait; on timeout the status word says so
   // and the outputs are not written).
   const bool have_w = bar_wait(&wbar, p.status) && have_g;
-  if (have_w) {
+  if (MMA && have_w) {
+    // Warp-level MMA, 16 weight rows x 8 tokens x 16 k a step, fp32 sums.
+    // Thread (g = lane / 4, q = lane % 4) of a warp takes, in every 64-k
+    // block, code word q of rows g and g + 8 and the 16 activations
+    // 16q .. 16q + 15 of token g: the MMA sums over its 16 k in any order, so
+    // the k of the fragments are matched up rather than laid out in order.
+    // A code word w (code of k = 16q + i at bit 8 (i % 4) + 2 (i / 4)) gives,
+    // per 16-bit half, w & 0x0003 -> c and w & 0x000C -> 4c: the fp16 with
+    // those bits is the subnormal c * 2^-24 or 4c * 2^-24, exact, and so is
+    // every product with an int8 activation.  The fp32 sums stay exact integer
+    // multiples of 2^-24 (of 2^-22 for the 4c terms, kept in their own
+    // accumulator) below 2^24 of those units for K <= 131072, and scale back
+    // to int32 exactly.  The activations are widened per use (two byte
+    // permutes and an fp16 subtract per pair).
+    constexpr int NT = MT >= 8 ? MT / 8 : 1;  // 8-token column tiles
+    constexpr int TT = NT == 1 ? 2 : 1;       // 16-row tiles of a unit (register budget)
+    constexpr uint32_t M0 = 0x00030003u, M1 = 0x000C000Cu;
+    const int warp = t >> 5, g = lane >> 2, q = lane & 3;
+    const int NG = (((RR + 15) >> 4) + TT - 1) / TT;  // row-tile groups
+    const uint32_t* w32 = reinterpret_cast<const uint32_t*>(dsmem);
+    int xrow[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) xrow[nt] = min(nt * 8 + g, MT - 1) * p.XS + 16 * q;
+    // The (group, k-block) space in group-major order, cut into one piece a
+    // warp; a piece that crosses into the next group flushes its sums there.
+    const int total = NG * KB;
+    int pos = (int)((int64_t)warp * total / kDecWarps);
+    const int end = (int)((int64_t)(warp + 1) * total / kDecWarps);
+    while (pos < end) {
+      const int gi = pos / KB, kb0 = pos - gi * KB;
+      const int kb1 = min(KB, kb0 + (end - pos));
+      pos += kb1 - kb0;
+      float acc[TT][NT][2][4];
+#pragma unroll
+      for (int ti = 0; ti < TT; ++ti)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[ti][nt][0][i] = acc[ti][nt][1][i] = 0.0f;
+      const int rbase = gi * TT * 16 + g;  // rows past RR read a valid row; their sums are dropped
+      for (int kb = kb0; kb < kb1; ++kb) {
+        uint32_t bf[NT][4][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + xrow[nt] + kb * 64);
+          int8x4_to_f16x2x2(xv.x, bf[nt][0][0], bf[nt][0][1]);
+          int8x4_to_f16x2x2(xv.y, bf[nt][1][0], bf[nt][1][1]);
+          int8x4_to_f16x2x2(xv.z, bf[nt][2][0], bf[nt][2][1]);
+          int8x4_to_f16x2x2(xv.w, bf[nt][3][0], bf[nt][3][1]);
+        }
+        const uint32_t* wp = w32 + (size_t)kb * RR * 4;
+#pragma unroll
+        for (int ti = 0; ti < TT; ++ti) {
+          // word s of the activations holds k = 16q + 4s + (0, 1, 2, 3); the
+          // code pairs (4s, 4s + 2) and (4s + 1, 4s + 3) match its halves
+          const uint32_t wa = wp[min(rbase + ti * 16, RR - 1) * 4 + q];
+          const uint32_t wb = wp[min(rbase + ti * 16 + 8, RR - 1) * 4 + q];
+          const uint32_t wa4 = wa >> 4, wb4 = wb >> 4, wa8 = wa >> 8, wb8 = wb >> 8;
+          const uint32_t wa12 = wa >> 12, wb12 = wb >> 12;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(acc[ti][nt][0], wa & M0, wb & M0, wa8 & M0, wb8 & M0, bf[nt][0][0], bf[nt][0][1]);
+            mma_f16(acc[ti][nt][1], wa & M1, wb & M1, wa8 & M1, wb8 & M1, bf[nt][1][0], bf[nt][1][1]);
+            mma_f16(acc[ti][nt][0], wa4 & M0, wb4 & M0, wa12 & M0, wb12 & M0, bf[nt][2][0], bf[nt][2][1]);
+            mma_f16(acc[ti][nt][1], wa4 & M1, wb4 & M1, wa12 & M1, wb12 & M1, bf[nt][3][0], bf[nt][3][1]);
+          }
+        }
+      }
+      // C fragment: (row g, tokens 2q, 2q + 1), then (row g + 8, the same tokens)
+#pragma unroll
+      for (int ti = 0; ti < TT; ++ti)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = (gi * TT + ti) * 16 + g + (i >= 2 ? 8 : 0);
+            const int m = nt * 8 + 2 * q + (i & 1);
+            const int v = __float2int_rn(acc[ti][nt][0][i] * 16777216.0f) +
+                          __float2int_rn(acc[ti][nt][1][i] * 4194304.0f);
+            if (row < RR && m < mcount && v != 0) atomicAdd(&red[m * RR + row], v);
+          }
+    }
+  } else if (have_w) {
     // chunk cc = kb * R + r, dealt out flat: thread t takes t, t + 512, ...
     const int4* xs4 = reinterpret_cast<const int4*>(xs);
-    const int K16 = K >> 4;
+    const int XS16 = p.XS >> 4;
     const int C = RR * KB;
     const int dq = kDecThreads / RR, dr = kDecThreads - dq * RR;
     int kb = t / RR, r = t - kb * RR;
@@ -525,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
       const uint4 wv = wsm[cc];
 #pragma unroll
       for (int m = 0; m < MT; ++m)
-        if (m < mcount) atomicAdd(&red[m * RR + r], chunk_dot(wv, xs4 + m * K16 + kb * 4));
+        if (m < mcount) atomicAdd(&red[m * RR + r], chunk_dot(wv, xs4 + m * XS16 + kb * 4));
       kb += dq;
       r += dr;
       if (r >= RR) {
@@ -569,29 +689,35 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest(int* status, unsigne
   if (threadIdx.x == 0) bar_wait(&bar, status, limit_ns);
 }
 
+// Bytes from one token row of xs to the next: K, or for the MMA dots K
+// rounded to an odd multiple of 64, so that the 8 token rows of a warp's
+// 16-byte activation loads fall on distinct shared-memory banks.
+int64_t decode_xs_stride(int64_t K, bool mma) { return mma && K % 128 == 0 ? K + 64 : K; }
+
 // Bytes of dynamic shared memory besides the weight planes.
-size_t decode_front_bytes(int64_t K, int mt, int rows_max, bool norm) {
-  size_t b = (size_t)mt * K;                               // xs
+size_t decode_front_bytes(int64_t K, int64_t xs_stride, int mt, int rows_max, bool norm) {
+  size_t b = (size_t)mt * xs_stride;                       // xs
   b = ((b + 15) & ~(size_t)15) + (size_t)mt * rows_max * 4;  // red
   b = (b + 15) & ~(size_t)15;
   if (norm) b += (size_t)K * 4;                            // gamma
   return (b + 127) & ~(size_t)127;
 }
 
-template <int MT, bool FUSED, bool NORM, int NJ>
+template <int MT, bool FUSED, bool NORM, int NJ, bool MMA = false>
 cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
+  if (p.XS != decode_xs_stride(p.K, MMA)) return cudaErrorInvalidValue;
   const size_t wbytes = ((size_t)p.rows_max * p.KB * 16 + 127) & ~(size_t)127;
   p.off_xs = (uint32_t)wbytes;
-  p.off_red = (uint32_t)(((wbytes + (size_t)MT * p.K) + 15) & ~(size_t)15);
+  p.off_red = (uint32_t)(((wbytes + (size_t)MT * p.XS) + 15) & ~(size_t)15);
   p.off_gs = (uint32_t)((p.off_red + (size_t)MT * p.rows_max * 4 + 15) & ~(size_t)15);
-  const size_t smem = wbytes + decode_front_bytes(p.K, MT, p.rows_max, NORM);
+  const size_t smem = wbytes + decode_front_bytes(p.K, p.XS, MT, p.rows_max, NORM);
   const size_t limit = dev.smem_optin - sizeof(RowQuantScratch) - 1024;
   if (smem > limit) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     static thread_local int configured_device = -1;
     if (configured_device != dev.device) {
       cudaError_t err =
-          cudaFuncSetAttribute(decode_kernel<MT, FUSED, NORM, NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+          cudaFuncSetAttribute(decode_kernel<MT, FUSED, NORM, NJ, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
       if (err != cudaSuccess) return err;
       configured_device = dev.device;
     }
@@ -606,7 +732,7 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NORM, NJ>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NORM, NJ, MMA>, p);
 }
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
@@ -616,21 +742,22 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
 // (two matrices of equal N) splits as one matrix whose rows weigh double:
 // every CTA holds the same rows of both.  Returns the total CTA count.
 int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm, bool gated,
-                const DeviceInfo& dev) {
+                const DeviceInfo& dev, bool mma = false) {
   p.K = (int)K;
   p.KB = (int)(K / 64);
+  p.XS = (int)decode_xs_stride(K, mma);
   p.nmats = nmats;
   p.gated = gated ? 1 : 0;
   const int per = gated ? 2 : 1;  // weight rows a CTA holds per output row
   int64_t all_rows = 0;
   for (int i = 0; i < (gated ? 1 : nmats); ++i) all_rows += mats[i].N;
-  const int64_t row_bytes = (int64_t)p.KB * 16 * per;
-  // Shared memory left for weights next to the activations, row sums (sized
-  // for the 512-row maximum here) and gamma.
-  const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 -
-                       (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);
-  const int64_t pair = (int64_t)dev.smem_per_sm / 2 - 1024 - kDecStaticSmem -
-                       (int64_t)decode_front_bytes(K, mt, kDecThreads, norm);  // two CTAs an SM
+  // Shared memory a CTA row costs: its weights and its row sums (one int32 a
+  // token); besides them the activations and gamma, and a little for the
+  // alignment of each part.
+  const int64_t row_bytes = ((int64_t)p.KB * 16 + (int64_t)mt * 4) * per;
+  const int64_t fixed = (int64_t)decode_front_bytes(K, p.XS, mt, 0, norm) + 384;
+  const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 - fixed;
+  const int64_t pair = (int64_t)dev.smem_per_sm / 2 - 1024 - kDecStaticSmem - fixed;  // two CTAs an SM
   int64_t rows_cap = (room < pair ? room : pair) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
   if (rows_cap * per > kDecThreads) rows_cap = kDecThreads / per;
@@ -705,6 +832,20 @@ cudaError_t launch_fused(const DecodeParams& p, int grid, int nj, bool pdl, cons
 
 }  // namespace
 
+// Token groups of up to 16 tokens whose activations stay within 64 KB.  A
+// group of 8 or 16 (one or two 8-token column tiles of the warp-level MMA)
+// takes the MMA dots; a smaller one dp4a, which at 3-4 tokens beats MMAs
+// whose column tiles would be half empty (and at K = 10240, where 8 tokens
+// of activations do not fit, 4-token dp4a groups beat 8-token MMA groups
+// with fewer weight rows a CTA: 12.4 vs 14.6 us a call at M = 8).
+int decode_token_group(int64_t M, int64_t K, bool* mma) {
+  int mt = M <= 2 ? (int)(M < 1 ? 1 : M) : (M <= 4 ? 4 : (M <= 8 ? 8 : 16));
+  while (mt > 8 && (int64_t)mt * decode_xs_stride(K, true) > 65536) mt >>= 1;
+  *mma = mt >= 8 && (int64_t)mt * decode_xs_stride(K, true) <= 65536;
+  while (!*mma && mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
+  return mt;
+}
+
 cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const DecodeMatrix* mats, int nmats,
                           int64_t K, bool gated, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
   DecodeParams p = {};
@@ -712,15 +853,16 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   p.sx_in = sx;
   p.status = dev.status;
   p.M = (int)M;
-  // Token group: up to 8 tokens whose activations (MT * K bytes) fit in 64 KB.
-  int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
-  while (mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
-  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev);
+  bool mma = false;
+  const int mt = decode_token_group(M, K, &mma);
+  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev, mma);
   switch (mt) {
     case 1: return launch_mt<1, false, false, 1>(p, grid, pdl, dev, stream);
     case 2: return launch_mt<2, false, false, 1>(p, grid, pdl, dev, stream);
     case 4: return launch_mt<4, false, false, 1>(p, grid, pdl, dev, stream);
-    default: return launch_mt<8, false, false, 1>(p, grid, pdl, dev, stream);
+    case 8: return mma ? launch_mt<8, false, false, 1, true>(p, grid, pdl, dev, stream)
+                       : launch_mt<8, false, false, 1>(p, grid, pdl, dev, stream);
+    default: return launch_mt<16, false, false, 1, true>(p, grid, pdl, dev, stream);
   }
 }
 

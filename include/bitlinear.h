@@ -151,9 +151,11 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  *   acc           device int32 [M, N] or NULL; when given it receives the raw
  *                 integer accumulators (for checking and debugging).
  * The kernel is chosen from M, N and K (BITLINEAR_ALGO_AUTO): the decode
- * kernel (packed weights bulk-copied into shared memory, dp4a on the 2-bit
- * codes; K <= 65536) for M <= 4, for M <= 8 when K <= 4096 or N < 32768, and
- * for M <= 16 when K < 8192 and N < 32768; the batched tcgen05 kernel (128 weight rows per tile on the
+ * kernel (packed weights bulk-copied into shared memory; K <= 65536; dp4a on
+ * the 2-bit codes for token groups of up to 4, the warp-level fp16 MMA for
+ * groups of 8 or 16 tokens whose activations fit 64 KB of shared memory) for
+ * M <= 4, for M <= 16 when K < 8192, and for M <= 8 when N < 32768; the
+ * batched tcgen05 kernel (128 weight rows per tile on the
  * MMA's M side, all tokens on its N side) for N <= 8192 and M <= 128; the
  * tcgen05 kernel with 128-token tiles (K <= 131072) otherwise.  Both
  * tensor-core kernels split K over up to 8 CTAs when their tiles fill less
@@ -267,8 +269,7 @@ typedef struct bitlinear_weight {
  * Otherwise it runs bitlinear_quant_act, then one launch per kernel that
  * bitlinear_forward's AUTO rule picks for some matrix: the matrices given to
  * the same kernel (decode, batched or 128-token-tile) share one grid, whose
- * tiles span all of them -- except that above 12 tokens matrices of 16384
- * rows or more together leave the decode kernel for the tensor-core ones.
+ * tiles span all of them.
  * Constraints: K % 64 == 0, K <= 32768, every matrix with the same K;
  * BITLINEAR_FLAG_PDL as for bitlinear_forward_ex (the packed weights and
  * scales must not come from the kernel immediately before on the stream);

@@ -107,7 +107,7 @@ def weights():
 
 
 @pytest.mark.parametrize("gated", [False, True])
-@pytest.mark.parametrize("M", [1, 8, 64])
+@pytest.mark.parametrize("M", [1, 8, 16, 64])
 def test_two_layer_schedule_in_one_graph(weights, M, gated):
     layers, g_norm, g_sub = weights
     x0 = synth.activations(M, D, synth.SEEDS["weight_set"]["x"]).cuda()

@@ -46,6 +46,44 @@ def test_shapes(algo, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
+    (3, 1, 64),         # one weight row: every 16-row tile reads a clamped row
+    (4, 17, 64),        # one k-block for all warps
+    (9, 7, 192),        # a 16-token group (two 8-token column tiles) holding 9 tokens
+    (16, 2000, 2560),   # two full column tiles; the xs rows padded to an odd multiple of 64
+    (12, 640, 10240),   # long K: 4-token groups keep the activations within 64 KB
+    (33, 300, 1024),    # three token groups, the last with one token
+    (8, 50000, 128),    # more CTAs than SMs
+])
+def test_decode_mma_shapes(M, N, K):
+    """The decode kernel's warp-level MMA dots (3 tokens and more), forced, on ragged shapes."""
+    W = synth.weight(N, K, 500 + N + K)
+    x = synth.activations(M, K, 600 + M + K, outlier_seed=700 + K)
+    full_parity(W, x, algo=bl.ALGO_DECODE)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 300, 10240), (16, 33, 2560)])
+def test_decode_mma_extreme_values(M, N, K):
+    """int8 inputs at -128 and 127 (the contraction takes any int8, not only act_quant's
+    [-127, 127]) against weights of all +-1: the largest sums the MMA dots meet, exact."""
+    rng = np.random.default_rng(M * 1000 + K)
+    xq = np.where(rng.random((M, K)) < 0.5, -128, 127).astype(np.int8)
+    xq[0, :] = -128                                   # one row at the int8 minimum throughout
+    Wq = np.where(rng.random((N, K)) < 0.5, -1, 1).astype(np.int8)
+    Wq[0, :] = 1
+    Wq[1 % N, :] = -1
+    sx = np.full(M, 0.5, np.float32)
+    sw = np.float32(1.0)
+    packed = oracle.pack(Wq)
+    acc_o, y_o = oracle.forward(xq, sx, packed, float(sw), N, K)
+    assert acc_o[0, 0] == -128 * K
+    acc_g, y_g = gpu_forward(torch.from_numpy(xq).cuda(), torch.from_numpy(sx).cuda(),
+                             torch.from_numpy(packed).cuda(), torch.tensor([sw]).cuda(), N,
+                             algo=bl.ALGO_DECODE)
+    np.testing.assert_array_equal(acc_g, acc_o)
+    assert max_rel_err(y_g, y_o) <= Y_RTOL
+
+
+@pytest.mark.parametrize("M,N,K", [
     (1, 1, 64), (2, 1, 128), (1, 80, 64), (3, 300, 192), (5, 1000, 640), (8, 153, 128),
     (17, 2000, 256), (64, 512, 512), (100, 257, 320), (128, 130, 64), (16, 50000, 128),
 ])
@@ -276,6 +314,19 @@ def _sampled_parity(W, x, rows, cols, algo, workspace=False):
     return acc_g, y_g
 
 
+@pytest.mark.parametrize("M", [12, 16])
+def test_lm_head_few_tokens_decode(M):
+    """The 50000 x 2560 LM head at 12 and 16 tokens: AUTO takes the decode kernel with
+    MMA dots (16-token groups over 300+ CTAs in waves); sampled outputs and every
+    token row's codes against the oracle."""
+    W = synth.weight(50000, 2560, 4321)
+    x = synth.activations(M, 2560, 4322, outlier_seed=4323)
+    rng = np.random.default_rng(1)
+    rows = np.arange(M)
+    cols = np.unique(np.concatenate([rng.choice(50000, 200, replace=False), [0, 15, 16, 49999]]))
+    _sampled_parity(W, x, rows, cols, bl.ALGO_AUTO)
+
+
 @pytest.mark.parametrize("path", ["tiles128", "wide"])
 @pytest.mark.parametrize("name,N,K,seed", [("up_shape", synth.FFN_3B, synth.DIM_3B, "W_up_shape"),
                                             ("down_shape", synth.DIM_3B, synth.FFN_3B, "W_down_shape")])
@@ -376,7 +427,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 2048, (300, 1000, 64, 7), "norm"),  # four matrices (the most one call takes), fused M = 1
     (40, 1024, (257, 100, 1000, 33), None), # four matrices on the batched kernel
     (5, 640, (500, 77, 1300, 16), "gated"), # four matrices on the decode kernel after act_quant
-    (16, 2560, (10240, 10240), None),       # 16 tokens, 20480 rows: the tensor-core kernels, not decode
+    (16, 2560, (10240, 10240), None),       # 16 tokens, 20480 rows: one decode launch, MMA dots
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_matches_oracle(M, K, Ns, prolog, ws):
@@ -472,7 +523,8 @@ def _f32_outputs(acc, sx, sw):
     (2, 2560, 10240, False),    # the same at BitNet-3B gate || up widths
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
     (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
-    (16, 2560, 10240, False),   # 16 tokens, 20480 rows: 128-token tiles, then the elementwise gating
+    (16, 2560, 10240, False),   # 16 tokens, 20480 rows: decode (MMA dots), gated in its epilogue
+    (12, 10240, 2560, False),   # long K above 8 tokens: batched tensor-core kernel, then the gating
 ])
 @pytest.mark.parametrize("ws", [False, True])
 def test_linear_gated(M, K, N, norm, ws):
