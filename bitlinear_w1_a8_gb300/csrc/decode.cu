@@ -421,6 +421,7 @@ __device__ __forceinline__ void quantize_rows_regs(const float* __restrict__ x, 
 template <int MT, bool FUSED, bool NORM, int NJ, bool MMA = false>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(!(MMA && FUSED), "the MMA dots take int8 token rows");
+  static_assert(MT <= kDecWarps, "the activation row sums take at least one warp a token row");
   extern __shared__ __align__(128) uint8_t dsmem[];
   __shared__ int sumx[MT];
   __shared__ float den[2][MT];  // sx * sw of each token, for mats[mi] and (gated) mats[1]
@@ -532,19 +533,24 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // Row sums of the activations (the bias of the biased codes c = Wq + 1);
-    // read after the barrier that ends the dots.
-    for (int m = 0; m < mcount; ++m) {
-      const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.XS);
-      int s = 0;
-      for (int i = t; i < K16; i += kDecThreads) {
-        const int4 v = row[i];
-        s = __dp4a(v.x, 0x01010101, s);
-        s = __dp4a(v.y, 0x01010101, s);
-        s = __dp4a(v.z, 0x01010101, s);
-        s = __dp4a(v.w, 0x01010101, s);
+    // read after the barrier that ends the dots.  The warps split the rows
+    // (kDecWarps / mcount warps a row), so the rows are summed side by side.
+    {
+      const int wpr = kDecWarps / mcount, warp = t >> 5;
+      const int m = warp / wpr;
+      if (m < mcount) {
+        const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.XS);
+        int s = 0;
+        for (int i = (warp - m * wpr) * 32 + lane; i < K16; i += wpr * 32) {
+          const int4 v = row[i];
+          s = __dp4a(v.x, 0x01010101, s);
+          s = __dp4a(v.y, 0x01010101, s);
+          s = __dp4a(v.z, 0x01010101, s);
+          s = __dp4a(v.w, 0x01010101, s);
+        }
+        s = __reduce_add_sync(kFullMask, s);
+        if (lane == 0 && s != 0) atomicAdd(&sumx[m], s);
       }
-      s = __reduce_add_sync(kFullMask, s);
-      if (lane == 0 && s != 0) atomicAdd(&sumx[m], s);
     }
   }
 
