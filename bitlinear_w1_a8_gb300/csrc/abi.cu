@@ -88,17 +88,18 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
   if (M <= 4 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   // Measured on GB300 (BitNet-3B projections, back-to-back calls, us a call,
   // decode / batched / 128-token tiles): from 5 tokens the decode kernel runs
-  // its dots on the warp-level MMA in 8- or 16-token groups and wins up to 16
-  // tokens wherever those groups fit (K < 8192), the very wide LM head
-  // included (10240 x 2560 at M = 16: 9.4 / 18.1 / 20.5; 50000 x 2560 at
-  // M = 12 / 16: 33.6 / 35.4 against 40.9 / 40.4 on 128-token tiles); at
-  // long K (10240: 4-token dp4a groups) up to 8 tokens (2560 x 10240 at
-  // M = 8: 12.4 / 14.4 / 22.1).  Beyond, the batched tensor-core kernel
+  // its dots on the warp-level MMA in 8- or 16-token groups (at long K split
+  // over a cluster) and wins up to 16 tokens, the very wide LM head included
+  // (10240 x 2560 at M = 16: 7.8 / 20.4 / 22.2; 2560 x 10240: 14.0 / 14.4 /
+  // 22.1; 50000 x 2560 at M = 12 / 16: 31.7 / 32.9 against 45.9 / 44.5 on
+  // 128-token tiles; eight BitNet-3B layers of calls at M = 12 / 16: 55.9 /
+  // 57.4 -> 54.1 / 56.2 us a layer with the long-K calls on decode too).
+  // Beyond, the batched tensor-core kernel
   // (weight rows on the MMA's M side, K split inside a cluster) wins up to 64
   // column tiles, and the 128-token-tile kernel on wider outputs (M = 32:
   // q||k||v 13.0 vs 18.8, o 8.4 vs 12.3, down 15.3 vs 22.3; 10240 x 2560
   // 19.6 vs 20.5 batched, 14.8 decode -- slower inside a layer's chain).
-  if (M <= 16 && K < 8192) return BITLINEAR_ALGO_DECODE;
+  if (M <= 16 && K <= 32768) return BITLINEAR_ALGO_DECODE;
   if (N >= 32768 || K > 131072) return BITLINEAR_ALGO_PREFILL;
   if (M <= 8 && K <= 65536) return BITLINEAR_ALGO_DECODE;
   if (M <= 128 && N <= 8192) return BITLINEAR_ALGO_BATCHED;
@@ -130,7 +131,8 @@ constexpr int64_t kFusedMaxK = 16384;
 // The decode grid's height (token groups) stays within the launch limit.
 bool decode_grid_ok(int64_t M, int64_t K) {
   bool mma = false;
-  const int64_t group = decode_token_group(M, K, &mma);
+  int ks = 1;
+  const int64_t group = decode_token_group(M, K, &mma, &ks);
   return (M + group - 1) / group <= 65535;
 }
 

@@ -189,9 +189,10 @@ struct DecodeMatrix {
   int32_t* acc;
 };
 
-// Tokens a decode CTA takes (a token group: gridDim.y is ceil(M / group))
-// and whether its dots run on the warp-level MMA.
-int decode_token_group(int64_t M, int64_t K, bool* mma);
+// Tokens a decode CTA takes (a token group: gridDim.y is ceil(M / group)),
+// whether its dots run on the warp-level MMA, and over how many CTAs of a
+// cluster K is split (1: none).
+int decode_token_group(int64_t M, int64_t K, bool* mma, int* ks);
 
 // gated: nmats == 2 with equal N (gate, up); every CTA takes the same rows of
 // both and mats[0].y receives (r * r) * u with r = max(gate, 0), mats[1].y u.

@@ -83,7 +83,8 @@ struct DecodeParams {
   float* sx_out;
   int* status;
   int M, K, KB;
-  int XS;           // bytes from one token row of xs to the next (K, or K + 64 for the MMA dots)
+  int ksplit;       // CTAs of a thread-block cluster, each taking one K range of the same rows
+  int XS;           // bytes from one token row of xs to the next (the CTA's K range, + 64 for the MMA dots)
   int rows_max;     // max rows of a CTA over all matrices
   uint32_t off_xs;  // byte offsets in dynamic shared memory: int8 activations,
   uint32_t off_red; //   int32 row sums,
@@ -147,6 +148,28 @@ __device__ __forceinline__ void bulk_copy(void* dst_smem, const void* src, uint3
                    smem_addr(dst_smem)),
                "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
+}
+// Thread-block clusters (the K split): this CTA's rank, the split halves of
+// the all-thread cluster barrier, and an atomic add into the shared memory
+// of another CTA of the cluster.
+__device__ __forceinline__ int cluster_rank_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t shared_of_rank(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void red_add_cluster(uint32_t cluster_addr, int v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 // 16-byte load through L2 only (the row was written by the previous kernel).
 __device__ __forceinline__ float4 ld_cg4(const float4* p) {
@@ -430,7 +453,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   __shared__ RowQuantScratch qsc;
 
   const int t = threadIdx.x, lane = t & 31;
-  const int c = blockIdx.x;
+  // With a K split, the ks CTAs of a cluster take the same rows, each one
+  // range of the k-blocks; rank 0 adds up the ranges and writes the outputs.
+  const int ks = MMA ? p.ksplit : 1;  // only the MMA dots take a split
+  const int rank = ks > 1 ? cluster_rank_id() : 0;
+  const int c = ks > 1 ? (int)blockIdx.x / ks : (int)blockIdx.x;
   const bool gated = p.gated != 0;
   int mi = 0;
 #pragma unroll
@@ -444,7 +471,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   const int r1 = (int)(((int64_t)(cl + 1) * mat.N) / mat.G);
   const int R = r1 - r0;
   const int RR = gated ? 2 * R : R;  // rows held: R of mats[mi], then (gated) the same R of mats[1]
-  const int KB = p.KB, K = p.K;
+  const int kb_lo = ks > 1 ? rank * p.KB / ks : 0;
+  const int KB = (ks > 1 ? (rank + 1) * p.KB / ks : p.KB) - kb_lo, K = p.K;  // this CTA's k-blocks
   const uint4* wsm = reinterpret_cast<const uint4*>(dsmem);
   int8_t* xs = reinterpret_cast<int8_t*>(dsmem + p.off_xs);
   int* red = reinterpret_cast<int*>(dsmem + p.off_red);
@@ -465,11 +493,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     }
     __syncwarp();
     if (norm && lane == 0) bulk_copy(gs, p.gamma, (uint32_t)K * 4u, &gbar);
-    const uint4* src = reinterpret_cast<const uint4*>(mat.packed) + r0;
+    const uint4* src = reinterpret_cast<const uint4*>(mat.packed) + (int64_t)kb_lo * mat.N + r0;
     for (int kb = lane; kb < KB; kb += 32)
       bulk_copy((void*)(wsm + (size_t)kb * RR), src + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
     if (gated) {
-      const uint4* src1 = reinterpret_cast<const uint4*>(p.mats[1].packed) + r0;
+      const uint4* src1 = reinterpret_cast<const uint4*>(p.mats[1].packed) + (int64_t)kb_lo * mat.N + r0;
       for (int kb = lane; kb < KB; kb += 32)
         bulk_copy((void*)(wsm + (size_t)kb * RR + R), src1 + (int64_t)kb * mat.N, (uint32_t)R * 16u, &wbar);
     }
@@ -479,6 +507,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
   pdl_release_dependents();
   if (t < MT) sumx[t] = 0;
   for (int i = t; i < MT * RR; i += kDecThreads) red[i] = 0;
+  // K split: the zeroed row sums are released to the other ranks, whose
+  // additions into rank 0's come after the matching wait.
+  if (ks > 1) cluster_arrive();
   // The weight scales, like the weights, do not come from the kernel before
   // (the rule of FLAG_PDL): their loads are off the path after the wait.
   const float sw = t < MT ? *mat.sw : 0.0f;
@@ -514,15 +545,16 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     __syncthreads();
   } else {
     // int8 rows -> shared memory in one round trip (cp.async bypasses the registers)
-    const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K);
-    const int K16 = K >> 4, XS16 = p.XS >> 4;
+    // this CTA's k range of each token row
+    const int4* src = reinterpret_cast<const int4*>(p.xq_in + (int64_t)m0 * K) + kb_lo * 4;
+    const int K16 = K >> 4, R16 = KB * 4, XS16 = p.XS >> 4;
     int4* dst = reinterpret_cast<int4*>(xs);
-    int m = t / K16, j = t - m * K16;  // element t + 512 i of the rows laid end to end
-    for (int i = t; i < mcount * K16; i += kDecThreads) {
-      cp_async16_row(dst + (m * XS16 + j), src + i);
+    int m = t / R16, j = t - m * R16;  // element t + 512 i of the ranges laid end to end
+    for (int i = t; i < mcount * R16; i += kDecThreads) {
+      cp_async16_row(dst + (m * XS16 + j), src + ((int64_t)m * K16 + j));
       j += kDecThreads;
-      while (j >= K16) {
-        j -= K16;
+      while (j >= R16) {
+        j -= R16;
         ++m;
       }
     }
@@ -541,7 +573,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
       if (m < mcount) {
         const int4* row = reinterpret_cast<const int4*>(xs + (size_t)m * p.XS);
         int s = 0;
-        for (int i = (warp - m * wpr) * 32 + lane; i < K16; i += wpr * 32) {
+        for (int i = (warp - m * wpr) * 32 + lane; i < R16; i += wpr * 32) {
           const int4 v = row[i];
           s = __dp4a(v.x, 0x01010101, s);
           s = __dp4a(v.y, 0x01010101, s);
@@ -661,7 +693,26 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const __grid_con
     }
   }
   __syncthreads();
-  if (have_w) {
+  bool write_out = have_w;
+  if (ks > 1) {
+    // Ranks 1 .. ks-1 add their sums, each less its own range's activation
+    // sums, into rank 0's (after rank 0's row sums were zeroed: the wait);
+    // the second barrier makes them visible to rank 0 and keeps rank 0's
+    // shared memory alive until the last of them.  A rank that timed out has
+    // set the status word, and then rank 0 writes nothing.
+    cluster_wait();
+    if (rank != 0 && have_w) {
+      const uint32_t red0 = shared_of_rank(smem_addr(red), 0);
+      for (int i = t; i < mcount * RR; i += kDecThreads) {
+        const int v = red[i] - sumx[i / RR];
+        if (v != 0) red_add_cluster(red0 + 4u * (uint32_t)i, v);
+      }
+    }
+    cluster_arrive();
+    cluster_wait();
+    write_out = have_w && rank == 0 && *reinterpret_cast<volatile int*>(p.status) == 0;
+  }
+  if (write_out) {
     for (int i = t; i < mcount * R; i += kDecThreads) {
       const int m = i / R, rr = i - m * R;
       const int64_t o = (int64_t)(m0 + m) * mat.N + r0 + rr;
@@ -709,10 +760,16 @@ size_t decode_front_bytes(int64_t K, int64_t xs_stride, int mt, int rows_max, bo
   return (b + 127) & ~(size_t)127;
 }
 
+// k-blocks of the widest K range of a split into ks ranges.
+int split_kblocks(int KB, int ks) { return (KB + ks - 1) / ks; }
+
 template <int MT, bool FUSED, bool NORM, int NJ, bool MMA = false>
 cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& dev, cudaStream_t stream) {
-  if (p.XS != decode_xs_stride(p.K, MMA)) return cudaErrorInvalidValue;
-  const size_t wbytes = ((size_t)p.rows_max * p.KB * 16 + 127) & ~(size_t)127;
+  const int ks = p.ksplit;
+  if (ks < 1 || ks > 8 || (ks > 1 && (!MMA || ks > p.KB))) return cudaErrorInvalidValue;
+  const int kbn = split_kblocks(p.KB, ks);
+  if (p.XS != decode_xs_stride((int64_t)kbn * 64, MMA)) return cudaErrorInvalidValue;
+  const size_t wbytes = ((size_t)p.rows_max * kbn * 16 + 127) & ~(size_t)127;
   p.off_xs = (uint32_t)wbytes;
   p.off_red = (uint32_t)(((wbytes + (size_t)MT * p.XS) + 15) & ~(size_t)15);
   p.off_gs = (uint32_t)((p.off_red + (size_t)MT * p.rows_max * 4 + 15) & ~(size_t)15);
@@ -729,15 +786,26 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid_x, (unsigned)((p.M + MT - 1) / MT), 1);
+  cfg.gridDim = dim3((unsigned)(grid_x * ks), (unsigned)((p.M + MT - 1) / MT), 1);
   cfg.blockDim = dim3(kDecThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)ks;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = (unsigned)na;
   return cudaLaunchKernelEx(&cfg, decode_kernel<MT, FUSED, NORM, NJ, MMA>, p);
 }
 
@@ -746,12 +814,15 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
 // for two CTAs on an SM -- this launch's and the next one's, or two of a tall
 // matrix's (more CTAs, in further waves, where a matrix needs it).  A gated pair
 // (two matrices of equal N) splits as one matrix whose rows weigh double:
-// every CTA holds the same rows of both.  Returns the total CTA count.
+// every CTA holds the same rows of both.  With a K split (ks > 1) the unit is
+// a row group of ks CTAs, one K range each.  Returns the total row-group count.
 int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K, int mt, bool norm, bool gated,
-                const DeviceInfo& dev, bool mma = false) {
+                const DeviceInfo& dev, bool mma = false, int ks = 1) {
   p.K = (int)K;
   p.KB = (int)(K / 64);
-  p.XS = (int)decode_xs_stride(K, mma);
+  p.ksplit = ks;
+  const int kbn = split_kblocks(p.KB, ks);  // a CTA's k-blocks (the widest range)
+  p.XS = (int)decode_xs_stride((int64_t)kbn * 64, mma);
   p.nmats = nmats;
   p.gated = gated ? 1 : 0;
   const int per = gated ? 2 : 1;  // weight rows a CTA holds per output row
@@ -760,7 +831,7 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   // Shared memory a CTA row costs: its weights and its row sums (one int32 a
   // token); besides them the activations and gamma, and a little for the
   // alignment of each part.
-  const int64_t row_bytes = ((int64_t)p.KB * 16 + (int64_t)mt * 4) * per;
+  const int64_t row_bytes = ((int64_t)kbn * 16 + (int64_t)mt * 4) * per;
   const int64_t fixed = (int64_t)decode_front_bytes(K, p.XS, mt, 0, norm) + 384;
   const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 - fixed;
   const int64_t pair = (int64_t)dev.smem_per_sm / 2 - 1024 - kDecStaticSmem - fixed;  // two CTAs an SM
@@ -773,7 +844,8 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   // behind the co-resident previous launch and delays the whole grid.
   // (Every matrix has one CTA first; the rest of the SMs are shared out.)
   const int nshare = gated ? 1 : nmats;
-  const int64_t pool = dev.num_sms > nshare ? dev.num_sms - nshare : 0;
+  const int64_t groups = dev.num_sms / ks;  // row groups of ks CTAs
+  const int64_t pool = groups > nshare ? groups - nshare : 0;
   int64_t share[kMaxDecodeMats];
   int64_t left = pool;
   for (int i = 0; i < nshare; ++i) {
@@ -844,10 +916,26 @@ cudaError_t launch_fused(const DecodeParams& p, int grid, int nj, bool pdl, cons
 // whose column tiles would be half empty (and at K = 10240, where 8 tokens
 // of activations do not fit, 4-token dp4a groups beat 8-token MMA groups
 // with fewer weight rows a CTA: 12.4 vs 14.6 us a call at M = 8).
-int decode_token_group(int64_t M, int64_t K, bool* mma) {
-  int mt = M <= 2 ? (int)(M < 1 ? 1 : M) : (M <= 4 ? 4 : (M <= 8 ? 8 : 16));
+int decode_token_group(int64_t M, int64_t K, bool* mma, int* ks) {
+  const int want = M <= 2 ? (int)(M < 1 ? 1 : M) : (M <= 4 ? 4 : (M <= 8 ? 8 : 16));
+  int mt = want;
+  *ks = 1;
   while (mt > 8 && (int64_t)mt * decode_xs_stride(K, true) > 65536) mt >>= 1;
   *mma = mt >= 8 && (int64_t)mt * decode_xs_stride(K, true) <= 65536;
+  if (want >= 8 && !*mma) {
+    // Long K: all the tokens (up to 16) in one group, K split over a
+    // cluster of 2, 4 or 8 CTAs so that a CTA's range of activations fits
+    // (BitNet-3B down, 2560 x 10240: 12.6 -> 8.3 us a call at M = 8, where
+    // 4-token dp4a groups ran before; 14.4 on the batched kernel at M = 16
+    // -> 14.0).
+    const int KB = (int)(K / 64);
+    for (int s = 2; s <= 8 && s <= KB; s *= 2)
+      if ((int64_t)want * decode_xs_stride((int64_t)split_kblocks(KB, s) * 64, true) <= 65536) {
+        *ks = s;
+        *mma = true;
+        return want;
+      }
+  }
   while (!*mma && mt > 1 && (int64_t)mt * K > 65536) mt >>= 1;
   return mt;
 }
@@ -860,8 +948,9 @@ cudaError_t launch_decode(const int8_t* xq, const float* sx, int64_t M, const De
   p.status = dev.status;
   p.M = (int)M;
   bool mma = false;
-  const int mt = decode_token_group(M, K, &mma);
-  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev, mma);
+  int ks = 1;
+  const int mt = decode_token_group(M, K, &mma, &ks);
+  const int grid = plan_decode(p, mats, nmats, K, mt, false, gated, dev, mma, ks);
   switch (mt) {
     case 1: return launch_mt<1, false, false, 1>(p, grid, pdl, dev, stream);
     case 2: return launch_mt<2, false, false, 1>(p, grid, pdl, dev, stream);

@@ -153,8 +153,9 @@ bitlinear_status bitlinear_quant_act(const float* x, const float* mul, int64_t M
  * The kernel is chosen from M, N and K (BITLINEAR_ALGO_AUTO): the decode
  * kernel (packed weights bulk-copied into shared memory; K <= 65536; dp4a on
  * the 2-bit codes for token groups of up to 4, the warp-level fp16 MMA for
- * groups of 8 or 16 tokens whose activations fit 64 KB of shared memory) for
- * M <= 4, for M <= 16 when K < 8192, and for M <= 8 when N < 32768; the
+ * groups of 8 or 16 tokens, with K split over a cluster of 2-8 CTAs when the
+ * group's activations would exceed 64 KB of shared memory) for M <= 16 when
+ * K <= 32768, and for M <= 8 when N < 32768; the
  * batched tcgen05 kernel (128 weight rows per tile on the
  * MMA's M side, all tokens on its N side) for N <= 8192 and M <= 128; the
  * tcgen05 kernel with 128-token tiles (K <= 131072) otherwise.  Both

@@ -50,7 +50,12 @@ def test_shapes(algo, M, N, K):
     (4, 17, 64),        # one k-block for all warps
     (9, 7, 192),        # a 16-token group (two 8-token column tiles) holding 9 tokens
     (16, 2000, 2560),   # two full column tiles; the xs rows padded to an odd multiple of 64
-    (12, 640, 10240),   # long K: 4-token groups keep the activations within 64 KB
+    (12, 640, 10240),   # long K: 16 tokens, K split over a cluster of 4 CTAs
+    (8, 300, 10240),    # K split over a cluster of 2
+    (6, 129, 8256),     # a split into uneven K ranges (129 k-blocks: 64 + 65)
+    (13, 1000, 8192),   # 16-token group, 4 ranges of 32 k-blocks
+    (9, 50, 16384),     # 16-token group, a cluster of 8
+    (16, 100, 32256),   # 8 ranges of 63 k-blocks: the largest split
     (33, 300, 1024),    # three token groups, the last with one token
     (8, 50000, 128),    # more CTAs than SMs
 ])
@@ -524,6 +529,7 @@ def _f32_outputs(acc, sx, sw):
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
     (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
     (16, 2560, 10240, False),   # 16 tokens, 20480 rows: decode (MMA dots), gated in its epilogue
+    (8, 8192, 777, False),      # long K at 8 tokens: decode with K split over a cluster, gated
     (12, 10240, 2560, False),   # long K above 8 tokens: batched tensor-core kernel, then the gating
 ])
 @pytest.mark.parametrize("ws", [False, True])
