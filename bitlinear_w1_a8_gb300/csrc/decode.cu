@@ -12,7 +12,8 @@
 //    which share one input -- split the SMs in proportion to their rows, or,
 //    for a gated gate / up pair, every CTA holds the same rows of both), and
 //    each CTA uses at most half of an SM (512 threads of <= 64 registers,
-//    <= ~110 KB of shared memory), so under programmatic dependent launch the
+//    <= ~110 KB of shared memory; for one or two tokens, whose launches
+//    follow one another directly), so under programmatic dependent launch the
 //    next launch's CTAs are resident while this one runs;
 //  * first thing, before griddepcontrol.wait, warp 0 bulk-copies the RMSNorm
 //    gamma when there is one (on its own mbarrier) and all of the CTA's
@@ -810,9 +811,10 @@ cudaError_t launch_mt(DecodeParams p, int grid_x, bool pdl, const DeviceInfo& de
 }
 
 // Splits the launch's matrices over about one CTA per SM, in proportion to
-// their rows, with at most 512 rows a CTA and no more weights than leave room
-// for two CTAs on an SM -- this launch's and the next one's, or two of a tall
-// matrix's (more CTAs, in further waves, where a matrix needs it).  A gated pair
+// their rows, with at most 512 rows a CTA and, for one or two tokens, no more
+// weights than leave room for two CTAs on an SM -- this launch's and the next
+// one's, or two of a tall matrix's (more CTAs, in further waves, where a
+// matrix needs it).  A gated pair
 // (two matrices of equal N) splits as one matrix whose rows weigh double:
 // every CTA holds the same rows of both.  With a K split (ks > 1) the unit is
 // a row group of ks CTAs, one K range each.  Returns the total row-group count.
@@ -835,7 +837,11 @@ int plan_decode(DecodeParams& p, const DecodeMatrix* mats, int nmats, int64_t K,
   const int64_t fixed = (int64_t)decode_front_bytes(K, p.XS, mt, 0, norm) + 384;
   const int64_t room = (int64_t)dev.smem_optin - (int64_t)sizeof(RowQuantScratch) - 1024 - fixed;
   const int64_t pair = (int64_t)dev.smem_per_sm / 2 - 1024 - kDecStaticSmem - fixed;  // two CTAs an SM
-  int64_t rows_cap = (room < pair ? room : pair) / row_bytes;
+  // Groups of 4 tokens or more come after an act_quant launch, during which
+  // the next decode launch becomes resident anyway: their CTAs may fill an SM
+  // (BitNet-3B token step at M = 16: 1846 -> 1718 us, gate || up's paired
+  // rows no longer cut into 209 CTAs; M = 4 and 8 unchanged).
+  int64_t rows_cap = (mt >= 4 ? room : (room < pair ? room : pair)) / row_bytes;
   if (rows_cap < 1) rows_cap = 1;
   if (rows_cap * per > kDecThreads) rows_cap = kDecThreads / per;
   // Each matrix's share of the SMs in proportion to its rows, rounded down and
