@@ -260,16 +260,20 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
   }
   if constexpr (NORM) {
     // RMSNorm: inv = fp32(1 / sqrt(S/K + eps)) in fp64 from the exact sum S
-    int e = 0;
+    int e = 0, lo = 255;
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
-      if (ok[j])
-        e = max(max(e, max(fp32_exponent(__float_as_uint(h[j].x)), fp32_exponent(__float_as_uint(h[j].y)))),
-                max(fp32_exponent(__float_as_uint(h[j].z)), fp32_exponent(__float_as_uint(h[j].w))));
-    const int emax = block_max_exponent(e, sc);
+      if (ok[j]) {
+        exponent_range_add(__float_as_uint(h[j].x), e, lo);
+        exponent_range_add(__float_as_uint(h[j].y), e, lo);
+        exponent_range_add(__float_as_uint(h[j].z), e, lo);
+        exponent_range_add(__float_as_uint(h[j].w), e, lo);
+      }
+    int emax, emin;
+    block_exponent_range(e, lo, sc, &emax, &emin);
     double S = 0.0;
     bool done = emax == 0;
-    if (!done) {
+    if (!done && emax - emin <= 31) {
       U128 W = {0, 0};
       int far = 0;
 #pragma unroll
@@ -282,7 +286,7 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
       }
       done = block_window0(W, far, emax, sc, &S);
     }
-    if (!done) {
+    if (!done && emax - emin <= 95) {
       U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
       int slow = 0;
 #pragma unroll
@@ -293,19 +297,20 @@ __device__ float quantize_row_regs(const float* __restrict__ x, const float* __r
         sq_window_add(__float_as_uint(h[j].z), emax, A, slow);
         sq_window_add(__float_as_uint(h[j].w), emax, A, slow);
       }
-      if (!block_windows(A, slow, emax, sc, &S)) {
-        zero_buckets(sc);
-        __syncthreads();
+      done = block_windows(A, slow, emax, sc, &S);
+    }
+    if (!done) {
+      zero_buckets(sc);
+      __syncthreads();
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const float4 v = ok[j] ? h[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-          bucket_sq_add(v.x, sc);
-          bucket_sq_add(v.y, sc);
-          bucket_sq_add(v.z, sc);
-          bucket_sq_add(v.w, sc);
-        }
-        S = bucket_fold(sc);
+      for (int j = 0; j < NJ; ++j) {
+        const float4 v = ok[j] ? h[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        bucket_sq_add(v.x, sc);
+        bucket_sq_add(v.y, sc);
+        bucket_sq_add(v.z, sc);
+        bucket_sq_add(v.w, sc);
       }
+      S = bucket_fold(sc);
     }
     // one thread takes the fp64 steps (fp64 is slow on this GPU), the block
     // picks the result up after a barrier

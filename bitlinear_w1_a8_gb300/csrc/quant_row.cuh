@@ -91,15 +91,31 @@ __device__ __forceinline__ void sq_window0_add(uint32_t bits, int emax, U128& W,
   const int sh = 62 - 2 * d;  // 0 .. 62
   add128(W, m2 << sh, sh ? m2 >> (64 - sh) : 0ull);
 }
-// Block-wide maximum of the exponents (every thread gets it).
-__device__ __forceinline__ int block_max_exponent(int e, RowQuantScratch& sc) {
+// Adds a float's exponent to a thread's largest exponent e and its smallest
+// nonzero one lo (start: e = 0, lo = 255).
+__device__ __forceinline__ void exponent_range_add(uint32_t bits, int& e, int& lo) {
+  const int x = fp32_exponent(bits);
+  e = max(e, x);
+  if (x) lo = min(lo, x);
+}
+// Block-wide largest exponent and smallest nonzero exponent of a row (every
+// thread gets both; 0 and 255 for a row of zeros): their spread picks the
+// exact-sum path directly, so a row of wide range (the FFN's ReLU^2(gate) *
+// up) does not first try window 0.
+__device__ __forceinline__ void block_exponent_range(int e, int lo, RowQuantScratch& sc, int* emax, int* emin) {
   e = __reduce_max_sync(kFullMask, e);
-  if ((threadIdx.x & 31) == 0) sc.ired[threadIdx.x >> 5] = e;
+  lo = __reduce_min_sync(kFullMask, lo);
+  if ((threadIdx.x & 31) == 0) sc.ired[threadIdx.x >> 5] = (e << 8) | lo;
   __syncthreads();
-  int m = 0;
+  int m = 0, n = 255;
   const int nw = (int)(blockDim.x >> 5);
-  for (int w = 0; w < nw; ++w) m = max(m, sc.ired[w]);
-  return m;
+  for (int w = 0; w < nw; ++w) {
+    const int v = sc.ired[w];
+    m = max(m, v >> 8);
+    n = min(n, v & 255);
+  }
+  *emax = m;
+  *emin = n;
 }
 // Rounds (A0 * 2^128 + A1 * 2^64 + A2) * 2^(2 emax - 490) to the nearest double.
 __device__ inline double windows_to_double(const U128 (&A)[3], int emax) {
@@ -221,16 +237,19 @@ __device__ inline double bucket_fold(RowQuantScratch& sc) {
 // Exact sum of squares of the K values in hs (shared memory); every thread of
 // the block calls it and gets the result.
 static __device__ double block_sq_sum_exact(const float4* hs, int K4, RowQuantScratch& sc) {
-  int e = 0;
+  int e = 0, lo = 255;
   for (int i = threadIdx.x; i < K4; i += blockDim.x) {
     const float4 h = hs[i];
-    e = max(max(fp32_exponent(__float_as_uint(h.x)), fp32_exponent(__float_as_uint(h.y))),
-            max(max(e, fp32_exponent(__float_as_uint(h.z))), fp32_exponent(__float_as_uint(h.w))));
+    exponent_range_add(__float_as_uint(h.x), e, lo);
+    exponent_range_add(__float_as_uint(h.y), e, lo);
+    exponent_range_add(__float_as_uint(h.z), e, lo);
+    exponent_range_add(__float_as_uint(h.w), e, lo);
   }
-  const int emax = block_max_exponent(e, sc);
+  int emax, emin;
+  block_exponent_range(e, lo, sc, &emax, &emin);
   if (emax == 0) return 0.0;
   double S;
-  {
+  if (emax - emin <= 31) {
     U128 W = {0, 0};
     int far = 0;
     for (int i = threadIdx.x; i < K4; i += blockDim.x) {
@@ -242,16 +261,18 @@ static __device__ double block_sq_sum_exact(const float4* hs, int K4, RowQuantSc
     }
     if (block_window0(W, far, emax, sc, &S)) return S;
   }
-  U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
-  int slow = 0;
-  for (int i = threadIdx.x; i < K4; i += blockDim.x) {
-    const float4 h = hs[i];
-    sq_window_add(__float_as_uint(h.x), emax, A, slow);
-    sq_window_add(__float_as_uint(h.y), emax, A, slow);
-    sq_window_add(__float_as_uint(h.z), emax, A, slow);
-    sq_window_add(__float_as_uint(h.w), emax, A, slow);
+  if (emax - emin <= 95) {
+    U128 A[3] = {{0, 0}, {0, 0}, {0, 0}};
+    int slow = 0;
+    for (int i = threadIdx.x; i < K4; i += blockDim.x) {
+      const float4 h = hs[i];
+      sq_window_add(__float_as_uint(h.x), emax, A, slow);
+      sq_window_add(__float_as_uint(h.y), emax, A, slow);
+      sq_window_add(__float_as_uint(h.z), emax, A, slow);
+      sq_window_add(__float_as_uint(h.w), emax, A, slow);
+    }
+    if (block_windows(A, slow, emax, sc, &S)) return S;
   }
-  if (block_windows(A, slow, emax, sc, &S)) return S;
   zero_buckets(sc);
   __syncthreads();
   for (int base = (threadIdx.x & ~31); base < K4; base += blockDim.x) {
