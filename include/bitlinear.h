@@ -170,7 +170,10 @@ bitlinear_status bitlinear_forward(const int8_t* xq, const float* x_scale, int64
 
 enum {
   BITLINEAR_ALGO_AUTO = 0,
-  BITLINEAR_ALGO_DECODE = 1,   /* CUDA-core kernel, any M */
+  BITLINEAR_ALGO_DECODE = 1,   /* the decode kernel (dp4a; the warp-level MMA for
+                                  8- or 16-token groups), K <= 65536, at most
+                                  65535 token groups (16 tokens a group, fewer
+                                  where 16 tokens of activations do not fit) */
   BITLINEAR_ALGO_PREFILL = 2,  /* tcgen05 kernel, any M: 128-token tiles */
   BITLINEAR_ALGO_BATCHED = 3,  /* tcgen05 kernel, 1 <= M <= 128: 128-row weight
                                   tiles with every token in one tile */
@@ -205,7 +208,9 @@ enum {
   BITLINEAR_FLAG_GATED = 2
 };
 
-/* bitlinear_forward with an explicit algorithm and flags (see above). */
+/* bitlinear_forward with an explicit algorithm and flags (see above).
+ * Errors: as bitlinear_forward; BITLINEAR_ERR_UNSUPPORTED for an unknown
+ * algorithm or flag bit, or a shape outside the chosen kernel's limits. */
 bitlinear_status bitlinear_forward_ex(const int8_t* xq, const float* x_scale, int64_t M,
                                       const uint8_t* packed, const float* w_scale,
                                       int64_t N, int64_t K, float* y, int32_t* acc,

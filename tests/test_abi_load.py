@@ -64,6 +64,11 @@ def test_forward_argument_errors(lib):
     assert f(A, A, 129, A, A, 64, 64, A, None, 3, 0, None) == -4           # batched past 128 tokens
     assert f(A, A, 1, A, A, 64, 64, A, None, 0, 8, None) == -4             # unknown flag
     assert f(A, A, 1 << 20, A, A, 1 << 20, 64, A, None, 0, 0, None) == -2  # M * N >= 2^40
+    # decode's grid holds at most 65535 token groups: of 16 tokens at K = 2560, of one token at
+    # K = 65536 (a group's activations stay within 64 KB of shared memory)
+    assert f(A, A, 16 * 65535 + 1, A, A, 64, 2560, A, None, 1, 0, None) == -4
+    assert f(A, A, 65535 + 1, A, A, 8, 65536, A, None, 1, 0, None) == -4
+    assert f(A, A, 1, A, A, 64, 65536 + 64, A, None, 1, 0, None) == -4   # decode past K = 65536
     assert f(A, A, 0, A, A, 64, 64, A, None, 0, 0, None) == 0              # empty batch
 
 
