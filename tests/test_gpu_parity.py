@@ -432,6 +432,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 2048, (300, 1000, 64, 7), "norm"),  # four matrices (the most one call takes), fused M = 1
     (40, 1024, (257, 100, 1000, 33), None), # four matrices on the batched kernel
     (5, 640, (500, 77, 1300, 16), "gated"), # four matrices on the decode kernel after act_quant
+    (12, 10240, (2560, 640), None),         # two matrices, 16-token MMA group, K split over 4 CTAs
+    (6, 8192, (300, 1000, 77), "norm"),     # three matrices, 8-token group, K split over 2 CTAs
     (16, 2560, (10240, 10240), None),       # 16 tokens, 20480 rows: one decode launch, MMA dots
 ])
 @pytest.mark.parametrize("ws", [False, True])
