@@ -31,8 +31,8 @@
  *    16 bytes, or a too small workspace.  M == 0 is a valid empty batch and enqueues nothing.
  *  - A failed launch returns BITLINEAR_ERR_CUDA.  Every wait inside a kernel
  *    is bounded; a wait that runs out records BITLINEAR_ERR_TIMEOUT in a
- *    per-device status word that bitlinear_device_status() reports, and the
- *    outputs that depended on it are not written.  While that word is set, a
+ *    per-device status word that bitlinear_device_status() reports, and that
+ *    launch's outputs are unspecified.  While that word is set, a
  *    decode launch whose K is split over a thread-block cluster writes no
  *    outputs at all (its CTAs learn of a peer's timeout through the word), so
  *    clear it before relying on results again.
