@@ -114,14 +114,18 @@ int auto_algo(int64_t M, int64_t N, int64_t K) {
 //   N = 2560, K = 10240:  M = 256 32.9 / 34.5, M = 512 49.3 / 41.4, M = 1024 61.2 / 65.0
 //   N = K = 2560:         M = 256 17.6 / 17.5, M = 512 19.2 / 23.3
 //   N = 1000, K = 4096, M = 200: 14.4 / 12.7;  N = K = 4096, M = 384: 28.8 / 29.4
-// so up to 512 tokens at K >= 8192 and up to 256 below; for wide outputs
-// (N = 8192, 10240) and at M = 2048 the other kernels measured faster.  Up to
-// M = 128 the batched kernel (K split inside a cluster) is within a few per
-// cent of WIDE without the pre-pass launch (BitNet-3B o / down at M = 64:
-// 10.1 / 17.4 us against 10.7 / 17.9).
+// and for wide outputs (N = 8192, 10240) and at M = 2048 the other kernels
+// measured faster.  Up to M = 128 the batched kernel (K split inside a
+// cluster) is within a few per cent of WIDE without the pre-pass launch
+// (BitNet-3B o / down at M = 64: 10.1 / 17.4 us against 10.7 / 17.9).  In a
+// layer's chain of calls WIDE pays only at long K: with q, k, v and o
+// (K = 2560) on it too, eight BitNet-3B layers took 126.0 / 133.3 / 155.7 us
+// a layer at M = 160 / 192 / 256, and 111.6 / 113.4 / 126.7 with down alone
+// on it (unchanged at M = 384 / 512, where only down qualified).  So: up to
+// 512 tokens at K >= 8192.
 bool wide_wins(int64_t M, int64_t N, int64_t K) {
   if (N > 4096 || M <= 128) return false;
-  return K >= 8192 ? M <= 512 : M <= 256;
+  return K >= 8192 && M <= 512;
 }
 
 // bitlinear_linear's single-launch path: the row quantiser keeps K fp32 values

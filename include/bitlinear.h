@@ -237,11 +237,12 @@ size_t bitlinear_forward_workspace(int64_t M, int64_t K);
  * 2-bit weight codes (into tensor memory) and bulk-copies the token tiles.
  * Results are bit-identical to every other algorithm.  BITLINEAR_ALGO_AUTO
  * follows bitlinear_forward's rule, except that it takes WIDE for narrow
- * outputs at medium token counts -- N <= 4096 and 128 < M <= 512 when
- * K >= 8192, 128 < M <= 256 otherwise -- where it measured up to 1.85x
- * faster on GB300 (BitNet-3B q/k/v/o and down, BitNet-1.3B down shapes); for
- * wide outputs, at more tokens and below 129 tokens the other kernels
- * measured faster or within a few per cent.  The other algorithms ignore the workspace.
+ * outputs of long K at medium token counts -- N <= 4096, K >= 8192 and
+ * 128 < M <= 512 -- where it measured faster on GB300 (BitNet-3B and
+ * BitNet-1.3B down shapes, alone and inside a layer's chain of calls); for
+ * shorter K (faster alone for some shapes, slower in the chain), wide outputs,
+ * more tokens and below 129 tokens the other kernels measured faster or
+ * within a few per cent.  The other algorithms ignore the workspace.
  * Errors: as bitlinear_forward_ex; BITLINEAR_ERR_WORKSPACE when
  * BITLINEAR_ALGO_WIDE is asked for without a large enough workspace;
  * BITLINEAR_ERR_ALIGN for a misaligned workspace.

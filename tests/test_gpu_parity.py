@@ -425,7 +425,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 128, (5,), None),                   # tiny
     (3, 640, (500, 77), None),              # M > 1: act_quant + one decode launch for both
     (130, 320, (257, 100), "norm"),         # tensor-core path per matrix
-    (200, 1024, (300, 1000, 2000), None),   # WIDE region (with ws): three matrices, one pre-pass
+    (160, 8192, (300, 257, 64), None),      # WIDE region (with ws): three matrices, one pre-pass
+    (200, 1024, (300, 1000, 2000), None),   # short K above 128 tokens: the tensor-core kernels
     (256, 8192, (2048,), "gated+norm"),     # a 1.3B FFN down call in the WIDE region
     (64, 8192, (2048, 300), "gated"),       # long K at M = 64: batched kernel, K split in a cluster
     (136, 8192, (1000, 300), "gated"),      # long K above 128 tokens: WIDE (with ws)
@@ -529,7 +530,8 @@ def _f32_outputs(acc, sx, sw):
     (2, 2560, 5120, False),     # two tokens quantised in every CTA (no act_quant launch), gated pairs
     (2, 2560, 10240, False),    # the same at BitNet-3B gate || up widths
     (40, 1024, 1000, False),    # batched tensor-core kernel, then the elementwise gating
-    (301, 512, 777, False),     # 128-token tiles (WIDE with a workspace); ragged M * N tail
+    (301, 512, 777, False),     # 128-token tiles; ragged M * N tail
+    (200, 8192, 640, False),    # WIDE with a workspace, then the elementwise gating
     (16, 2560, 10240, False),   # 16 tokens, 20480 rows: decode (MMA dots), gated in its epilogue
     (8, 8192, 777, False),      # long K at 8 tokens: decode with K split over a cluster, gated
     (12, 10240, 2560, False),   # long K above 8 tokens: batched tensor-core kernel, then the gating
