@@ -74,11 +74,12 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 constexpr int64_t kDecodeMaxK = 65536;
 // Tensor-core kernel: the fp32 accumulator is exact while 127 * K < 2^24.
 constexpr int64_t kPrefillMaxK = 131072;
-// AUTO, from timings on GB300 over the BitNet-3B shapes (back-to-back calls):
-//  * the decode kernel (dp4a; its work grows with every token) for a few
-//    tokens: M <= 4 always, M <= 8 (very wide outputs, N >= 32768 such as a
-//    50000-row LM head, only for K <= 4096), and M <= 16 when K < 8192 and the
-//    output is narrower;
+// AUTO, from timings on GB300 over the BitNet-3B shapes (back-to-back calls
+// and a layer's chain of calls):
+//  * the decode kernel for up to 16 tokens (K <= 32768; up to 8 tokens at
+//    longer K): dp4a in token groups of up to 4, the warp-level MMA in groups
+//    of 8 or 16 (K split over a cluster where a group's activations would
+//    exceed 64 KB);
 //  * the batched tensor-core kernel (weight rows on the MMA's M side, all
 //    tokens in one tile) for outputs up to 8192 rows up to M = 128;
 //  * the tensor-core kernel with 128-token tiles otherwise (both tensor-core
