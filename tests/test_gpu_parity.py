@@ -48,6 +48,8 @@ def test_shapes(algo, M, N, K):
 @pytest.mark.parametrize("M,N,K", [
     (3, 1, 64),         # one weight row: every 16-row tile reads a clamped row
     (4, 17, 64),        # one k-block for all warps
+    (5, 300, 64),       # one k-block on the MMA dots: most warps get no piece
+    (16, 33, 64),       # the same with two column tiles
     (9, 7, 192),        # a 16-token group (two 8-token column tiles) holding 9 tokens
     (16, 2000, 2560),   # two full column tiles; the xs rows padded to an odd multiple of 64
     (12, 640, 10240),   # long K: 16 tokens, K split over a cluster of 4 CTAs
