@@ -146,6 +146,16 @@ def test_batched_bitnet3b_m32(N, K):
     full_parity(W, x, algo=bl.ALGO_BATCHED)
 
 
+@pytest.mark.parametrize("M", [4, 5, 8, 9, 16, 17, 128, 129, 512, 513])
+def test_auto_boundaries_with_workspace(M):
+    """bitlinear_forward_ws with AUTO on both sides of every boundary of its rule at a long K
+    (K = 8192, N = 300): dp4a decode | MMA decode (8-token groups, K split over a cluster) |
+    16-token groups | the batched tensor-core kernel | WIDE | 128-token tiles."""
+    W = synth.weight(300, 8192, 800 + M)
+    x = synth.activations(M, 8192, 900 + M, outlier_seed=901)
+    full_parity(W, x, algo=bl.ALGO_AUTO, flags=bl.FLAG_PDL, workspace=True)
+
+
 @pytest.mark.parametrize("M", [1, 4, 64])
 def test_pdl_flag(M):
     W = synth.weight(2000, 640, 7)
